@@ -1,0 +1,486 @@
+#!/usr/bin/env python
+"""Throughput of the fused FP8 paged MQA-logits + per-row top-k path on GB300.
+
+One step = one pmqa_logits_topk call over one decode batch (block-table KV
+gather, FP8 q.K^T on tensor cores, relu-weighted head sum with masks, per-row
+top-k). Inputs are synthetic (synth.config_problem) and resident in HBM; L2 is
+flushed (256 MB write) before every timed step, and each step is timed with
+CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C0..C4] [--all]
+    python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Prints one JSON line (rank 0). Multi-GPU runs (torchrun) are independent
+replicas: every rank owns a full copy of the batch, no data-path collective.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens scored/sec and achieved HBM GB/s (% of GB300 peak); top-k rows/sec"
+DEFAULT_WORKLOAD = "C2"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--all", action="store_true", help="also time every workload")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    """Largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def read_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_pmqa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from a committed ncu summary,
+    or None when absent or taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def algorithmic_bytes(prob, k: int, logits_written: bool = False) -> dict:
+    import numpy as np
+
+    ctx = prob.context_lens.astype(np.int64)
+    rows = prob.bs * prob.next_n
+    parts = {
+        "kv": 132 * int(ctx.sum()),
+        "block_table": 4 * int(((ctx + prob.block_size - 1) // prob.block_size).sum()),
+        "q": int(prob.q.size),
+        "weights": 4 * rows * prob.heads,
+        "context_lens": 4 * prob.bs,
+        "topk_out": 4 * rows * k,
+    }
+    if logits_written:
+        parts["logits"] = 4 * rows * prob.max_model_len
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.gpu = gpu_index
+        self.proc = None
+        self.enabled = enabled
+
+    def start(self):
+        if not self.enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def device_problem(prob, device):
+    import torch
+
+    return dict(
+        q=torch.from_numpy(prob.q).to(device).view(torch.float8_e4m3fn),
+        kv=torch.from_numpy(prob.kv).to(device),
+        w=torch.from_numpy(prob.weights).to(device),
+        ctx=torch.from_numpy(prob.context_lens).to(device),
+        bt=torch.from_numpy(prob.block_tables).to(device),
+    )
+
+
+def time_steps(step, steps: int, flush) -> list:
+    """Per-step device times (ms) with an L2 flush before each step."""
+    import torch
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        flush()
+        e0.record()
+        step()
+        e1.record()
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
+    import torch
+
+    from sparse_attention_indexer_pmqa_gb300 import pmqa
+    from synth import config_problem
+
+    prob = config_problem(name)
+    k = prob.k
+    d = device_problem(prob, device)
+    rows = prob.rows
+    ws = pmqa.workspace(prob.bs, prob.next_n, prob.max_model_len, k, pmqa.PMQA_OP_LOGITS_TOPK,
+                        device)
+    idx = torch.empty((rows, k), dtype=torch.int32, device=device)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    def step():
+        pmqa.pmqa_logits_topk(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], prob.max_model_len, k,
+                              idx=idx, ws=ws)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    times = time_steps(step, args.steps, flush)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    status = pmqa.pmqa_read_device_status(ws)
+    if status:
+        raise RuntimeError(f"device status {status:#x} during the timed steps")
+    ms = statistics.fmean(times)
+    ms_max = max_over_ranks(ms, dist, device)
+    out = {"prob": prob, "ms": ms_max, "ms_median": statistics.median(times), "wall_s": wall,
+           "times": times}
+
+    if with_paths:
+        logits = torch.empty((rows, prob.max_model_len), dtype=torch.float32, device=device)
+        ws_l = pmqa.workspace(prob.bs, prob.next_n, prob.max_model_len, 0, pmqa.PMQA_OP_LOGITS,
+                              device)
+
+        def step_logits():
+            pmqa.pmqa_logits(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], prob.max_model_len,
+                             out=logits, ws=ws_l)
+
+        def step_topk():
+            pmqa.pmqa_topk(logits, d["ctx"], prob.next_n, k, idx=idx, ws=ws)
+
+        n = min(args.steps, 50)
+        for _ in range(3):
+            step_logits()
+            step_topk()
+        out["paths_ms"] = {
+            "pmqa_logits": statistics.fmean(time_steps(step_logits, n, flush)),
+            "pmqa_topk": statistics.fmean(time_steps(step_topk, n, flush)),
+            "pmqa_logits_topk": ms,
+        }
+        del logits
+
+    if with_e2e:
+        host = {key: v.cpu().pin_memory() for key, v in d.items()}
+        idx_h = torch.empty((rows, k), dtype=torch.int32).pin_memory()
+
+        def step_e2e():
+            for key in d:
+                d[key].copy_(host[key], non_blocking=True)
+            step()
+            idx_h.copy_(idx, non_blocking=True)
+
+        step_e2e()
+        torch.cuda.synchronize()
+        e_times = time_steps(step_e2e, args.e2e_steps, flush)
+        out["e2e_ms"] = max_over_ranks(statistics.fmean(e_times), dist, device)
+        out["h2d_bytes"] = sum(v.numel() * v.element_size() for v in host.values())
+        out["d2h_bytes"] = idx_h.numel() * idx_h.element_size()
+    return out
+
+
+def cpu_baseline(prob, min_seconds: float = 10.0, max_reps: int = 3):
+    """The oracle, as it stands, on the whole workload (logits + top-k)."""
+    import oracle
+
+    oracle.build()
+    nthreads = oracle.default_threads()
+    reps, t_total = 0, 0.0
+    while reps < max_reps and (reps == 0 or t_total < min_seconds):
+        t0 = time.perf_counter()
+        _, o64, _ = oracle.logits(prob, want64=True, nthreads=nthreads)
+        oracle.topk(o64, prob.context_lens, prob.next_n, prob.k, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        del o64
+    per = t_total / reps
+    return {"value": prob.total_ctx / per, "unit": "tokens/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"whole {prob.name} batch ({prob.total_ctx} tokens, logits + top-k), "
+                      f"{reps} repetition(s), {per:.2f} s each"}
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from synth import CONFIGS
+
+    sampler = ClockSampler(local, enabled=not args.no_clocks and rank == 0)
+    sampler.start()
+    res = bench_workload(args.workload, args, device, dist, with_e2e=True, with_paths=True)
+    clocks = sampler.stop()
+    prob = res["prob"]
+    ms = res["ms"]
+    tokens_all = sum_over_ranks(prob.total_ctx, dist, device)
+    value = tokens_all / (ms * 1e-3)
+    peak, peak_kind = read_peak()
+    ab = algorithmic_bytes(prob, prob.k)
+    achieved = ab["total"] / (res["ms"] * 1e-3) / 1e9
+    traffic = measured_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8e4m3-in/fp32-acc",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {CONFIGS[args.workload]['desc']}",
+            "bs": prob.bs, "next_n": prob.next_n, "heads": prob.heads, "head_dim": 128,
+            "block_size": prob.block_size, "sum_ctx": prob.total_ctx, "k": prob.k,
+            "max_model_len": prob.max_model_len, "seed": 0,
+            "l2": "flushed before every timed step (256 MB device write, not timed)",
+            "parallelism": f"replicas x{world}",
+        },
+        "hbm_gbs": achieved,
+        "kv_stream_gbs": ab["kv"] / (ms * 1e-3) / 1e9,
+        "topk_rows_per_s": world * prob.rows / (ms * 1e-3),
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+            "kernel": "pmqa_main_kernel<64,true> (fused logits + top-k)",
+            "algorithmic_bytes_per_launch": ab,
+        },
+        "e2e": {
+            "value": tokens_all / (res["e2e_ms"] * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": res["h2d_bytes"], "d2h_bytes_per_step": res["d2h_bytes"],
+            "note": "every input (q, whole KV pool, weights, lengths, tables) copied from "
+                    "pinned host memory and the top-k indices read back, each step",
+        },
+        "gpu_launches": args.steps,
+        "paths_ms": res.get("paths_ms"),
+        "ms_median": res["ms_median"],
+    }
+    if clocks:
+        line["clocks"] = clocks
+    if args.all:
+        per = {}
+        for wl in CONFIGS:
+            if wl == args.workload:
+                r = res
+            else:
+                r = bench_workload(wl, args, device, dist, with_e2e=False, with_paths=True)
+            p = r["prob"]
+            b = algorithmic_bytes(p, p.k)
+            per[wl] = {"ms": r["ms"], "tokens_per_s": p.total_ctx / (r["ms"] * 1e-3),
+                       "gbs": b["total"] / (r["ms"] * 1e-3) / 1e9,
+                       "frac": b["total"] / (r["ms"] * 1e-3) / 1e9 / peak,
+                       "paths_ms": r.get("paths_ms")}
+        line["workloads"] = per
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(prob)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    """The CPU oracle on the same workload: each step scores one request of the
+    batch (its logits rows and their top-k), in request order."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from synth import CONFIGS, Problem, config_problem
+
+    oracle.build()
+    prob = config_problem(args.workload)
+    nthreads = oracle.default_threads()
+
+    def step(s):
+        i = s % prob.bs
+        sub = Problem(
+            q=np.ascontiguousarray(prob.q[i:i + 1]), kv=prob.kv,
+            weights=np.ascontiguousarray(prob.weights[i * prob.next_n:(i + 1) * prob.next_n]),
+            context_lens=prob.context_lens[i:i + 1].copy(),
+            block_tables=np.ascontiguousarray(prob.block_tables[i:i + 1]), bs=1,
+            next_n=prob.next_n, heads=prob.heads, block_size=prob.block_size,
+            max_model_len=prob.max_model_len, k=prob.k, name=prob.name)
+        _, o64, _ = oracle.logits(sub, want64=True, nthreads=nthreads)
+        oracle.topk(o64, sub.context_lens, sub.next_n, sub.k, nthreads=nthreads)
+        return int(sub.context_lens[0])
+
+    for s in range(args.warmup):
+        step(s)
+    tokens, t0 = 0, time.perf_counter()
+    for s in range(args.steps):
+        tokens += step(args.warmup + s)
+    dt = time.perf_counter() - t0
+    value = tokens / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {CONFIGS[args.workload]['desc']}",
+                   "bs": prob.bs, "next_n": prob.next_n, "heads": prob.heads,
+                   "block_size": prob.block_size, "k": prob.k,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                         "sample": "each step: one request of the batch, in order "
+                                   "(its logits rows + top-k)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

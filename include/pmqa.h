@@ -1,0 +1,151 @@
+/*
+ * pmqa.h -- C ABI of libpmqa: the FP8 paged MQA-logits indexer and its per-row
+ * top-k, as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * What is computed. Sources: the page "[Bug] aiter ops triton attention pa"
+ * (stepcodex.com issue mirror), section "Minimal reproduction" (the reference
+ * function `torch_ref` and the `test` driver); the page "[Bugfix][Hardware][AMD]
+ * Fix last_page_len calculation in AITER MLA decode" (vLLM PR 31282), section
+ * "Comparison with Other Backends" (tokens held by a request's last page).
+ *
+ *   For request i < bs, draft row j < next_n (row r = i*next_n + j) and
+ *   logical token t:
+ *     valid(r, t)  <=>  t < ctx_i  and  t <= ctx_i - next_n + j
+ *     phys         =   block_tables[i][t / P] * P + t % P
+ *     k_t          =   kv_cache[phys][0..127] as fp8 e4m3fn
+ *     s_t          =   fp32 whose little-endian bytes are kv_cache[phys][128..131]
+ *     logits[r][t] =   sum_h weights[r][h] * relu(s_t * dot(q[i][j][h], k_t))
+ *                      if valid(r, t), else -inf, for 0 <= t < max_model_len
+ *   Top-k of row r: the positions of the min(k, valid_len(r)) largest logits
+ *   among t < valid_len(r) = clamp(ctx_i - next_n + j + 1, 0, ctx_i); remaining
+ *   slots hold -1. The order of positions within a row is unspecified; among
+ *   equal values any choice is returned. The last page of a request holds
+ *   ((ctx_i - 1) mod P) + 1 tokens; its other slots are never read.
+ *
+ * Memory. Every pointer is a DEVICE pointer owned by the caller. The library
+ * allocates nothing, keeps no global state between calls, never synchronises
+ * the stream (except pmqa_read_device_status) and enqueues its work on the
+ * given stream. Calls that share one workspace must not overlap on the GPU.
+ *
+ * Errors. Functions return PMQA_OK (0) or a negative PMQA_ERR_* code; on an
+ * error nothing has been enqueued. Faults the host cannot see (a block table
+ * entry outside the pool, a context longer than max_model_len or than the
+ * table covers, a pipeline wait that ran out) never trap: the kernel skips the
+ * access (a bad table entry reads as zeros), records a PMQA_DEV_* bit in the
+ * workspace status word and finishes; pmqa_read_device_status reports it.
+ */
+#ifndef PMQA_H
+#define PMQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *pmqa_stream_t;
+
+enum {
+    PMQA_OK = 0,
+    PMQA_ERR_INVALID_ARG = -1,  /* null pointer, negative size, misalignment, k < 1 */
+    PMQA_ERR_UNSUPPORTED = -2,  /* head_dim != 128, heads not in {16,32,64,128},
+                                   next_n not in 1..4, k too large for the kernel */
+    PMQA_ERR_WORKSPACE = -3,    /* workspace smaller than pmqa_workspace_bytes */
+    PMQA_ERR_CUDA = -4,         /* a CUDA runtime call or a launch failed */
+    PMQA_ERR_DEVICE = -5        /* reported by pmqa_read_device_status only */
+};
+
+/* Bits of the device status word. */
+#define PMQA_DEV_BAD_BLOCK_ID 0x1u /* a block table entry outside [0, num_blocks) */
+#define PMQA_DEV_BAD_CONTEXT 0x2u  /* ctx < 0, ctx > max_model_len, or ctx > P * max_blocks_per_seq;
+                                      the kernel clamps it */
+#define PMQA_DEV_TIMEOUT 0x4u      /* a pipeline wait exceeded its limit; results are invalid */
+#define PMQA_DEV_OVERFLOW 0x8u     /* top-k candidate storage exceeded; results are invalid */
+
+/* Workspace-size selector for pmqa_workspace_bytes. */
+enum { PMQA_OP_LOGITS = 0, PMQA_OP_TOPK = 1, PMQA_OP_LOGITS_TOPK = 2 };
+
+/*
+ * One decode-step problem, in the argument order of the reference function
+ * (q, kv_cache, weights, context_lens, block_tables, max_model_len) plus sizes.
+ *   q             fp8 e4m3fn [bs, next_n, heads, head_dim], contiguous, 16-byte aligned
+ *   kv_cache      uint8 [num_blocks, block_size, head_dim + 4], contiguous, 4-byte aligned:
+ *                 per token head_dim fp8 bytes then a little-endian fp32 scale
+ *   weights       fp32 [bs * next_n, heads], contiguous, 16-byte aligned
+ *   context_lens  int32 [bs]
+ *   block_tables  int32 [bs, max_blocks_per_seq], row-major; only the first
+ *                 ceil(ctx_i / block_size) entries of row i are read
+ */
+typedef struct pmqa_problem {
+    const void *q;
+    const void *kv_cache;
+    const float *weights;
+    const int32_t *context_lens;
+    const int32_t *block_tables;
+    int32_t bs;
+    int32_t next_n;
+    int32_t heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t max_blocks_per_seq;
+    int32_t max_model_len;
+    int64_t num_blocks;
+} pmqa_problem;
+
+/*
+ * Bytes of device workspace an operation needs for rows = bs * next_n rows of
+ * width max_model_len and top-k size k (k is ignored for PMQA_OP_LOGITS).
+ * Returns 0 for invalid arguments. The workspace must be 256-byte aligned and
+ * zero-filled before its first use (pmqa_workspace_init); every call leaves it
+ * zero-filled again except for the status word.
+ */
+size_t pmqa_workspace_bytes(int32_t bs, int32_t next_n, int32_t max_model_len, int32_t k, int op);
+
+/* Zero-fill a workspace (cudaMemsetAsync on the stream). */
+int pmqa_workspace_init(void *ws, size_t ws_bytes, pmqa_stream_t stream);
+
+/*
+ * Logits, the definition above. logits: fp32 [bs * next_n, max_model_len],
+ * 4-byte aligned; every entry of every row is written (-inf outside the mask),
+ * so no caller pre-fill is needed.
+ */
+int pmqa_logits(const pmqa_problem *p, float *logits, void *ws, size_t ws_bytes,
+                pmqa_stream_t stream);
+
+/*
+ * Per-row top-k of existing logits rows. logits: fp32 [bs * next_n, max_model_len];
+ * only t < valid_len(r) is read (entries beyond are ignored whatever they hold).
+ * idx: int32 [bs * next_n, k], -1 past min(k, valid_len(r)).
+ * vals: fp32 [bs * next_n, k] or NULL; the logits at idx (-inf where idx is -1).
+ */
+int pmqa_topk(const float *logits, const int32_t *context_lens, int32_t bs, int32_t next_n,
+              int32_t max_model_len, int32_t k, int32_t *idx, float *vals, void *ws,
+              size_t ws_bytes, pmqa_stream_t stream);
+
+/*
+ * Fused logits + top-k in one pass over the KV cache: the logits rows need not
+ * be written to memory. idx and vals as for pmqa_topk; logits may be NULL, or
+ * a [bs * next_n, max_model_len] buffer that then receives the full logits.
+ */
+int pmqa_logits_topk(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals, float *logits,
+                     void *ws, size_t ws_bytes, pmqa_stream_t stream);
+
+/*
+ * Synchronise the stream, return the device status bits recorded since the
+ * last read (>= 0) and clear them, or a negative PMQA_ERR_* code.
+ */
+int pmqa_read_device_status(void *ws, pmqa_stream_t stream);
+
+/* Static text for a return code. */
+const char *pmqa_status_string(int code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pmqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PMQA_H */

@@ -1,0 +1,220 @@
+"""ctypes binding of libpmqa (include/pmqa.h). Argument marshalling only.
+
+Functions carry the C names. Tensors are torch CUDA tensors; torch supplies
+device memory and the current stream, every step of the computation runs in
+the library's kernels. There is no CPU path: if the library is missing,
+``load()`` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+PMQA_OK = 0
+PMQA_ERR_INVALID_ARG = -1
+PMQA_ERR_UNSUPPORTED = -2
+PMQA_ERR_WORKSPACE = -3
+PMQA_ERR_CUDA = -4
+PMQA_ERR_DEVICE = -5
+
+PMQA_DEV_BAD_BLOCK_ID = 0x1
+PMQA_DEV_BAD_CONTEXT = 0x2
+PMQA_DEV_TIMEOUT = 0x4
+PMQA_DEV_OVERFLOW = 0x8
+
+PMQA_OP_LOGITS = 0
+PMQA_OP_TOPK = 1
+PMQA_OP_LOGITS_TOPK = 2
+
+EXPORTED = (
+    "pmqa_workspace_bytes", "pmqa_workspace_init", "pmqa_logits", "pmqa_topk",
+    "pmqa_logits_topk", "pmqa_read_device_status", "pmqa_status_string", "pmqa_version",
+)
+
+
+class PmqaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {code} ({status_string(code)})")
+
+
+class Problem(ctypes.Structure):
+    """Mirror of struct pmqa_problem."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("kv_cache", ctypes.c_void_p),
+        ("weights", ctypes.c_void_p),
+        ("context_lens", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p),
+        ("bs", ctypes.c_int32),
+        ("next_n", ctypes.c_int32),
+        ("heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("max_model_len", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int64),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libpmqa.so (built by build.build()); raise if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise FileNotFoundError(
+            f"{path} is missing: build it with sparse_attention_indexer_pmqa_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    PP = ctypes.POINTER(Problem)
+    sig = {
+        "pmqa_workspace_bytes": ([I32, I32, I32, I32, ctypes.c_int], SZ),
+        "pmqa_workspace_init": ([V, SZ, V], ctypes.c_int),
+        "pmqa_logits": ([PP, V, V, SZ, V], ctypes.c_int),
+        "pmqa_topk": ([V, V, I32, I32, I32, I32, V, V, V, SZ, V], ctypes.c_int),
+        "pmqa_logits_topk": ([PP, I32, V, V, V, V, SZ, V], ctypes.c_int),
+        "pmqa_read_device_status": ([V, V], ctypes.c_int),
+        "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "pmqa_version": ([], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    del I64
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().pmqa_status_string(code).decode()
+
+
+def _stream(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(code: int, what: str) -> None:
+    if code != PMQA_OK:
+        raise PmqaError(code, what)
+
+
+def make_problem(q, kv_cache, weights, context_lens, block_tables, max_model_len: int) -> Problem:
+    """Fill a pmqa_problem from tensors shaped as in the C header."""
+    bs, next_n, heads, head_dim = q.shape
+    num_blocks, block_size = kv_cache.shape[0], kv_cache.shape[1]
+    assert kv_cache.shape[-1] == head_dim + 4, "kv rows hold head_dim fp8 bytes + fp32 scale"
+    for t in (q, kv_cache, weights, context_lens, block_tables):
+        assert t.is_cuda and t.is_contiguous()
+    return Problem(
+        q=q.data_ptr(), kv_cache=kv_cache.data_ptr(), weights=weights.data_ptr(),
+        context_lens=context_lens.data_ptr(), block_tables=block_tables.data_ptr(),
+        bs=bs, next_n=next_n, heads=heads, head_dim=head_dim, block_size=block_size,
+        max_blocks_per_seq=block_tables.shape[1], max_model_len=max_model_len,
+        num_blocks=num_blocks)
+
+
+def pmqa_workspace_bytes(bs: int, next_n: int, max_model_len: int, k: int, op: int) -> int:
+    return int(load().pmqa_workspace_bytes(bs, next_n, max_model_len, k, op))
+
+
+def workspace(bs: int, next_n: int, max_model_len: int, k: int, op: int, device=None, stream=None):
+    """A zero-initialised workspace tensor for the given operation."""
+    import torch
+
+    n = pmqa_workspace_bytes(bs, next_n, max_model_len, k, op)
+    if n == 0:
+        raise PmqaError(PMQA_ERR_INVALID_ARG, "pmqa_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    pmqa_workspace_init(ws, stream=stream)
+    return ws
+
+
+def pmqa_workspace_init(ws, stream=None) -> None:
+    _check(load().pmqa_workspace_init(_ptr(ws), ws.numel(), _stream(stream)),
+           "pmqa_workspace_init")
+
+
+def pmqa_logits(q, kv_cache, weights, context_lens, block_tables, max_model_len: int, *,
+                out=None, ws=None, stream=None):
+    """fp32 logits [bs*next_n, max_model_len]."""
+    import torch
+
+    p = make_problem(q, kv_cache, weights, context_lens, block_tables, max_model_len)
+    rows = p.bs * p.next_n
+    if out is None:
+        out = torch.empty((rows, max_model_len), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(p.bs, p.next_n, max_model_len, 0, PMQA_OP_LOGITS, q.device, stream)
+    _check(load().pmqa_logits(ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "pmqa_logits")
+    return out
+
+
+def pmqa_topk(logits, context_lens, next_n: int, k: int, *, idx=None, vals=None,
+              want_vals: bool = False, ws=None, stream=None):
+    """int32 positions [rows, k] (and fp32 values) of each row's top-k."""
+    import torch
+
+    rows, mml = logits.shape
+    bs = context_lens.shape[0]
+    assert rows == bs * next_n
+    if idx is None:
+        idx = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
+    if vals is None and want_vals:
+        vals = torch.empty((rows, k), dtype=torch.float32, device=logits.device)
+    if ws is None:
+        ws = workspace(bs, next_n, mml, k, PMQA_OP_TOPK, logits.device, stream)
+    _check(load().pmqa_topk(_ptr(logits), _ptr(context_lens), bs, next_n, mml, k, _ptr(idx),
+                            _ptr(vals), _ptr(ws), ws.numel(), _stream(stream)), "pmqa_topk")
+    return (idx, vals) if want_vals or vals is not None else idx
+
+
+def pmqa_logits_topk(q, kv_cache, weights, context_lens, block_tables, max_model_len: int,
+                     k: int, *, idx=None, vals=None, logits=None, want_vals: bool = False,
+                     ws=None, stream=None):
+    """Fused logits + top-k; returns idx, or (idx, vals) when values are asked for."""
+    import torch
+
+    p = make_problem(q, kv_cache, weights, context_lens, block_tables, max_model_len)
+    rows = p.bs * p.next_n
+    if idx is None:
+        idx = torch.empty((rows, k), dtype=torch.int32, device=q.device)
+    if vals is None and want_vals:
+        vals = torch.empty((rows, k), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(p.bs, p.next_n, max_model_len, k, PMQA_OP_LOGITS_TOPK, q.device, stream)
+    _check(load().pmqa_logits_topk(ctypes.byref(p), k, _ptr(idx), _ptr(vals), _ptr(logits),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "pmqa_logits_topk")
+    return (idx, vals) if want_vals or vals is not None else idx
+
+
+def pmqa_read_device_status(ws, stream=None) -> int:
+    rc = load().pmqa_read_device_status(_ptr(ws), _stream(stream))
+    if rc < 0:
+        raise PmqaError(rc, "pmqa_read_device_status")
+    return rc
+
+
+def pmqa_version() -> int:
+    return int(load().pmqa_version())

@@ -1,0 +1,89 @@
+"""Comparison rules between the CUDA path and the oracle.
+
+Logits: the -inf pattern must match exactly; every finite entry must satisfy
+|gpu - oracle| <= 1e-3 * (1 + sum_h |w_h| |x_h|) (the oracle's tolerance array).
+Top-k: per row the selected set has exactly min(k, valid_len) distinct positions
+inside the window and -1 after; it equals the oracle's set except for positions
+whose oracle logit lies within the tolerance of the oracle's k-th value (for a
+swapped pair both entries' errors count, so the bound is twice the larger of
+their tolerances).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def valid_len(ctx: int, nn: int, j: int) -> int:
+    return max(0, min(ctx - nn + j + 1, ctx))
+
+
+def check_logits(gpu: np.ndarray, ref: np.ndarray, tol: np.ndarray) -> float:
+    """Returns the largest |error| / tolerance over finite entries."""
+    assert gpu.shape == ref.shape
+    ninf_g, ninf_r = np.isneginf(gpu), np.isneginf(ref)
+    bad = np.argwhere(ninf_g != ninf_r)
+    assert bad.size == 0, f"-inf pattern differs at {bad[:5].tolist()} (of {len(bad)})"
+    fin = ~ninf_r
+    assert np.all(np.isfinite(gpu[fin])), "non-finite logits where the oracle is finite"
+    if not fin.any():
+        return 0.0
+    err = np.abs(gpu[fin].astype(np.float64) - ref[fin].astype(np.float64))
+    ratio = err / tol[fin]
+    worst = float(ratio.max())
+    assert worst <= 1.0, f"logit error {worst:.3g} x tolerance (max abs {err.max():.3g})"
+    return worst
+
+
+def check_topk_rows(idx: np.ndarray, ref64: np.ndarray, tol: np.ndarray, ctx, nn: int, k: int,
+                    vals: np.ndarray | None = None) -> int:
+    """Check GPU top-k against oracle values; returns the number of tie swaps."""
+    ctx = np.asarray(ctx)
+    swaps = 0
+    for r in range(idx.shape[0]):
+        i, j = divmod(r, nn)
+        n = valid_len(int(ctx[i]), nn, j)
+        ke = min(k, n)
+        sel = idx[r, :ke]
+        assert np.all(idx[r, ke:] == -1), f"row {r}: slots past k_eff not -1"
+        assert np.all((sel >= 0) & (sel < n)), f"row {r}: position outside the window"
+        assert len(np.unique(sel)) == ke, f"row {r}: repeated positions"
+        if ke == 0:
+            continue
+        row = ref64[r, :n]
+        order = np.lexsort((np.arange(n), -row))
+        ref_set = order[:ke]
+        kth = row[ref_set[-1]]
+        g, o = set(sel.tolist()), set(ref_set.tolist())
+        extra, missing = g - o, o - g
+        # A swap needs the two entries' GPU errors to bridge their gap, so each
+        # swapped position lies within the sum of two entry tolerances of the
+        # k-th value.
+        if extra:
+            tmax = max(float(tol[r, p]) for p in extra | missing | {int(ref_set[-1])})
+            for p in extra:
+                assert row[p] >= kth - 2 * tmax, f"row {r}: chose {p} ({row[p]}) below k-th {kth}"
+            for p in missing:
+                assert row[p] <= kth + 2 * tmax, f"row {r}: missed {p} ({row[p]}) above k-th {kth}"
+        swaps += len(extra)
+        if vals is not None:
+            assert np.all(np.isneginf(vals[r, ke:])), f"row {r}: padding values not -inf"
+            err = np.abs(vals[r, :ke].astype(np.float64) - row[sel])
+            assert np.all(err <= tol[r, sel]), f"row {r}: returned values off by {err.max()}"
+    return swaps
+
+
+def check_topk_exact(idx: np.ndarray, vals32: np.ndarray, ctx, nn: int, k: int) -> None:
+    """Top-k of given fp32 rows: the chosen values equal the oracle's as a multiset."""
+    ctx = np.asarray(ctx)
+    for r in range(idx.shape[0]):
+        i, j = divmod(r, nn)
+        n = valid_len(int(ctx[i]), nn, j)
+        ke = min(k, n)
+        sel = idx[r, :ke]
+        assert np.all(idx[r, ke:] == -1)
+        assert np.all((sel >= 0) & (sel < n))
+        assert len(np.unique(sel)) == ke
+        want = np.sort(vals32[r, :n])[::-1][:ke]
+        got = np.sort(vals32[r, sel])[::-1]
+        assert np.array_equal(got, want), f"row {r}: selected values differ from the top-{ke}"

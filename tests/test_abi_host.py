@@ -1,0 +1,128 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports every
+function include/pmqa.h declares, and rejects bad arguments before touching
+the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_indexer_pmqa_gb300 import build, pmqa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "pmqa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pmqa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pmqa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(pmqa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert pmqa.pmqa_version() == 100
+    assert pmqa.status_string(0) == "ok"
+    assert pmqa.status_string(-3) == "workspace too small"
+    assert pmqa.status_string(12345) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    assert pmqa.pmqa_workspace_bytes(4, 2, 1000, 2048, pmqa.PMQA_OP_LOGITS) == 256
+    n = pmqa.pmqa_workspace_bytes(4, 2, 1000, 2048, pmqa.PMQA_OP_LOGITS_TOPK)
+    assert n == 256 + 256 + 256 + 8 * 1000 * 8
+    assert pmqa.pmqa_workspace_bytes(4, 2, 1000, 2048, pmqa.PMQA_OP_TOPK) == n
+    assert pmqa.pmqa_workspace_bytes(-1, 1, 10, 1, 0) == 0
+    assert pmqa.pmqa_workspace_bytes(1, 1, 10, 1, 7) == 0
+
+
+def _problem(**kw):
+    # fake, suitably aligned device addresses: argument checks run before any CUDA call
+    base = dict(q=0x10000, kv_cache=0x20000, weights=0x30000, context_lens=0x40000,
+                block_tables=0x50000, bs=2, next_n=1, heads=64, head_dim=128, block_size=1,
+                max_blocks_per_seq=64, max_model_len=64, num_blocks=128)
+    base.update(kw)
+    return pmqa.Problem(**base)
+
+
+WS = ctypes.c_void_p(0x100000)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=64), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(heads=48), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(next_n=5), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(next_n=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(bs=-1), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(block_size=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(max_model_len=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(q=None), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(q=0x10004), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(weights=0x30008), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(kv_cache=0x20002), pmqa.PMQA_ERR_INVALID_ARG),
+])
+def test_problem_validation(lib, kw, code):
+    p = _problem(**kw)
+    assert lib.pmqa_logits(ctypes.byref(p), ctypes.c_void_p(0x60000), WS, 1 << 20, None) == code
+    assert lib.pmqa_logits_topk(ctypes.byref(p), 16, ctypes.c_void_p(0x70000), None, None, WS,
+                                1 << 20, None) == code
+
+
+def test_null_problem_and_outputs(lib):
+    assert lib.pmqa_logits(None, ctypes.c_void_p(0x60000), WS, 1 << 20, None) == -1
+    p = _problem()
+    assert lib.pmqa_logits(ctypes.byref(p), None, WS, 1 << 20, None) == -1
+    assert lib.pmqa_logits_topk(ctypes.byref(p), 16, None, None, None, WS, 1 << 20, None) == -1
+    assert lib.pmqa_logits_topk(ctypes.byref(p), 0, ctypes.c_void_p(0x70000), None, None, WS,
+                                1 << 20, None) == -1
+
+
+def test_workspace_checks(lib):
+    p = _problem()
+    out = ctypes.c_void_p(0x60000)
+    assert lib.pmqa_logits(ctypes.byref(p), out, WS, 255, None) == pmqa.PMQA_ERR_WORKSPACE
+    assert lib.pmqa_logits(ctypes.byref(p), out, ctypes.c_void_p(0x100010), 1 << 20, None) == -1
+    need = pmqa.pmqa_workspace_bytes(2, 1, 64, 16, pmqa.PMQA_OP_LOGITS_TOPK)
+    assert lib.pmqa_logits_topk(ctypes.byref(p), 16, ctypes.c_void_p(0x70000), None, None, WS,
+                                need - 1, None) == pmqa.PMQA_ERR_WORKSPACE
+
+
+def test_topk_validation(lib):
+    L = ctypes.c_void_p(0x10000)
+    C = ctypes.c_void_p(0x20000)
+    I = ctypes.c_void_p(0x30000)
+    need = pmqa.pmqa_workspace_bytes(2, 1, 64, 8, pmqa.PMQA_OP_TOPK)
+    assert lib.pmqa_topk(L, C, 2, 1, 64, 0, I, None, WS, need, None) == -1
+    assert lib.pmqa_topk(L, C, 2, 0, 64, 8, I, None, WS, need, None) == -1
+    assert lib.pmqa_topk(L, C, 2, 1, 64, 8, I, None, WS, need - 1, None) == -3
+    assert lib.pmqa_topk(None, C, 2, 1, 64, 8, I, None, WS, need, None) == -1
+    assert lib.pmqa_topk(L, C, 2, 1, 64, 8, ctypes.c_void_p(0x30002), None, WS, need, None) == -1
+    assert lib.pmqa_topk(L, C, 2, 1, 64, 1 << 20, I, None, WS, need, None) == -2
+
+
+def test_empty_batch_is_a_no_op(lib):
+    p = _problem(bs=0, q=None)
+    assert lib.pmqa_logits(ctypes.byref(p), ctypes.c_void_p(0x60000), WS, 1 << 20, None) == 0
+    assert lib.pmqa_topk(None, None, 0, 1, 64, 8, None, None, WS, 1 << 20, None) == 0
+
+
+def test_workspace_init_checks(lib):
+    assert lib.pmqa_workspace_init(None, 1024, None) == -1
+    assert lib.pmqa_workspace_init(ctypes.c_void_p(0x100004), 1024, None) == -1
+    assert lib.pmqa_read_device_status(None, None) == -1

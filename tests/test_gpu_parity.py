@@ -1,0 +1,213 @@
+"""GPU parity: libpmqa (through its C ABI) against the CPU oracle.
+
+Logits: -inf pattern bit-exact, finite entries within 1e-3 (1 + sum_h |w_h||x_h|).
+Top-k: index sets equal up to swaps inside the tolerance of the k-th value.
+Sizes span several 128-token tiles with ragged tails; the five workloads run at
+their full sizes in the launch configuration the benchmark times.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import config_problem, make_problem
+from synth.inputs import random_logits
+from tests.parity import check_logits, check_topk_exact, check_topk_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(prob):
+    return dict(
+        q=torch.from_numpy(prob.q).cuda().view(torch.float8_e4m3fn),
+        kv=torch.from_numpy(prob.kv).cuda(),
+        w=torch.from_numpy(prob.weights).cuda(),
+        ctx=torch.from_numpy(prob.context_lens).cuda(),
+        bt=torch.from_numpy(prob.block_tables).cuda(),
+    )
+
+
+def gpu_logits(L, prob, d=None, ws=None):
+    d = d or dev(prob)
+    out = L.pmqa_logits(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], prob.max_model_len, ws=ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def gpu_fused(L, prob, k, d=None, ws=None, logits=None):
+    d = d or dev(prob)
+    idx, vals = L.pmqa_logits_topk(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], prob.max_model_len,
+                                   k, want_vals=True, ws=ws, logits=logits)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), vals.cpu().numpy()
+
+
+def oracle_all(prob):
+    out, o64, tol = oracle.logits(prob, want64=True, want_tol=True)
+    return out, o64, tol
+
+
+SMALL = [
+    # bs, next_n, heads, block_size, context lengths, max_model_len, table
+    (1, 1, 32, 1, [300], 512, "identity"),
+    (3, 1, 64, 1, [1, 127, 129], 256, "perm"),
+    (2, 1, 16, 1, [200, 0], 256, "perm"),
+    (4, 2, 64, 1, [1, 2, 255, 513], 640, "perm"),
+    (2, 3, 32, 16, [33, 400], 512, "perm"),
+    (3, 4, 64, 1, [3, 4, 700], 768, "perm"),
+    (2, 4, 128, 64, [130, 1000], 1024, "perm"),
+    (2, 2, 128, 1, [640, 129], 640, "perm"),
+    (5, 1, 128, 64, [64, 65, 127, 1, 300], 320, "perm"),
+    (2, 4, 16, 1, [77, 5], 128, "perm"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"bs{c[0]}nn{c[1]}H{c[2]}P{c[3]}")
+def test_logits_small(cuda_lib, case):
+    bs, nn, H, P, ctx, mml, table = case
+    prob = make_problem(bs, nn, H, P, ctx, mml, seed=sum(ctx) + H, table=table, extra_blocks=2)
+    ref, _, tol = oracle_all(prob)
+    check_logits(gpu_logits(cuda_lib, prob), ref, tol)
+
+
+@pytest.mark.parametrize("k", [1, 7, 100, 2048])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"bs{c[0]}nn{c[1]}H{c[2]}P{c[3]}")
+def test_fused_topk_small(cuda_lib, case, k):
+    bs, nn, H, P, ctx, mml, table = case
+    prob = make_problem(bs, nn, H, P, ctx, mml, seed=sum(ctx) + H + 1, table=table, extra_blocks=2)
+    ref, r64, tol = oracle_all(prob)
+    logits = torch.empty((bs * nn, mml), dtype=torch.float32, device="cuda")
+    idx, vals = gpu_fused(cuda_lib, prob, k, logits=logits)
+    check_topk_rows(idx, r64, tol, prob.context_lens, nn, k, vals=vals)
+    check_logits(logits.cpu().numpy(), ref, tol)
+
+
+@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("k", [1, 5, 300, 2048])
+def test_standalone_topk_exact(cuda_lib, k, ties):
+    ctx, nn, mml = [0, 1, 7, 129, 3000, 5000], 2, 5120
+    vals = random_logits(len(ctx) * nn, mml, seed=k, ties=ties)
+    t = torch.from_numpy(vals).cuda()
+    c = torch.tensor(ctx, dtype=torch.int32, device="cuda")
+    idx, got = cuda_lib.pmqa_topk(t, c, nn, k, want_vals=True)
+    idx, got = idx.cpu().numpy(), got.cpu().numpy()
+    check_topk_exact(idx, vals, ctx, nn, k)
+    ke_rows = [min(k, max(0, min(cx - nn + j + 1, cx))) for cx in ctx for j in range(nn)]
+    for r, ke in enumerate(ke_rows):
+        assert np.array_equal(got[r, :ke], vals[r, idx[r, :ke]])
+    # the oracle's own selection agrees on the chosen values
+    ref = oracle.topk(vals.astype(np.float64), ctx, nn, k)
+    for r, ke in enumerate(ke_rows):
+        assert np.array_equal(np.sort(vals[r, ref[r, :ke]]), np.sort(vals[r, idx[r, :ke]]))
+
+
+def test_standalone_topk_of_oracle_logits(cuda_lib):
+    prob = make_problem(4, 2, 32, 1, [5000, 2049, 2048, 17], 6144, seed=3)
+    out, _, _ = oracle_all(prob)
+    t = torch.from_numpy(out).cuda()
+    c = torch.from_numpy(prob.context_lens).cuda()
+    idx = cuda_lib.pmqa_topk(t, c, 2, 2048).cpu().numpy()
+    check_topk_exact(idx, out, prob.context_lens, 2, 2048)
+
+
+# ------------------------------------------------------------- invariants
+
+
+def test_permutation_invariance_bit_exact(cuda_lib):
+    prob = make_problem(3, 2, 64, 1, [900, 130, 2000], 2048, seed=21, table="identity",
+                        extra_blocks=5)
+    a = gpu_logits(cuda_lib, prob)
+    perm = np.random.default_rng(5).permutation(prob.num_blocks)
+    kv2 = np.empty_like(prob.kv)
+    kv2[perm] = prob.kv
+    prob.kv = kv2
+    prob.block_tables = np.where(prob.block_tables >= 0,
+                                 perm[np.maximum(prob.block_tables, 0)], -1).astype(np.int32)
+    b = gpu_logits(cuda_lib, prob)
+    assert np.array_equal(a, b)
+
+
+def test_context_2048_to_2049_bit_exact(cuda_lib):
+    prob = make_problem(1, 1, 32, 1, [2049], 4096, seed=42, table="identity", extra_blocks=16)
+    a = gpu_logits(cuda_lib, prob)
+    prob.context_lens[:] = 2048
+    b = gpu_logits(cuda_lib, prob)
+    assert np.array_equal(a[0, :2048], b[0, :2048])
+    assert np.isneginf(b[0, 2048]) and np.isfinite(a[0, 2048])
+    idx, _ = gpu_fused(cuda_lib, prob, 2048)
+    assert np.array_equal(np.sort(idx[0]), np.arange(2048))
+    prob.context_lens[:] = 2049
+    ref, r64, tol = oracle_all(prob)
+    idx, vals = gpu_fused(cuda_lib, prob, 2048)
+    check_topk_rows(idx, r64, tol, [2049], 1, 2048, vals=vals)
+
+
+def test_workspace_is_reusable(cuda_lib):
+    """Calls leave the workspace clean: repeated and reshaped calls agree."""
+    prob = make_problem(4, 2, 64, 1, [3000, 5000, 100, 2500], 5120, seed=8)
+    d = dev(prob)
+    ws = cuda_lib.workspace(4, 2, 5120, 512, cuda_lib.PMQA_OP_LOGITS_TOPK)
+    i1, v1 = gpu_fused(cuda_lib, prob, 512, d=d, ws=ws)
+    i2, v2 = gpu_fused(cuda_lib, prob, 512, d=d, ws=ws)
+    assert np.array_equal(np.sort(i1, axis=1), np.sort(i2, axis=1))
+    prob.context_lens[:] = [2999, 17, 100, 4000]
+    d = dev(prob)
+    i3, v3 = gpu_fused(cuda_lib, prob, 512, d=d, ws=ws)
+    _, r64, tol = oracle_all(prob)
+    check_topk_rows(i3, r64, tol, prob.context_lens, 2, 512, vals=v3)
+    assert cuda_lib.pmqa_read_device_status(ws) == 0
+
+
+def test_bad_table_entry_sets_status_without_fault(cuda_lib):
+    prob = make_problem(2, 1, 64, 1, [300, 200], 512, seed=9)
+    prob.block_tables[1, 10] = prob.num_blocks + 7
+    d = dev(prob)
+    ws = cuda_lib.workspace(2, 1, 512, 0, cuda_lib.PMQA_OP_LOGITS)
+    out = cuda_lib.pmqa_logits(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], 512, ws=ws)
+    st = cuda_lib.pmqa_read_device_status(ws)
+    assert st & cuda_lib.PMQA_DEV_BAD_BLOCK_ID
+    assert cuda_lib.pmqa_read_device_status(ws) == 0  # cleared by the read
+    o = out.cpu().numpy()
+    prob.block_tables[1, 10] = prob.block_tables[1, 11]
+    ref, _, tol = oracle_all(prob)
+    assert np.array_equal(o[0], gpu_logits(cuda_lib, prob)[0])
+    assert o[1, 10] == 0.0  # the bad token reads as zeros
+
+
+def test_context_longer_than_max_model_len_is_flagged(cuda_lib):
+    prob = make_problem(1, 1, 32, 1, [100], 128, seed=10)
+    d = dev(prob)
+    d["ctx"][0] = 200
+    ws = cuda_lib.workspace(1, 1, 128, 0, cuda_lib.PMQA_OP_LOGITS)
+    cuda_lib.pmqa_logits(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], 128, ws=ws)
+    assert cuda_lib.pmqa_read_device_status(ws) & cuda_lib.PMQA_DEV_BAD_CONTEXT
+
+
+# ------------------------------------------------------------- full workloads
+
+
+@pytest.fixture(scope="module", params=["C0", "C1", "C2", "C3", "C4"])
+def workload(request):
+    prob = config_problem(request.param)
+    ref, r64, tol = oracle_all(prob)
+    return prob, ref, r64, tol
+
+
+def test_workload_logits(cuda_lib, workload):
+    prob, ref, _, tol = workload
+    check_logits(gpu_logits(cuda_lib, prob), ref, tol)
+
+
+def test_workload_fused_topk(cuda_lib, workload):
+    prob, _, r64, tol = workload
+    idx, vals = gpu_fused(cuda_lib, prob, prob.k)
+    check_topk_rows(idx, r64, tol, prob.context_lens, prob.next_n, prob.k, vals=vals)
+
+
+def test_workload_standalone_topk(cuda_lib, workload):
+    prob, ref, _, _ = workload
+    t = torch.from_numpy(ref).cuda()
+    c = torch.from_numpy(prob.context_lens).cuda()
+    idx = cuda_lib.pmqa_topk(t, c, prob.next_n, prob.k).cpu().numpy()
+    check_topk_exact(idx, ref, prob.context_lens, prob.next_n, prob.k)
