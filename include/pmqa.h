@@ -23,9 +23,10 @@
  *   ((ctx_i - 1) mod P) + 1 tokens; its other slots are never read.
  *
  * Memory. Every pointer is a DEVICE pointer owned by the caller. The library
- * allocates nothing, keeps no global state between calls, never synchronises
- * the stream (except pmqa_read_device_status) and enqueues its work on the
- * given stream. Calls that share one workspace must not overlap on the GPU.
+ * allocates nothing, keeps no global state between calls (the one exception is
+ * the built-in scratch of pmqa_logits_topk_noalloc), never synchronises the
+ * stream (except pmqa_read_device_status) and enqueues its work on the given
+ * stream. Calls that share one workspace must not overlap on the GPU.
  *
  * Errors. Functions return PMQA_OK (0) or a negative PMQA_ERR_* code; on an
  * error nothing has been enqueued. Faults the host cannot see (a block table
@@ -131,6 +132,28 @@ int pmqa_topk(const float *logits, const int32_t *context_lens, int32_t bs, int3
  */
 int pmqa_logits_topk(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals, float *logits,
                      void *ws, size_t ws_bytes, pmqa_stream_t stream);
+
+/*
+ * pmqa_logits_topk without a caller-supplied workspace. The pages have no
+ * counterpart to this entry point: it exists for callers that are given device
+ * buffers for their inputs and outputs but cannot allocate device memory of
+ * their own (for example a plugin inside a host program that owns the whole
+ * device-memory pool and offers no allocation hook, or a latency-critical loop
+ * that must not call cudaMalloc, which may synchronise the device).
+ * The workspace is a 32 MiB array that the library keeps in device memory on
+ * every GPU where it is loaded, until the process exits. Problems whose
+ * pmqa_workspace_bytes(bs, next_n, max_model_len, k, PMQA_OP_LOGITS_TOPK)
+ * exceeds 32 MiB return PMQA_ERR_WORKSPACE with nothing enqueued.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before capturing
+ * any stream. Every call shares the one array and clears its counters at the
+ * start, so calls that overlap on the GPU (other streams, other threads) race
+ * and must be serialised by the caller. Device-side status bits of these calls
+ * are not reported. Allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library call.
+ */
+int pmqa_logits_topk_noalloc(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
+                             float *logits, pmqa_stream_t stream);
 
 /*
  * Synchronise the stream, return the device status bits recorded since the

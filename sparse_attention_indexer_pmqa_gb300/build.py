@@ -1,8 +1,9 @@
 """Build libpmqa.so in-tree with nvcc for sm_103a (GB300).
 
-Five translation units compile in parallel (the C ABI plus one per supported
-head count) and link into one shared library with the CUDA runtime linked
-statically, so the library loads on a machine without a GPU too.
+Six translation units compile in parallel (the C ABI, the allocation-free
+entry point and one per supported head count) and link into one shared library
+with the CUDA runtime linked statically, so the library loads on a machine
+without a GPU too.
 """
 
 from __future__ import annotations
@@ -30,7 +31,8 @@ def _nvcc() -> str:
 def _sources():
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".cu"))]
     deps.append(os.path.join(INCLUDE, "pmqa.h"))
-    units = [("pmqa_api", os.path.join(CSRC, "pmqa_api.cu"), [])]
+    units = [("pmqa_api", os.path.join(CSRC, "pmqa_api.cu"), []),
+             ("pmqa_noalloc", os.path.join(CSRC, "pmqa_noalloc.cu"), [])]
     for h in HEADS:
         units.append((f"pmqa_main_h{h}", os.path.join(CSRC, "pmqa_main_inst.cu"),
                       [f"-DPMQA_HEADS={h}"]))

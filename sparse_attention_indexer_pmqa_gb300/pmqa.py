@@ -31,7 +31,8 @@ PMQA_OP_LOGITS_TOPK = 2
 
 EXPORTED = (
     "pmqa_workspace_bytes", "pmqa_workspace_init", "pmqa_logits", "pmqa_topk",
-    "pmqa_logits_topk", "pmqa_read_device_status", "pmqa_status_string", "pmqa_version",
+    "pmqa_logits_topk", "pmqa_logits_topk_noalloc", "pmqa_read_device_status",
+    "pmqa_status_string", "pmqa_version",
 )
 
 
@@ -86,6 +87,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pmqa_logits": ([PP, V, V, SZ, V], ctypes.c_int),
         "pmqa_topk": ([V, V, I32, I32, I32, I32, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_logits_topk": ([PP, I32, V, V, V, V, SZ, V], ctypes.c_int),
+        "pmqa_logits_topk_noalloc": ([PP, I32, V, V, V, V], ctypes.c_int),
         "pmqa_read_device_status": ([V, V], ctypes.c_int),
         "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pmqa_version": ([], ctypes.c_int),
@@ -207,6 +209,17 @@ def pmqa_logits_topk(q, kv_cache, weights, context_lens, block_tables, max_model
     _check(load().pmqa_logits_topk(ctypes.byref(p), k, _ptr(idx), _ptr(vals), _ptr(logits),
                                    _ptr(ws), ws.numel(), _stream(stream)), "pmqa_logits_topk")
     return (idx, vals) if want_vals or vals is not None else idx
+
+
+def pmqa_logits_topk_noalloc(q, kv_cache, weights, context_lens, block_tables,
+                             max_model_len: int, k: int, *, idx, vals=None, logits=None,
+                             stream=None):
+    """Fused logits + top-k with the library's built-in device scratch; the
+    caller passes every output buffer, nothing is allocated."""
+    p = make_problem(q, kv_cache, weights, context_lens, block_tables, max_model_len)
+    _check(load().pmqa_logits_topk_noalloc(ctypes.byref(p), k, _ptr(idx), _ptr(vals), _ptr(logits),
+                                           _stream(stream)), "pmqa_logits_topk_noalloc")
+    return idx
 
 
 def pmqa_read_device_status(ws, stream=None) -> int:
