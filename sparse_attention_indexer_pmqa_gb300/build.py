@@ -39,19 +39,25 @@ def _sources():
     return units, deps
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          defines=(), out: str | None = None) -> str:
+    """Compile and link; ``defines`` (e.g. "PMQA_MAX_STAGES=6") and ``out``
+    produce a separately named tuning build."""
     units, deps = _sources()
+    lib = out or LIB
+    build_dir = BUILD if out is None else out + ".objs"
     newest = max(os.path.getmtime(d) for d in deps + [__file__])
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= newest:
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
+    dflags = [f"-D{d}" for d in defines]
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     procs, objs = [], []
     for name, src, defs in units:
-        obj = os.path.join(BUILD, name + ".o")
+        obj = os.path.join(build_dir, name + ".o")
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *FLAGS, *defs, *extra, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *dflags, *defs, *extra, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((name, subprocess.Popen(cmd, stdout=subprocess.PIPE,
@@ -65,13 +71,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             failed.append(name)
     if failed:
         raise RuntimeError("nvcc failed for " + ", ".join(failed))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -1,6 +1,7 @@
 // pmqa_api.cu -- the C ABI of include/pmqa.h: argument checks, workspace and
-// shared-memory layout, kernel launches. No allocation, no synchronisation
-// (except pmqa_read_device_status), no state kept between calls.
+// shared-memory layout, TMA descriptor, kernel launches. No allocation, no
+// synchronisation (except pmqa_read_device_status), no state kept between calls.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -8,55 +9,62 @@
 
 #include "../../include/pmqa.h"
 #include "pmqa_main.cuh"
-#include "pmqa_topk_kernel.cuh"
+#include "pmqa_select.cuh"
 
 namespace pmqa {
-cudaError_t launch_main_h16(const MainArgs &, bool, int, int, cudaStream_t);
-cudaError_t launch_main_h32(const MainArgs &, bool, int, int, cudaStream_t);
-cudaError_t launch_main_h64(const MainArgs &, bool, int, int, cudaStream_t);
-cudaError_t launch_main_h128(const MainArgs &, bool, int, int, cudaStream_t);
+cudaError_t launch_main_h16(const MainArgs &, int, int, cudaStream_t);
+cudaError_t launch_main_h32(const MainArgs &, int, int, cudaStream_t);
+cudaError_t launch_main_h64(const MainArgs &, int, int, cudaStream_t);
+cudaError_t launch_main_h128(const MainArgs &, int, int, cudaStream_t);
+size_t fused_ws_zero_bytes(int bs, int next_n);
 }  // namespace pmqa
 
 using namespace pmqa;
 
 namespace {
 
-constexpr int kVersion = 100;          // 0.1.0
+constexpr int kVersion = 200;  // 0.2.0
 constexpr uint32_t kMaxDynSmem = 232448 - 1024;
 constexpr uint32_t kMinMainSmem = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr size_t kWsAlign = 256;
+constexpr int kSelChunk = 8192;  // positions per selection CTA
+// Tuning constants of the main kernel (compile time; -D overrides in tuning builds).
+#ifndef PMQA_MAX_STAGING
+#define PMQA_MAX_STAGING 8
+#endif
+#ifndef PMQA_OP_STAGES
+#define PMQA_OP_STAGES 2
+#endif
+#ifndef PMQA_L2_POLICY
+#define PMQA_L2_POLICY 0
+#endif
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Workspace: status word | per-row counters | per-row histograms | tie lists
+// | compact logits (fused only). Everything before the tie lists must be zero
+// when a call starts; every call leaves it zero again (status word aside).
 struct WsLayout {
-    size_t arrive, cand_cnt, cand, total;
+    size_t sel_cnt, tie_cnt, arrive, hist, ties, clogits, total;
 };
 
 bool ws_layout(long long rows, long long mml, int op, WsLayout *L)
 {
-    if (rows < 0 || mml < 1)
+    if (rows < 0 || mml < 1 || op < PMQA_OP_LOGITS || op > PMQA_OP_LOGITS_TOPK)
         return false;
-    L->arrive = kWsAlign;
     if (op == PMQA_OP_LOGITS) {
-        L->cand_cnt = L->cand = L->total = kWsAlign;
+        L->sel_cnt = L->tie_cnt = L->arrive = L->hist = L->ties = L->clogits = L->total = kWsAlign;
         return true;
     }
-    L->cand_cnt = L->arrive + align_up((size_t)rows * 4, kWsAlign);
-    L->cand = L->cand_cnt + align_up((size_t)rows * 4, kWsAlign);
-    L->total = L->cand + (size_t)rows * (size_t)mml * 8;
+    const size_t r4 = align_up((size_t)rows * 4, kWsAlign);
+    L->sel_cnt = kWsAlign;
+    L->tie_cnt = L->sel_cnt + r4;
+    L->arrive = L->tie_cnt + r4;
+    L->hist = L->arrive + r4;
+    L->ties = L->hist + (size_t)rows * kHistBins * 4;
+    L->clogits = L->ties + align_up((size_t)rows * (size_t)mml * 4, kWsAlign);
+    L->total = op == PMQA_OP_LOGITS_TOPK ? L->clogits + (size_t)rows * (size_t)mml * 4 : L->clogits;
     return true;
-}
-
-TopkWs ws_view(void *ws, const WsLayout &L, long long mml)
-{
-    uint8_t *b = static_cast<uint8_t *>(ws);
-    TopkWs w;
-    w.status = reinterpret_cast<uint32_t *>(b);
-    w.arrive = reinterpret_cast<uint32_t *>(b + L.arrive);
-    w.cand_cnt = reinterpret_cast<uint32_t *>(b + L.cand_cnt);
-    w.cand = reinterpret_cast<uint2 *>(b + L.cand);
-    w.row_cap = mml;
-    return w;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -92,8 +100,9 @@ int check_problem(const pmqa_problem *p)
     return PMQA_OK;
 }
 
-// Shared-memory and pipeline layout of the main kernel.
-bool main_layout(int heads, int nn, bool fused, int k, MainArgs &a)
+// Shared-memory and pipeline layout of the main kernel: the deepest staging
+// ring that fits, preferring two query slots at equal depth.
+bool main_layout(int heads, int nn, bool with_hist, MainArgs &a)
 {
     const int N = heads * nn;
     a.N = N;
@@ -107,44 +116,114 @@ bool main_layout(int heads, int nn, bool fused, int k, MainArgs &a)
     a.cols = cols;
     a.NBUF = std::min(8, 512 / cols);
     a.tmem_cols = a.NBUF * cols;
-    for (int S = 4; S >= 2; --S) {
+    a.S = PMQA_OP_STAGES;
+    for (int SG = PMQA_MAX_STAGING; SG >= 3; --SG) {
         for (int QS = 2; QS >= 1; --QS) {
-            uint32_t off = (uint32_t)S * kStageBytes;
+            const int RS = a.S + a.NBUF;
+            uint32_t off = (uint32_t)SG * kPRWarps * kWarpSlotBytes;
+            a.off_op = off;
+            off += (uint32_t)a.S * kStageBytes;
             a.off_q = off;
             off += (uint32_t)(QS * N * kHeadDim);
             a.off_w = off;
             off += (uint32_t)(QS * N * 4);
             off = (uint32_t)align_up(off, 16);
-            const int RS = S + a.NBUF;
             a.off_scale = off;
-            off += (uint32_t)RS * 512u;
+            off += (uint32_t)RS * kTileTokens * 4u;
+            a.off_meta = off;
+            off += (uint32_t)(kPRWarps * SG * 32);
+            off = (uint32_t)align_up(off, 16);
             a.off_bar = off;
-            off += (uint32_t)(2 * S + 2 * a.NBUF + 2 * QS + RS + 1) * 8u;
-            off = (uint32_t)align_up(off, 128);
-            a.off_cand = off;
-            int cap = 0;
-            if (fused) {
-                const long fixed = 64 + (long)sizeof(WgScratch);
-                const long avail = (long)kMaxDynSmem - 1024 - (long)off - a.E * fixed;
-                if (avail <= 0)
-                    continue;
-                cap = (int)std::min<long>(avail / ((long)a.E * a.rpw * 8), 4096) & ~127;
-                if (cap < k + 256)
-                    continue;
-                off += (uint32_t)(a.E * ((long)a.rpw * cap * 8 + fixed));
-            }
-            uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
+            off += (uint32_t)(2 * a.S + 2 * a.NBUF + 2 * QS + RS + 1) * 8u;
+            off = (uint32_t)align_up(off, 16);
+            a.off_hist = off;
+            if (with_hist)
+                off += (uint32_t)(a.E * a.rpw * kHistBins * 4);
+            const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
             if (total > kMaxDynSmem)
                 continue;
-            a.S = S;
+            a.SG = SG;
             a.QS = QS;
             a.RS = RS;
-            a.cap = cap;
             a.smem_bytes = total;
             return true;
         }
     }
     return false;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;  // driver entry point, looked up once
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// q viewed as [bs * N rows, 128 bytes]; box [128 bytes, q_box rows]; 128B swizzle.
+// q_box = N / ceil(N / 256) <= 256 rows, so whole boxes cover one request exactly.
+bool encode_q_map(CUtensorMap *m, const void *q, long long rows, int q_box)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+    const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)q_box};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(q), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+SelectArgs select_args(const float *logits, const int32_t *ctx, int bs, int nn, int mml, int k,
+                       int32_t *idx, float *vals, void *ws, const WsLayout &L)
+{
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    SelectArgs s{};
+    s.logits = logits;
+    s.ctx_lens = ctx;
+    s.bs = bs;
+    s.nn = nn;
+    s.mml = mml;
+    s.k = k;
+    s.idx = idx;
+    s.vals = vals;
+    s.status = reinterpret_cast<uint32_t *>(b);
+    s.sel_cnt = reinterpret_cast<uint32_t *>(b + L.sel_cnt);
+    s.tie_cnt = reinterpret_cast<uint32_t *>(b + L.tie_cnt);
+    s.arrive = reinterpret_cast<uint32_t *>(b + L.arrive);
+    s.hist = reinterpret_cast<uint32_t *>(b + L.hist);
+    s.ties = reinterpret_cast<int32_t *>(b + L.ties);
+    s.chunk = kSelChunk;
+    s.splits = (mml + kSelChunk - 1) / kSelChunk;
+    return s;
+}
+
+int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
+{
+    const long long rows = (long long)s.bs * s.nn;
+    if (rows == 0)
+        return PMQA_OK;
+    if (rows > 65535)
+        return PMQA_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)s.splits, (unsigned)rows);
+    if (with_hist_pass)
+        pmqa_hist_kernel<<<grid, kSelThreads, 0, stream>>>(s);
+    pmqa_select_kernel<<<grid, kSelThreads, 0, stream>>>(s);
+    return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }
 
 int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals, float *logits,
@@ -172,49 +251,81 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     if (ws_bytes < L.total)
         return PMQA_ERR_WORKSPACE;
     MainArgs a{};
-    if (!main_layout(p->heads, p->next_n, fused, k, a))
+    if (!main_layout(p->heads, p->next_n, fused, a))
+        return PMQA_ERR_UNSUPPORTED;
+    if (fused && rows > 65535)
         return PMQA_ERR_UNSUPPORTED;
     if (p->bs == 0)
         return PMQA_OK;
+    const int nbox = (a.N + 255) / 256;
+    a.q_box = a.N / nbox;
+    if (a.q_box * nbox != a.N || a.q_box % 8 != 0)
+        return PMQA_ERR_UNSUPPORTED;
+    if (!encode_q_map(&a.tmap_q, p->q, rows * p->heads, a.q_box))
+        return PMQA_ERR_CUDA;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
     a.q = static_cast<const uint8_t *>(p->q);
     a.kv = static_cast<const uint8_t *>(p->kv_cache);
     a.w = p->weights;
     a.ctx_lens = p->context_lens;
     a.bt = p->block_tables;
     a.num_blocks = p->num_blocks;
+    a.pool_bytes = p->num_blocks * (long long)p->block_size * kKvRowBytes;
     a.bs = p->bs;
     a.nn = p->next_n;
     a.P = p->block_size;
     a.W = p->max_blocks_per_seq;
     a.mml = p->max_model_len;
     a.logits = logits;
-    a.k = fused ? k : 0;
-    a.out_idx = idx;
-    a.out_vals = vals;
-    a.ws = ws_view(ws, L, p->max_model_len);
+    a.status = reinterpret_cast<uint32_t *>(wsb);
+    a.l2_policy = PMQA_L2_POLICY;
+    float *sel_src = logits;
+    if (fused) {
+        a.hist = reinterpret_cast<uint32_t *>(wsb + L.hist);
+        if (!logits) {
+            a.clogits = reinterpret_cast<float *>(wsb + L.clogits);
+            sel_src = a.clogits;
+        }
+    }
     int sms = 0;
     if ((rc = sm_count(&sms)) != PMQA_OK)
         return rc;
     const int threads = 32 * (kFirstEpiWarp + 4 * a.E);
     cudaError_t e;
     switch (p->heads) {
-    case 16: e = launch_main_h16(a, fused, sms, threads, stream); break;
-    case 32: e = launch_main_h32(a, fused, sms, threads, stream); break;
-    case 64: e = launch_main_h64(a, fused, sms, threads, stream); break;
-    default: e = launch_main_h128(a, fused, sms, threads, stream); break;
+    case 16: e = launch_main_h16(a, sms, threads, stream); break;
+    case 32: e = launch_main_h32(a, sms, threads, stream); break;
+    case 64: e = launch_main_h64(a, sms, threads, stream); break;
+    default: e = launch_main_h128(a, sms, threads, stream); break;
     }
-    return e == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
+    if (e != cudaSuccess)
+        return PMQA_ERR_CUDA;
+    if (!fused)
+        return PMQA_OK;
+    const SelectArgs s = select_args(sel_src, p->context_lens, p->bs, p->next_n, p->max_model_len,
+                                     k, idx, vals, ws, L);
+    return launch_select(s, false, stream);
 }
 
 }  // namespace
+
+namespace pmqa {
+// Bytes at the start of a fused-call workspace that must be zero when a call starts.
+size_t fused_ws_zero_bytes(int bs, int next_n)
+{
+    WsLayout L;
+    if (!ws_layout((long long)bs * next_n, 1, PMQA_OP_LOGITS_TOPK, &L))
+        return 0;
+    return L.ties;
+}
+}  // namespace pmqa
 
 extern "C" {
 
 size_t pmqa_workspace_bytes(int32_t bs, int32_t next_n, int32_t max_model_len, int32_t k, int op)
 {
     (void)k;
-    if (bs < 0 || next_n < 1 || max_model_len < 1 || op < PMQA_OP_LOGITS ||
-        op > PMQA_OP_LOGITS_TOPK)
+    if (bs < 0 || next_n < 1 || max_model_len < 1)
         return 0;
     WsLayout L;
     if (!ws_layout((long long)bs * next_n, max_model_len, op, &L))
@@ -255,40 +366,16 @@ int pmqa_topk(const float *logits, const int32_t *context_lens, int32_t bs, int3
         return PMQA_ERR_INVALID_ARG;
     if (ws_bytes < L.total)
         return PMQA_ERR_WORKSPACE;
+    if (rows > 65535)
+        return PMQA_ERR_UNSUPPORTED;
     if (bs == 0)
         return PMQA_OK;
     if (!logits || !context_lens || !idx || !aligned(logits, 4) || !aligned(context_lens, 4) ||
         !aligned(idx, 4) || (vals && !aligned(vals, 4)))
         return PMQA_ERR_INVALID_ARG;
-    const long long cap = std::max<long long>(4096, (long long)align_up((size_t)k + 1024, 128));
-    const size_t smem = sizeof(WgScratch) + 16 + (size_t)cap * 8;
-    if (smem > kMaxDynSmem)
-        return PMQA_ERR_UNSUPPORTED;
-    TopkArgs a{};
-    a.logits = logits;
-    a.ctx_lens = context_lens;
-    a.bs = bs;
-    a.nn = next_n;
-    a.mml = max_model_len;
-    a.k = k;
-    a.idx = idx;
-    a.vals = vals;
-    a.ws = ws_view(ws, L, max_model_len);
-    a.cap = (int)cap;
-    int sms = 0;
-    int rc = sm_count(&sms);
-    if (rc != PMQA_OK)
-        return rc;
-    if (cudaFuncSetAttribute(pmqa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-        return PMQA_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pmqa_topk_kernel, 128, smem) !=
-            cudaSuccess ||
-        per_sm < 1)
-        return PMQA_ERR_CUDA;
-    pmqa_topk_kernel<<<sms * std::min(per_sm, 4), 128, smem, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
+    const SelectArgs s =
+        select_args(logits, context_lens, bs, next_n, max_model_len, k, idx, vals, ws, L);
+    return launch_select(s, true, stream);
 }
 
 int pmqa_read_device_status(void *ws, pmqa_stream_t stream)

@@ -7,50 +7,66 @@
 //
 // One CTA per SM walks a contiguous range of (request, 128-token tile) work
 // items, balanced by tile count over all requests. Warp roles:
-//   warp 0        allocates TMEM; lane 0 issues tcgen05.mma
-//   warps 1..4    gather: block-table lookup, then per token one warp-wide
-//                 4-byte cp.async of the 128 fp8 bytes straight into the
-//                 128B-swizzled K-major operand tile, plus the fp32 scale
-//   warps 5..     epilogue work groups (1 or 2 x 4 warps): tcgen05.ld of the
-//                 fp32 scores (one token per thread, all heads of a row in
-//                 registers), relu * weight head sum, scale, mask, store;
-//                 optionally the streaming top-k of pmqa_topk_wg.cuh.
+//   warp 0      allocates TMEM; lane 0 issues tcgen05.mma
+//   warp 1      lane 0 loads each request's q (TMA, 128B swizzle) and weights
+//               (bulk copy) into a query slot
+//   warps 2..5  gather + repack, 32 tokens of every tile each: the block table
+//               is read three tiles ahead; every 132-byte row is fetched as its
+//               16-byte aligned 144-byte window with 16-byte cp.async into a
+//               per-warp staging ring (several tiles in flight); once a tile
+//               has landed the warp moves each row's 32 fp8 words (shifted by
+//               the row's 0/4/8/12-byte misalignment) into the 128B-swizzled
+//               K-major operand tile and its fp32 scale into a scale ring
+//   warps 6..   epilogue work groups (1 or 2 x 4 warps): tcgen05.ld of the
+//               fp32 scores (one token per thread, all heads of a row in
+//               registers), relu * weight head sum, scale, mask; full logits
+//               rows and/or the compact logits + an 11-bit key histogram per
+//               row for the selection kernel.
 // The MMA computes D[token][(j,h)] = K_tile[128 x 128] * Q[(j,h) x 128]^T with
 // tokens as M = 128 and N = next_n * heads, fp8 e4m3 in, fp32 accumulate in
-// TMEM. Pipelines: S shared-memory K stages, NBUF TMEM accumulators, QS query
-// slots, a scale ring of S + NBUF entries; all handshakes are mbarriers.
+// TMEM (NBUF accumulators). All hand-offs are mbarriers; waits are bounded.
 #pragma once
+
+#include <cuda.h>
 
 #include <cstdint>
 
 #include "pmqa_ptx.cuh"
-#include "pmqa_topk_wg.cuh"
 
 namespace pmqa {
 
+constexpr uint32_t kFullMask = 0xFFFFFFFFu;
 constexpr int kTileTokens = 128;
 constexpr int kHeadDim = 128;
 constexpr int kKvRowBytes = kHeadDim + 4;
-constexpr int kProducerWarps = 4;
-constexpr int kFirstEpiWarp = 1 + kProducerWarps;
-constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16 KB
+constexpr int kPRWarps = 4;
+constexpr int kFirstPRWarp = 2;
+constexpr int kFirstEpiWarp = kFirstPRWarp + kPRWarps;
+constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16 KB operand tile
+constexpr uint32_t kWinBytes = 144;                        // aligned window of one row
+constexpr uint32_t kWarpSlotBytes = 32 * kWinBytes;        // one warp's rows of a tile
+constexpr int kHistBins = 2048;                            // top 11 bits of the order key
+constexpr int kHistShift = 21;
 
 struct MainArgs {
+    CUtensorMap tmap_q;  // q as [bs * N rows, 128 bytes], 128B swizzle, box [128, q_box]
     const uint8_t *q;
     const uint8_t *kv;
     const float *w;
     const int32_t *ctx_lens;
     const int32_t *bt;
     long long num_blocks;
+    long long pool_bytes;  // num_blocks * block_size * 132
     int bs, nn, P, W, mml;
-    float *logits;  // may be null in the fused kernel
-    int k;
-    int32_t *out_idx;
-    float *out_vals;
-    TopkWs ws;
+    float *logits;     // full rows [rows, mml], or null
+    float *clogits;    // compact logits (valid positions only) for the selection, or null
+    uint32_t *hist;    // per-row key histograms [rows, 2048], or null
+    uint32_t *status;
+    int l2_policy;     // KV stream: 0 evict_first, 1 evict_normal, 2 evict_last
     // shared-memory / pipeline layout, computed on the host
-    int N, S, NBUF, QS, RS, cols, tmem_cols, E, rpw, cap;
-    uint32_t off_q, off_w, off_scale, off_bar, off_cand, smem_bytes;
+    int N, S, SG, NBUF, QS, RS, cols, tmem_cols, E, rpw;
+    int q_box;  // rows per q TMA box: N / ceil(N / 256)
+    uint32_t off_op, off_q, off_w, off_scale, off_meta, off_bar, off_hist, smem_bytes;
 };
 
 struct CtaCtl {
@@ -61,6 +77,13 @@ struct CtaCtl {
     int abort;
     uint32_t tmem_base;
 };
+
+// f32 -> u32 with a > b  <=>  key(a) > key(b); -0 is folded onto +0.
+__device__ __forceinline__ uint32_t f32_order_key(float f)
+{
+    uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 __device__ __forceinline__ int clamp_ctx(int c, long long lim)
 {
@@ -80,10 +103,9 @@ __device__ __forceinline__ int valid_len(int ctx, int nn, int j)
     return v < 0 ? 0 : (v > ctx ? ctx : v);
 }
 
-// Split `total` units (per-item counts given by len_of) evenly over the grid.
-// Every thread calls it; results land in c.start/c.count/c.i0/c.m0.
+// Split the items' total length evenly over the grid (every thread calls).
 template <class LenFn>
-static __device__ void balance_schedule(int n_items, LenFn len_of, CtaCtl &c)
+__device__ void balance_schedule(int n_items, LenFn len_of, CtaCtl &c)
 {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
     long long loc = 0;
@@ -162,16 +184,13 @@ struct TileIter {
     }
 };
 
-// sfull: the scale ring slot of a tile has landed. The epilogue reads the
-// scales written by the gather warps, so it acquires them from those warps'
-// own barrier rather than through the MMA thread.
 struct Bars {
-    uint64_t *full, *empty, *tfull, *tempty, *qfull, *qempty, *sfull, *done;
+    uint64_t *op_full, *op_empty, *tfull, *tempty, *qfull, *qempty, *sfull, *done;
     __device__ Bars(const MainArgs &a, uint8_t *smem)
     {
-        full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
-        empty = full + a.S;
-        tfull = empty + a.S;
+        op_full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
+        op_empty = op_full + a.S;
+        tfull = op_empty + a.S;
         tempty = tfull + a.NBUF;
         qfull = tempty + a.NBUF;
         qempty = qfull + a.QS;
@@ -188,116 +207,194 @@ __device__ __forceinline__ void cp_async_wait_upto(int n)
     case 2: cp_async_wait_group<2>(); break;
     case 3: cp_async_wait_group<3>(); break;
     case 4: cp_async_wait_group<4>(); break;
-    default: cp_async_wait_group<5>(); break;
+    case 5: cp_async_wait_group<5>(); break;
+    case 6: cp_async_wait_group<6>(); break;
+    case 7: cp_async_wait_group<7>(); break;
+    case 8: cp_async_wait_group<8>(); break;
+    case 9: cp_async_wait_group<9>(); break;
+    default: cp_async_wait_group<10>(); break;
     }
 }
 
 __device__ __forceinline__ void raise_abort(const MainArgs &a, CtaCtl &c)
 {
     c.abort = 1;
-    atomicOr(a.ws.status, 0x4u);
+    atomicOr(a.status, 0x4u);
 }
 
-// ---------------------------------------------------------------- gather
+// ---------------------------------------------------------------- query loader
 
-static __device__ void producer_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int pw)
+static __device__ void qload_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
 {
     const Bars B(a, smem);
-    const int lane = threadIdx.x & 31, ptid = pw * 32 + lane;
-    const uint64_t pol = l2_evict_first_policy();
-    const int N = a.N, lag = a.S - 1;
-    const int count = (int)c.count;
+    const int N = a.N, count = (int)c.count;
     TileIter it;
     it.init(a, c.i0, c.m0);
-    uint32_t req = 0, hist_first = 0, hist_qs = 0;
-    int kk = 0;
-    bool ok = true;
-    for (; kk < count; ++kk) {
-        const int s = kk % a.S;
-        if (!mbar_wait(&B.empty[s], ((kk / a.S) & 1) ^ 1, &c.abort)) {
-            ok = false;
-            break;
-        }
-        const bool first = kk == 0 || it.m == 0;
-        uint32_t qs = 0;
-        if (first) {
-            qs = req % a.QS;
+    uint32_t req = 0;
+    for (int kk = 0; kk < count; ++kk) {
+        if (kk == 0 || it.m == 0) {
+            const uint32_t qs = req % a.QS;
             if (!mbar_wait(&B.qempty[qs], ((req / a.QS) & 1) ^ 1, &c.abort)) {
-                ok = false;
-                break;
+                raise_abort(a, c);
+                return;
             }
-            // q rows (j, h) of request i into the swizzled B-operand slot
-            const uint8_t *qsrc = a.q + (long long)it.i * N * kHeadDim;
+            mbar_arrive_expect_tx(&B.qfull[qs], (uint32_t)N * (kHeadDim + 4));
             const uint32_t qdst = smem_u32(smem + a.off_q + qs * (uint32_t)N * kHeadDim);
-            for (int ch = ptid; ch < N * 8; ch += 128) {
-                const int n = ch >> 3, cc = ch & 7;
-                cp_async_16(qdst + (n >> 3) * 1024 + (n & 7) * 128 + ((cc ^ (n & 7)) << 4),
-                            qsrc + n * kHeadDim + cc * 16);
-            }
-            const float *wsrc = a.w + (long long)it.i * N;
-            const uint32_t wdst = smem_u32(smem + a.off_w + qs * (uint32_t)N * 4);
-            for (int ch = ptid; ch < N / 4; ch += 128)
-                cp_async_16(wdst + ch * 16, wsrc + ch * 4);
+            // boxes of q_box rows tile the request's N rows exactly (N = nbox * q_box)
+            for (int nc = 0; nc * a.q_box < N; ++nc)
+                tma_load_2d(qdst + nc * a.q_box * kHeadDim, &a.tmap_q, 0, it.i * N + nc * a.q_box,
+                            &B.qfull[qs]);
+            bulk_load(smem_u32(smem + a.off_w + qs * (uint32_t)N * 4), a.w + (long long)it.i * N,
+                      (uint32_t)N * 4, &B.qfull[qs]);
             ++req;
-        }
-        // this warp's 32 tokens of the tile
-        const int t = it.m * kTileTokens + pw * 32 + lane;
-        const uint8_t *rowp = a.kv;
-        uint32_t nb = 0;
-        if (t < it.ctx) {
-            const int blk = t / a.P;
-            const int off = t - blk * a.P;
-            const int b = __ldg(a.bt + (long long)it.i * a.W + blk);
-            if (b >= 0 && (long long)b < a.num_blocks) {
-                rowp = a.kv + ((long long)b * a.P + off) * kKvRowBytes;
-                nb = 4;
-            } else {
-                atomicOr(a.ws.status, 0x1u);
-            }
-        }
-        const uint32_t sbase = smem_u32(smem + (uint32_t)s * kStageBytes);
-        const uint32_t chunk_off = (uint32_t)(lane & 3) * 4;
-        const uint32_t chunk_id = (uint32_t)lane >> 2;
-#pragma unroll 8
-        for (int jj = 0; jj < 32; ++jj) {
-            const uint8_t *src = reinterpret_cast<const uint8_t *>(
-                __shfl_sync(kFullMask, reinterpret_cast<unsigned long long>(rowp), jj));
-            const uint32_t n = __shfl_sync(kFullMask, nb, jj);
-            const uint32_t r = (uint32_t)(pw * 32 + jj);
-            cp_async_4(sbase + r * 128 + ((chunk_id ^ (r & 7)) << 4) + chunk_off, src + lane * 4,
-                       n, pol);
-        }
-        const int sri = kk % a.RS;
-        cp_async_4(smem_u32(smem + a.off_scale + sri * 512 + (pw * 32 + lane) * 4),
-                   rowp + kHeadDim, nb, pol);
-        cp_async_commit();
-        hist_first = (hist_first << 1) | (first ? 1u : 0u);
-        hist_qs = (hist_qs << 1) | qs;
-        if (kk >= lag) {
-            cp_async_wait_upto(lag);
-            fence_proxy_async_smem();
-            mbar_arrive(&B.full[(kk - lag) % a.S]);
-            mbar_arrive(&B.sfull[(kk - lag) % a.RS]);
-            if ((hist_first >> lag) & 1u)
-                mbar_arrive(&B.qfull[(hist_qs >> lag) & 1u]);
         }
         it.next(a);
     }
+}
+
+// ---------------------------------------------------------------- gather + repack
+
+// Block-table entry of this lane's token in tile `t` (-1: no token).
+__device__ __forceinline__ int32_t table_entry(const MainArgs &a, const TileIter &t, int lane_tok)
+{
+    const int tok = t.m * kTileTokens + lane_tok;
+    if (t.nt == 0 || tok >= t.ctx)
+        return -1;
+    return __ldg(a.bt + (long long)t.i * a.W + tok / a.P);
+}
+
+static __device__ void gather_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int pw)
+{
+    const Bars B(a, smem);
+    const int lane = threadIdx.x & 31;
+    const int lane_tok = pw * 32 + lane;  // this lane's token row within a tile
+    const uint64_t pol = a.l2_policy == 0   ? l2_evict_first_policy()
+                         : a.l2_policy == 2 ? l2_evict_last_policy()
+                                            : l2_evict_normal_policy();
+    const int count = (int)c.count, SG = a.SG;
+    uint8_t *stg = smem + (uint32_t)pw * (uint32_t)SG * kWarpSlotBytes;
+    // per-lane metadata of the tiles in the staging ring: bit 2 = row present,
+    // bits 0-1 = misalignment of the row in 4-byte words
+    uint8_t *meta = smem + a.off_meta + (uint32_t)pw * (uint32_t)SG * 32u;
+    float *sring = reinterpret_cast<float *>(smem + a.off_scale);
+
+    TileIter iss, tab;
+    iss.init(a, c.i0, c.m0);
+    tab = iss;
+    // block-table entries of the next three tiles to issue
+    int32_t e0 = -1, e1 = -1, e2 = -1;
+    if (count > 0)
+        e0 = table_entry(a, tab, lane_tok);
+    if (count > 1) {
+        tab.next(a);
+        e1 = table_entry(a, tab, lane_tok);
+    }
+    if (count > 2) {
+        tab.next(a);
+        e2 = table_entry(a, tab, lane_tok);
+    }
+
+    auto issue = [&](int ki) {
+        const int32_t b = e0;
+        e0 = e1;
+        e1 = e2;
+        if (ki + 3 < count) {
+            tab.next(a);
+            e2 = table_entry(a, tab, lane_tok);
+        }
+        const int t = iss.m * kTileTokens + lane_tok;
+        long long w0 = 0;
+        uint32_t m = 0;
+        bool tail_ok = true;
+        if (t < iss.ctx) {
+            if (b >= 0 && (long long)b < a.num_blocks) {
+                const long long o = ((long long)b * a.P + (t % a.P)) * kKvRowBytes;
+                w0 = o & ~15ll;
+                m = 4u | (uint32_t)((o >> 2) & 3);
+                tail_ok = w0 + kWinBytes <= a.pool_bytes;
+            } else {
+                atomicOr(a.status, 0x1u);
+            }
+        }
+        const int slot = ki % SG;
+        meta[slot * 32 + lane] = (uint8_t)m;
+        const uint32_t sb = smem_u32(stg + (uint32_t)slot * kWarpSlotBytes);
+#pragma unroll
+        for (int qq = 0; qq < 9; ++qq) {
+            const int e = qq * 32 + lane;
+            const int j = e / 9, ch = e - j * 9;
+            const long long wj = __shfl_sync(kFullMask, w0, j);
+            const uint32_t mj = __shfl_sync(kFullMask, m, j);
+            const bool tj = __shfl_sync(kFullMask, tail_ok, j);
+            if (mj & 4u) {
+                const uint32_t dst = sb + (uint32_t)j * kWinBytes + (uint32_t)ch * 16u;
+                const uint8_t *src = a.kv + wj + ch * 16;
+                if (ch < 8 || tj) {
+                    cp_async_16_hint(dst, src, pol);
+                } else {
+                    // last row of the pool: never read past its end
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const bool in = wj + 128 + 4 * (q4 + 1) <= a.pool_bytes;
+                        cp_async_4(dst + 4 * q4, in ? src + 4 * q4 : a.kv, in ? 4u : 0u, pol);
+                    }
+                }
+            }
+        }
+        cp_async_commit();
+        iss.next(a);
+    };
+
+    // prologue: SG - 1 tiles in flight before the first repack. Tile k is this
+    // thread's cp.async group k, so tile kk has landed once at most
+    // (issued - kk - 1) groups are still pending.
+    int ki = 0;
+    for (; ki < SG - 1 && ki < count; ++ki)
+        issue(ki);
+    bool ok = true;
+    for (int kk = 0; kk < count; ++kk) {
+        if (ki < count) {
+            issue(ki);
+            ++ki;
+        }
+        cp_async_wait_upto(ki - kk - 1);
+        __syncwarp();
+        const int s = kk % a.S;
+        if (!mbar_wait(&B.op_empty[s], ((kk / a.S) & 1) ^ 1, &c.abort)) {
+            ok = false;
+            break;
+        }
+        const int slot = kk % SG;
+        const uint8_t *sb = stg + (uint32_t)slot * kWarpSlotBytes;
+        const uint32_t my_m = meta[slot * 32 + lane];
+        uint8_t *ob = smem + a.off_op + (uint32_t)s * kStageBytes;
+        const uint32_t chunk_off = (uint32_t)(lane & 3) * 4u;
+        const uint32_t chunk_id = (uint32_t)lane >> 2;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t mj = __shfl_sync(kFullMask, my_m, j);
+            uint32_t v = 0;
+            if (mj & 4u)
+                v = *reinterpret_cast<const uint32_t *>(sb + j * kWinBytes +
+                                                        ((mj & 3u) + (uint32_t)lane) * 4u);
+            const uint32_t r = (uint32_t)(pw * 32 + j);
+            *reinterpret_cast<uint32_t *>(ob + r * 128u + ((chunk_id ^ (r & 7u)) << 4) +
+                                          chunk_off) = v;
+        }
+        float sc = 0.0f;
+        if (my_m & 4u)
+            sc = *reinterpret_cast<const float *>(sb + lane * kWinBytes + ((my_m & 3u) + 32u) * 4u);
+        sring[(kk % a.RS) * kTileTokens + lane_tok] = sc;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&B.op_full[s]);
+            mbar_arrive(&B.sfull[kk % a.RS]);
+        }
+    }
     cp_async_wait_all();
-    fence_proxy_async_smem();
-    if (!ok) {
+    if (!ok)
         raise_abort(a, c);
-        return;
-    }
-    for (int d = lag - 1; d >= 0; --d) {
-        const int kd = kk - 1 - d;
-        if (kd < 0)
-            continue;
-        mbar_arrive(&B.full[kd % a.S]);
-        mbar_arrive(&B.sfull[kd % a.RS]);
-        if ((hist_first >> d) & 1u)
-            mbar_arrive(&B.qfull[(hist_qs >> d) & 1u]);
-    }
 }
 
 // ---------------------------------------------------------------- MMA issue
@@ -319,13 +416,13 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
             ok = false;
             break;
         }
-        if (!mbar_wait(&B.full[s], (kk / a.S) & 1, &c.abort) ||
+        if (!mbar_wait(&B.op_full[s], (kk / a.S) & 1, &c.abort) ||
             !mbar_wait(&B.tempty[b], ((kk / a.NBUF) & 1) ^ 1, &c.abort)) {
             ok = false;
             break;
         }
         tc_fence_after_sync();
-        const uint32_t abase = smem_u32(smem + (uint32_t)s * kStageBytes);
+        const uint32_t abase = smem_u32(smem + a.off_op + (uint32_t)s * kStageBytes);
         const uint32_t bbase = smem_u32(smem + a.off_q + qs * (uint32_t)N * kHeadDim);
 #pragma unroll
         for (int k4 = 0; k4 < kHeadDim / 32; ++k4) {
@@ -337,7 +434,7 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
                           idesc_e4m3_f32(128, nw), k4 > 0 ? 1u : 0u);
             }
         }
-        umma_commit(&B.empty[s]);
+        umma_commit(&B.op_empty[s]);
         umma_commit(&B.tfull[b]);
         if (kk == count - 1 || it.m == it.nt - 1) {
             umma_commit(&B.qempty[qs]);
@@ -347,16 +444,15 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
     }
     if (!ok)
         raise_abort(a, c);
-    // all MMAs issued by this thread have completed once `done` flips
     umma_commit(B.done);
     if (!mbar_wait(B.done, 0, nullptr))
-        atomicOr(a.ws.status, 0x4u);
+        atomicOr(a.status, 0x4u);
 }
 
 // ---------------------------------------------------------------- epilogue
 
 // Scores of rows j = g, g + E, ... for this thread's token: TMEM columns
-// [j*H, j*H + H) of buffer b. Releases the TMEM buffer after the last load.
+// [j*H, j*H + H) of the buffer. Releases the TMEM buffer after the last load.
 template <int H>
 __device__ __forceinline__ void epi_rows(uint32_t taddr, const float *wsl, float sc, int g, int E,
                                          int nn, float (&logit)[2], uint64_t *tempty_bar,
@@ -439,21 +535,7 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, const float *wsl, float
     }
 }
 
-// Wait on an mbarrier for a whole work group and agree on the outcome.
-__device__ __forceinline__ bool wg_wait(uint64_t *bar, uint32_t parity, CtaCtl &c, const Wg &g)
-{
-    if (g.warp == 0) {
-        const bool ok = mbar_wait(bar, parity, &c.abort);
-        if (g.lane == 0)
-            g.scr->flag = ok ? 1u : 0u;
-    }
-    g.sync();
-    const bool ok = g.scr->flag != 0;
-    g.sync();
-    return ok;
-}
-
-template <int H, bool FUSED>
+template <int H>
 static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int g, int we)
 {
     const Bars B(a, smem);
@@ -461,32 +543,17 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
     const int r = qd * 32 + lane;  // token row of the tile = TMEM lane
     const int N = a.N, nn = a.nn, E = a.E;
     const float NEG_INF = -__int_as_float(0x7f800000);
-
-    // per-work-group top-k state
-    uint8_t *cbase = smem + a.off_cand +
-                     (uint32_t)g * ((uint32_t)a.rpw * (uint32_t)a.cap * 8u + 64u +
-                                    (uint32_t)sizeof(WgScratch));
-    Wg wg;
-    wg.tid = (uint32_t)(we * 32 + lane);
-    wg.lane = (uint32_t)lane;
-    wg.warp = (uint32_t)we;
-    wg.bar = 1u + (uint32_t)g;
-    wg.scr = reinterpret_cast<WgScratch *>(cbase + (uint32_t)a.rpw * a.cap * 8u + 64u);
-    CandBuf cb[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        cb[u].key = reinterpret_cast<uint32_t *>(cbase) + (uint32_t)u * a.cap;
-        cb[u].pos = reinterpret_cast<int32_t *>(cbase + (uint32_t)a.rpw * a.cap * 4u) +
-                    (uint32_t)u * a.cap;
-        cb[u].count = reinterpret_cast<uint32_t *>(cbase + (uint32_t)a.rpw * a.cap * 8u) + 2 * u;
-        cb[u].thresh = cb[u].count + 1;
-        cb[u].cap = (uint32_t)a.cap;
-    }
+    const uint32_t wtid = (uint32_t)(we * 32 + lane);
+    const uint32_t bar_id = 1u + (uint32_t)g;
+    const bool want_hist = a.hist != nullptr;
+    uint32_t *shist = reinterpret_cast<uint32_t *>(smem + a.off_hist) +
+                      (uint32_t)g * (uint32_t)a.rpw * kHistBins;
+    const uint64_t keep_pol = l2_evict_last_policy();
     const int rows_here = (nn - g + E - 1) / E;
 
     // -inf beyond the last tile of each row: this CTA's share of every row
     if (a.logits) {
-        const int etid = g * 128 + we * 32 + lane, ethr = E * 128;
+        const int etid = g * 128 + (int)wtid, ethr = E * 128;
         for (int rr = 0; rr < a.bs * nn; ++rr) {
             const int cx = ctx_of(a, rr / nn);
             const long long lo =
@@ -499,90 +566,72 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
                 row[t] = NEG_INF;
         }
     }
-    if constexpr (FUSED) {
-        // requests with no tokens: no segment will ever merge their rows
-        if (blockIdx.x == 0 && g == 0) {
-            for (int rr = 0; rr < a.bs * nn; ++rr) {
-                if (ctx_of(a, rr / nn) > 0)
-                    continue;
-                for (int e = wg.tid; e < a.k; e += 128) {
-                    a.out_idx[(long long)rr * a.k + e] = -1;
-                    if (a.out_vals)
-                        a.out_vals[(long long)rr * a.k + e] = NEG_INF;
-                }
-            }
-        }
-        for (int u = 0; u < rows_here; ++u)
-            cand_reset(cb[u], wg);
+    if (want_hist) {
+        for (int e = (int)wtid; e < a.rpw * kHistBins; e += 128)
+            shist[e] = 0;
+        named_bar_sync(bar_id, 128);
     }
 
     const int count = (int)c.count;
     TileIter it;
     it.init(a, c.i0, c.m0);
-    uint32_t req = 0, seg_tiles = 0;
+    uint32_t req = 0;
+    // Waits that fail (abort or time limit) skip the data work but keep the
+    // work group's barrier schedule, so no warp is left waiting on another.
     for (int kk = 0; kk < count; ++kk) {
         const int b = kk % a.NBUF;
         const uint32_t qs = req % a.QS;
         const bool first = kk == 0 || it.m == 0;
-        if (first) {
-            seg_tiles = 0;
-            bool ok;
-            if constexpr (FUSED)
-                ok = wg_wait(&B.qfull[qs], (req / a.QS) & 1, c, wg);
-            else
-                ok = mbar_wait(&B.qfull[qs], (req / a.QS) & 1, &c.abort);
-            if (!ok) {
-                raise_abort(a, c);
-                break;
-            }
-        }
+        bool ok = true;
+        if (first)
+            ok = mbar_wait(&B.qfull[qs], (req / a.QS) & 1, &c.abort);
         const int sri = kk % a.RS;
-        const uint32_t sph = (uint32_t)(kk / a.RS) & 1u;
-        bool ok;
-        if constexpr (FUSED)
-            ok = wg_wait(&B.sfull[sri], sph, c, wg) &&
-                 wg_wait(&B.tfull[b], (kk / a.NBUF) & 1, c, wg);
-        else
-            ok = mbar_wait(&B.sfull[sri], sph, &c.abort) &&
-                 mbar_wait(&B.tfull[b], (kk / a.NBUF) & 1, &c.abort);
-        if (!ok) {
-            raise_abort(a, c);
-            break;
-        }
-        tc_fence_after_sync();
-        const float sc =
-            reinterpret_cast<const float *>(smem + a.off_scale)[sri * kTileTokens + r];
-        const int t = it.m * kTileTokens + r;
-        const float *wsl = reinterpret_cast<const float *>(smem + a.off_w + qs * (uint32_t)N * 4);
-        const uint32_t taddr = c.tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * a.cols);
-        float logit[2];
-        epi_rows<H>(taddr, wsl, sc, g, E, nn, logit, &B.tempty[b], lane);
-
-        for (int u = 0; u < rows_here; ++u) {
-            const int j = g + u * E;
-            const bool valid = t < valid_len(it.ctx, nn, j);
-            if (a.logits && t < a.mml)
-                a.logits[((long long)it.i * nn + j) * a.mml + t] = valid ? logit[u] : NEG_INF;
-            if constexpr (FUSED) {
-                const uint32_t key = f32_order_key(logit[u]);
-                cand_append(cb[u], wg, key, t, valid && key >= *cb[u].thresh);
+        ok = ok && mbar_wait(&B.sfull[sri], (uint32_t)(kk / a.RS) & 1u, &c.abort) &&
+             mbar_wait(&B.tfull[b], (kk / a.NBUF) & 1, &c.abort);
+        if (ok) {
+            tc_fence_after_sync();
+            const float sc =
+                reinterpret_cast<const float *>(smem + a.off_scale)[sri * kTileTokens + r];
+            const int t = it.m * kTileTokens + r;
+            const float *wsl =
+                reinterpret_cast<const float *>(smem + a.off_w + qs * (uint32_t)N * 4);
+            const uint32_t taddr =
+                c.tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * a.cols);
+            float logit[2];
+            epi_rows<H>(taddr, wsl, sc, g, E, nn, logit, &B.tempty[b], lane);
+            for (int u = 0; u < rows_here; ++u) {
+                const int j = g + u * E;
+                const long long row = (long long)it.i * nn + j;
+                const bool valid = t < valid_len(it.ctx, nn, j);
+                if (a.logits && t < a.mml)
+                    a.logits[row * a.mml + t] = valid ? logit[u] : NEG_INF;
+                if (a.clogits && valid)
+                    st_global_hint(a.clogits + row * a.mml + t, logit[u], keep_pol);
+                if (want_hist) {
+                    const uint32_t bin = f32_order_key(logit[u]) >> kHistShift;
+                    const uint32_t grp =
+                        __match_any_sync(kFullMask, valid ? bin : 0x10000u + (uint32_t)lane);
+                    if (valid && (__ffs(grp) - 1) == lane)
+                        atomicAdd(shist + u * kHistBins + bin, (uint32_t)__popc(grp));
+                }
             }
-        }
-        ++seg_tiles;
-        if constexpr (FUSED) {
-            for (int u = 0; u < rows_here; ++u)
-                cand_make_room(cb[u], (uint32_t)a.k, wg);
+        } else {
+            raise_abort(a, c);
         }
         if (kk == count - 1 || it.m == it.nt - 1) {
-            if constexpr (FUSED) {
+            if (want_hist) {
+                named_bar_sync(bar_id, 128);
                 for (int u = 0; u < rows_here; ++u) {
-                    const int j = g + u * E;
-                    const uint32_t vl = (uint32_t)valid_len(it.ctx, nn, j);
-                    const uint32_t k_eff = vl < (uint32_t)a.k ? vl : (uint32_t)a.k;
-                    segment_finish(cb[u], a.ws, (long long)it.i * nn + j, seg_tiles,
-                                   (uint32_t)it.nt, (uint32_t)a.k, k_eff, a.out_idx, a.out_vals,
-                                   wg);
+                    const long long row = (long long)it.i * nn + g + u * E;
+                    for (int e = (int)wtid; e < kHistBins; e += 128) {
+                        const uint32_t v = shist[u * kHistBins + e];
+                        if (v) {
+                            atomicAdd(a.hist + row * kHistBins + e, v);
+                            shist[u * kHistBins + e] = 0;
+                        }
+                    }
                 }
+                named_bar_sync(bar_id, 128);
             }
             __syncwarp();
             if (lane == 0)
@@ -595,8 +644,10 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
 
 // ---------------------------------------------------------------- kernel
 
-template <int H, bool FUSED>
-__global__ void __launch_bounds__(32 * (kFirstEpiWarp + 8), 1)
+constexpr int kMaxThreads = 32 * (kFirstEpiWarp + 8);
+
+template <int H>
+__global__ void __launch_bounds__(kMaxThreads, 1)
     pmqa_main_kernel(const __grid_constant__ MainArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -609,19 +660,19 @@ __global__ void __launch_bounds__(32 * (kFirstEpiWarp + 8), 1)
         ctl.abort = 0;
         const Bars B(a, smem);
         for (int s = 0; s < a.S; ++s) {
-            mbar_init(&B.full[s], 32 * kProducerWarps);
-            mbar_init(&B.empty[s], 1);
+            mbar_init(&B.op_full[s], kPRWarps);
+            mbar_init(&B.op_empty[s], 1);
         }
         for (int b = 0; b < a.NBUF; ++b) {
             mbar_init(&B.tfull[b], 1);
             mbar_init(&B.tempty[b], 4 * a.E);
         }
         for (int q = 0; q < a.QS; ++q) {
-            mbar_init(&B.qfull[q], 32 * kProducerWarps);
+            mbar_init(&B.qfull[q], 1);
             mbar_init(&B.qempty[q], 1 + 4 * a.E);
         }
         for (int q = 0; q < a.RS; ++q)
-            mbar_init(&B.sfull[q], 32 * kProducerWarps);
+            mbar_init(&B.sfull[q], kPRWarps);
         mbar_init(B.done, 1);
         mbar_init_fence();
     }
@@ -637,7 +688,7 @@ __global__ void __launch_bounds__(32 * (kFirstEpiWarp + 8), 1)
         for (int i = threadIdx.x; i < a.bs; i += blockDim.x) {
             const int cx = __ldg(a.ctx_lens + i);
             if (cx < 0 || cx > lim)
-                atomicOr(a.ws.status, 0x2u);
+                atomicOr(a.status, 0x2u);
         }
     }
     tc_fence_before_sync();
@@ -648,11 +699,15 @@ __global__ void __launch_bounds__(32 * (kFirstEpiWarp + 8), 1)
         if ((threadIdx.x & 31) == 0)
             mma_role(a, smem, ctl);
         __syncwarp();
+    } else if (warp == 1) {
+        if ((threadIdx.x & 31) == 0)
+            qload_role(a, smem, ctl);
+        __syncwarp();
     } else if (warp < kFirstEpiWarp) {
-        producer_role(a, smem, ctl, warp - 1);
+        gather_role(a, smem, ctl, warp - kFirstPRWarp);
     } else {
         const int e = warp - kFirstEpiWarp;
-        epilogue_role<H, FUSED>(a, smem, ctl, e >> 2, e & 3);
+        epilogue_role<H>(a, smem, ctl, e >> 2, e & 3);
     }
 
     tc_fence_before_sync();

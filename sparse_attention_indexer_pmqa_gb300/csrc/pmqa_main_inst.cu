@@ -14,19 +14,15 @@
 
 namespace pmqa {
 
-cudaError_t PMQA_CAT(launch_main_h, PMQA_HEADS)(const MainArgs &a, bool fused, int grid,
-                                                int threads, cudaStream_t stream)
+cudaError_t PMQA_CAT(launch_main_h, PMQA_HEADS)(const MainArgs &a, int grid, int threads,
+                                                cudaStream_t stream)
 {
-    const void *fn = fused ? reinterpret_cast<const void *>(&pmqa_main_kernel<PMQA_HEADS, true>)
-                           : reinterpret_cast<const void *>(&pmqa_main_kernel<PMQA_HEADS, false>);
-    cudaError_t e =
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem_bytes);
+    cudaError_t e = cudaFuncSetAttribute(pmqa_main_kernel<PMQA_HEADS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)a.smem_bytes);
     if (e != cudaSuccess)
         return e;
-    if (fused)
-        pmqa_main_kernel<PMQA_HEADS, true><<<grid, threads, a.smem_bytes, stream>>>(a);
-    else
-        pmqa_main_kernel<PMQA_HEADS, false><<<grid, threads, a.smem_bytes, stream>>>(a);
+    pmqa_main_kernel<PMQA_HEADS><<<grid, threads, a.smem_bytes, stream>>>(a);
     return cudaGetLastError();
 }
 

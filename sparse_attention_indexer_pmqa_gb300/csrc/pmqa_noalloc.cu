@@ -19,6 +19,10 @@
 
 #include "../../include/pmqa.h"
 
+namespace pmqa {
+size_t fused_ws_zero_bytes(int bs, int next_n);
+}
+
 namespace {
 
 constexpr size_t kScratchBytes = size_t(32) << 20;
@@ -65,12 +69,11 @@ extern "C" int pmqa_logits_topk_noalloc(const pmqa_problem *p, int32_t k, int32_
     int rc = scratch_for_current_device(&ws);
     if (rc != PMQA_OK)
         return rc;
-    // The array keeps whatever the previous call left. The fused kernel needs
-    // the status word and the per-row counters at zero; the candidate area is
-    // always written before it is read. 256 + two 256-aligned counter arrays:
-    const size_t rows = (size_t)p->bs * (size_t)p->next_n;
-    const size_t counters = 256 + 2 * ((rows * 4 + 255) / 256 * 256);
-    if (cudaMemsetAsync(ws, 0, counters, stream) != cudaSuccess)
+    // The array keeps whatever the previous call left. The fused call needs its
+    // status word, per-row counters and per-row histograms at zero; the rest is
+    // always written before it is read.
+    const size_t zero = pmqa::fused_ws_zero_bytes(p->bs, p->next_n);
+    if (zero == 0 || cudaMemsetAsync(ws, 0, zero, stream) != cudaSuccess)
         return PMQA_ERR_CUDA;
     return pmqa_logits_topk(p, k, idx, vals, logits, ws, kScratchBytes, stream);
 }

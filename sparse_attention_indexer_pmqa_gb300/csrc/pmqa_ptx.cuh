@@ -84,6 +84,20 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_normal_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 4-byte asynchronous copy global -> shared; src_bytes 0 zero-fills without reading.
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes,
                                            uint64_t policy)
@@ -97,6 +111,54 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(src), "l"(policy)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+
+// Expect `bytes` more transaction bytes on the barrier and arrive once.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 2-D tiled tensor load (box given by the tensor map) into shared memory,
+// completion signalled as transaction bytes on `bar`. x is the innermost
+// coordinate (bytes for a uint8 map) and must keep the 16-byte rule.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared; addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Global store with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_global_hint(float *p, float v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy)
+                 : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit()

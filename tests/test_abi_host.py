@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert pmqa.pmqa_version() == 100
+    assert pmqa.pmqa_version() == 200
     assert pmqa.status_string(0) == "ok"
     assert pmqa.status_string(-3) == "workspace too small"
     assert pmqa.status_string(12345) == "unknown status"
@@ -44,9 +44,14 @@ def test_version_and_status_strings(lib):
 
 def test_workspace_sizes(lib):
     assert pmqa.pmqa_workspace_bytes(4, 2, 1000, 2048, pmqa.PMQA_OP_LOGITS) == 256
-    n = pmqa.pmqa_workspace_bytes(4, 2, 1000, 2048, pmqa.PMQA_OP_LOGITS_TOPK)
-    assert n == 256 + 256 + 256 + 8 * 1000 * 8
-    assert pmqa.pmqa_workspace_bytes(4, 2, 1000, 2048, pmqa.PMQA_OP_TOPK) == n
+    rows, mml = 8, 1000
+    counters = 256 + 3 * 256  # status word, then three 256-aligned per-row counter arrays
+    hist = rows * 2048 * 4  # per-row key histograms
+    ties = -(-rows * mml * 4 // 256) * 256
+    topk = pmqa.pmqa_workspace_bytes(4, 2, mml, 2048, pmqa.PMQA_OP_TOPK)
+    assert topk == counters + hist + ties
+    fused = pmqa.pmqa_workspace_bytes(4, 2, mml, 2048, pmqa.PMQA_OP_LOGITS_TOPK)
+    assert fused == topk + rows * mml * 4  # plus the compact logits
     assert pmqa.pmqa_workspace_bytes(-1, 1, 10, 1, 0) == 0
     assert pmqa.pmqa_workspace_bytes(1, 1, 10, 1, 7) == 0
 
@@ -113,7 +118,8 @@ def test_topk_validation(lib):
     assert lib.pmqa_topk(L, C, 2, 1, 64, 8, I, None, WS, need - 1, None) == -3
     assert lib.pmqa_topk(None, C, 2, 1, 64, 8, I, None, WS, need, None) == -1
     assert lib.pmqa_topk(L, C, 2, 1, 64, 8, ctypes.c_void_p(0x30002), None, WS, need, None) == -1
-    assert lib.pmqa_topk(L, C, 2, 1, 64, 1 << 20, I, None, WS, need, None) == -2
+    big = pmqa.pmqa_workspace_bytes(70000, 1, 64, 8, pmqa.PMQA_OP_TOPK)
+    assert lib.pmqa_topk(L, C, 70000, 1, 64, 8, I, None, WS, big, None) == -2
 
 
 def test_empty_batch_is_a_no_op(lib):

@@ -211,3 +211,19 @@ def test_workload_standalone_topk(cuda_lib, workload):
     c = torch.from_numpy(prob.context_lens).cuda()
     idx = cuda_lib.pmqa_topk(t, c, prob.next_n, prob.k).cpu().numpy()
     check_topk_exact(idx, ref, prob.context_lens, prob.next_n, prob.k)
+
+
+@pytest.mark.parametrize("nn,H", [(1, 64), (2, 32), (4, 64), (3, 128)])
+def test_many_short_requests(cuda_lib, nn, H):
+    """Each CTA walks many requests, several shorter than the copy pipeline."""
+    rng = np.random.default_rng(nn * H)
+    ctx = rng.integers(0, 400, size=300)
+    ctx[::7] = rng.integers(1, 4, size=len(ctx[::7]))
+    prob = make_problem(300, nn, H, 1, ctx, 512, seed=nn + H, table="perm")
+    ref, r64, tol = oracle_all(prob)
+    d = dev(prob)
+    ws = cuda_lib.workspace(300, nn, 512, 64, cuda_lib.PMQA_OP_LOGITS_TOPK)
+    check_logits(gpu_logits(cuda_lib, prob, d=d, ws=ws), ref, tol)
+    idx, vals = gpu_fused(cuda_lib, prob, 64, d=d, ws=ws)
+    check_topk_rows(idx, r64, tol, prob.context_lens, nn, 64, vals=vals)
+    assert cuda_lib.pmqa_read_device_status(ws) == 0
