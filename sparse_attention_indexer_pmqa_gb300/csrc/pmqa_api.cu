@@ -24,7 +24,8 @@ using namespace pmqa;
 namespace {
 
 constexpr int kVersion = 200;  // 0.2.0
-constexpr uint32_t kMaxDynSmem = 232448 - 1024;
+// 227 KB per CTA, shared between the static CtaCtl block and the dynamic layout
+constexpr uint32_t kMaxDynSmem = 232448 - ((uint32_t)sizeof(CtaCtl) + 127u) / 128u * 128u;
 constexpr uint32_t kMinMainSmem = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr size_t kWsAlign = 256;
 constexpr int kSelChunk = 8192;  // positions per selection CTA
@@ -33,7 +34,7 @@ constexpr int kSelChunk = 8192;  // positions per selection CTA
 #define PMQA_MAX_STAGING 8
 #endif
 #ifndef PMQA_OP_STAGES
-#define PMQA_OP_STAGES 2
+#define PMQA_OP_STAGES 3
 #endif
 #ifndef PMQA_L2_POLICY
 #define PMQA_L2_POLICY 0
@@ -106,8 +107,6 @@ bool main_layout(int heads, int nn, bool with_hist, MainArgs &a)
 {
     const int N = heads * nn;
     a.N = N;
-    a.E = nn >= 2 ? 2 : 1;
-    a.rpw = (nn + a.E - 1) / a.E;
     int cols = 32;
     while (cols < N)
         cols <<= 1;
@@ -120,7 +119,7 @@ bool main_layout(int heads, int nn, bool with_hist, MainArgs &a)
     for (int SG = PMQA_MAX_STAGING; SG >= 3; --SG) {
         for (int QS = 2; QS >= 1; --QS) {
             const int RS = a.S + a.NBUF;
-            uint32_t off = (uint32_t)SG * kPRWarps * kWarpSlotBytes;
+            uint32_t off = (uint32_t)SG * kSlotBytes;  // staging ring
             a.off_op = off;
             off += (uint32_t)a.S * kStageBytes;
             a.off_q = off;
@@ -131,14 +130,16 @@ bool main_layout(int heads, int nn, bool with_hist, MainArgs &a)
             a.off_scale = off;
             off += (uint32_t)RS * kTileTokens * 4u;
             a.off_meta = off;
-            off += (uint32_t)(kPRWarps * SG * 32);
+            off += (uint32_t)(SG * kTileTokens);
             off = (uint32_t)align_up(off, 16);
+            a.off_tab = off;
+            off += (uint32_t)(SG * kTileTokens * 4);
             a.off_bar = off;
-            off += (uint32_t)(2 * a.S + 2 * a.NBUF + 2 * QS + RS + 1) * 8u;
+            off += (uint32_t)(2 * a.S + 2 * a.NBUF + 2 * QS + RS + 2 * SG + 1) * 8u;
             off = (uint32_t)align_up(off, 16);
             a.off_hist = off;
             if (with_hist)
-                off += (uint32_t)(a.E * a.rpw * kHistBins * 4);
+                off += (uint32_t)(nn * kHistBins * 4);
             const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
             if (total > kMaxDynSmem)
                 continue;
@@ -290,7 +291,7 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     int sms = 0;
     if ((rc = sm_count(&sms)) != PMQA_OK)
         return rc;
-    const int threads = 32 * (kFirstEpiWarp + 4 * a.E);
+    const int threads = kMaxThreads;
     cudaError_t e;
     switch (p->heads) {
     case 16: e = launch_main_h16(a, sms, threads, stream); break;

@@ -7,24 +7,32 @@
 //
 // One CTA per SM walks a contiguous range of (request, 128-token tile) work
 // items, balanced by tile count over all requests. Warp roles:
-//   warp 0      allocates TMEM; lane 0 issues tcgen05.mma
-//   warp 1      lane 0 loads each request's q (TMA, 128B swizzle) and weights
+//   warp 14     lane 0 issues tcgen05.mma (warp 0 allocates TMEM)
+//   warp 8      lane 0 loads each request's q (TMA, 128B swizzle) and weights
 //               (bulk copy) into a query slot
-//   warps 2..5  gather + repack, 32 tokens of every tile each: the block table
-//               is read three tiles ahead; every 132-byte row is fetched as its
-//               16-byte aligned 144-byte window with 16-byte cp.async into a
-//               per-warp staging ring (several tiles in flight); once a tile
-//               has landed the warp moves each row's 32 fp8 words (shifted by
-//               the row's 0/4/8/12-byte misalignment) into the 128B-swizzled
-//               K-major operand tile and its fp32 scale into a scale ring
-//   warps 6..   epilogue work groups (1 or 2 x 4 warps): tcgen05.ld of the
-//               fp32 scores (one token per thread, all heads of a row in
-//               registers), relu * weight head sum, scale, mask; full logits
+//   gather warps (0, 1, 4, 5), 32 tokens of every tile each: block-table entries
+//               arrive by cp.async a ring-depth ahead; every 132-byte row is
+//               fetched as its 16-byte aligned 144-byte window with 16-byte
+//               cp.async into the staging ring, whose mbarrier completes when
+//               the copies land (several tiles in flight, no blocking)
+//   repack warps (2, 3, 6, 7), 32 tokens of every tile each: once a tile has landed,
+//               each row's 32 fp8 words (shifted by the row's 0/4/8/12-byte
+//               misalignment) go into the 128B-swizzled K-major operand tile
+//               and its fp32 scale into a scale ring
+//   warps 10..13 the epilogue work group: tcgen05.ld of the fp32 scores (one
+//               token per thread, all heads of a row in registers), relu *
+//               weight head sum, scale, mask for every draft row; full logits
 //               rows and/or the compact logits + an 11-bit key histogram per
 //               row for the selection kernel.
 // The MMA computes D[token][(j,h)] = K_tile[128 x 128] * Q[(j,h) x 128]^T with
 // tokens as M = 128 and N = next_n * heads, fp8 e4m3 in, fp32 accumulate in
 // TMEM (NBUF accumulators). All hand-offs are mbarriers; waits are bounded.
+// A warp runs on sub-partition warp % 4. Gather and repack warps sit on
+// different sub-partitions (gather on 0 and 1, repack on 2 and 3), so each
+// sub-partition's instruction cache holds the code of at most two busy roles,
+// and the MMA issue (on 2) does not queue behind the gathers' global copies;
+// the epilogue needs one warp on every sub-partition (warp w reads TMEM lanes
+// 32 * (w % 4) ...). Warps 9 and 15 have no role.
 #pragma once
 
 #include <cuda.h>
@@ -39,12 +47,19 @@ constexpr uint32_t kFullMask = 0xFFFFFFFFu;
 constexpr int kTileTokens = 128;
 constexpr int kHeadDim = 128;
 constexpr int kKvRowBytes = kHeadDim + 4;
-constexpr int kPRWarps = 4;
-constexpr int kFirstPRWarp = 2;
-constexpr int kFirstEpiWarp = kFirstPRWarp + kPRWarps;
+constexpr int kGatherWarps = 4;
+constexpr int kRepackWarps = 4;
+constexpr int kTokPerWarp = kTileTokens / kGatherWarps;    // 32 tokens per gather/repack warp
+constexpr int kFirstEpiWarp = 10;
+constexpr int kMmaWarp = 14;
+constexpr int kQloadWarp = 8;
+
+// Row block (0..3) of a gather warp (0, 1, 4, 5) or a repack warp (2, 3, 6, 7).
+__device__ __forceinline__ int row_block_of(int warp) { return (warp & 1) | ((warp >> 2) & 1) << 1; }
+constexpr int kMaxRows = 4;                                // draft rows per request
 constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16 KB operand tile
 constexpr uint32_t kWinBytes = 144;                        // aligned window of one row
-constexpr uint32_t kWarpSlotBytes = 32 * kWinBytes;        // one warp's rows of a tile
+constexpr uint32_t kSlotBytes = kTileTokens * kWinBytes;   // one staging slot (18 KB)
 constexpr int kHistBins = 2048;                            // top 11 bits of the order key
 constexpr int kHistShift = 21;
 
@@ -64,10 +79,12 @@ struct MainArgs {
     uint32_t *status;
     int l2_policy;     // KV stream: 0 evict_first, 1 evict_normal, 2 evict_last
     // shared-memory / pipeline layout, computed on the host
-    int N, S, SG, NBUF, QS, RS, cols, tmem_cols, E, rpw;
+    int N, S, SG, NBUF, QS, RS, cols, tmem_cols;
     int q_box;  // rows per q TMA box: N / ceil(N / 256)
-    uint32_t off_op, off_q, off_w, off_scale, off_meta, off_bar, off_hist, smem_bytes;
+    uint32_t off_op, off_q, off_w, off_scale, off_meta, off_tab, off_bar, off_hist, smem_bytes;
 };
+
+constexpr int kCtxCache = 512;  // context lengths of the CTA's first requests, in smem
 
 struct CtaCtl {
     long long red[16];
@@ -76,6 +93,7 @@ struct CtaCtl {
     int i0, m0;
     int abort;
     uint32_t tmem_base;
+    int ctx[kCtxCache];  // clamped context of request i0 + n, n < kCtxCache
 };
 
 // f32 -> u32 with a > b  <=>  key(a) > key(b); -0 is folded onto +0.
@@ -157,35 +175,65 @@ __device__ void balance_schedule(int n_items, LenFn len_of, CtaCtl &c)
     }
 }
 
-// Walks (request, tile) pairs in order, skipping empty requests.
+// Walks (request, tile) pairs in order, skipping empty requests. Context
+// lengths come from the CTA's shared-memory cache while it covers them. Every
+// field the walk needs is copied out of the kernel parameters at init, so the
+// hot loops never re-read parameter memory.
 struct TileIter {
     int i, m, nt, ctx;
-    __device__ void init(const MainArgs &a, int i0, int m0)
+    int bs, i0, lim;
+    const int *cache;  // clamped contexts of requests i0 .. i0 + kCtxCache - 1
+    const int32_t *ctx_lens;
+    __device__ int ctx_at(int r) const
     {
-        i = i0;
-        m = m0;
-        ctx = i < a.bs ? ctx_of(a, i) : 0;
+        const int n = r - i0;
+        return (n >= 0 && n < kCtxCache) ? cache[n] : clamp_ctx(__ldg(ctx_lens + r), (long long)lim);
+    }
+    __device__ void init(const MainArgs &a, const CtaCtl &cc)
+    {
+        bs = a.bs;
+        i0 = cc.i0;
+        lim = (int)min((long long)a.mml, (long long)a.W * a.P);
+        cache = cc.ctx;
+        ctx_lens = a.ctx_lens;
+        i = cc.i0;
+        m = cc.m0;
+        ctx = i < bs ? ctx_at(i) : 0;
         nt = (ctx + kTileTokens - 1) / kTileTokens;
     }
-    __device__ void next(const MainArgs &a)
+    __device__ void next()
     {
         if (++m < nt)
             return;
         m = 0;
         do {
-            if (++i >= a.bs) {
+            if (++i >= bs) {
                 nt = 0;
                 ctx = 0;
                 return;
             }
-            ctx = ctx_of(a, i);
+            ctx = ctx_at(i);
             nt = (ctx + kTileTokens - 1) / kTileTokens;
         } while (nt == 0);
     }
 };
 
+// Position in a ring of n slots plus the parity of the current lap.
+struct Ring {
+    int n, slot;
+    uint32_t phase;
+    __device__ explicit Ring(int n_) : n(n_), slot(0), phase(0) {}
+    __device__ void advance()
+    {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 struct Bars {
-    uint64_t *op_full, *op_empty, *tfull, *tempty, *qfull, *qempty, *sfull, *done;
+    uint64_t *op_full, *op_empty, *tfull, *tempty, *qfull, *qempty, *sfull, *gfull, *gempty, *done;
     __device__ Bars(const MainArgs &a, uint8_t *smem)
     {
         op_full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
@@ -195,7 +243,9 @@ struct Bars {
         qfull = tempty + a.NBUF;
         qempty = qfull + a.QS;
         sfull = qempty + a.QS;
-        done = sfull + a.RS;
+        gfull = sfull + a.RS;
+        gempty = gfull + a.SG;
+        done = gempty + a.SG;
     }
 };
 
@@ -224,175 +274,204 @@ __device__ __forceinline__ void raise_abort(const MainArgs &a, CtaCtl &c)
 
 // ---------------------------------------------------------------- query loader
 
+// Each role copies the kernel parameters its loop needs into registers before
+// the loop: the loops are full of inline-asm memory clobbers, after which any
+// field read through the parameter reference would be fetched again.
+
 static __device__ void qload_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
 {
     const Bars B(a, smem);
-    const int N = a.N, count = (int)c.count;
+    const int N = a.N, count = (int)c.count, q_box = a.q_box;
+    const uint32_t q_bytes = (uint32_t)N * kHeadDim, w_bytes = (uint32_t)N * 4u;
+    const uint32_t q0 = smem_u32(smem + a.off_q), w0 = smem_u32(smem + a.off_w);
+    const float *const w = a.w;
+    const void *const tmap = &a.tmap_q;
     TileIter it;
-    it.init(a, c.i0, c.m0);
-    uint32_t req = 0;
+    it.init(a, c);
+    Ring q(a.QS);
     for (int kk = 0; kk < count; ++kk) {
         if (kk == 0 || it.m == 0) {
-            const uint32_t qs = req % a.QS;
-            if (!mbar_wait(&B.qempty[qs], ((req / a.QS) & 1) ^ 1, &c.abort)) {
+            if (!mbar_wait(&B.qempty[q.slot], q.phase ^ 1u, &c.abort)) {
                 raise_abort(a, c);
                 return;
             }
-            mbar_arrive_expect_tx(&B.qfull[qs], (uint32_t)N * (kHeadDim + 4));
-            const uint32_t qdst = smem_u32(smem + a.off_q + qs * (uint32_t)N * kHeadDim);
+            mbar_arrive_expect_tx(&B.qfull[q.slot], q_bytes + w_bytes);
+            const uint32_t qdst = q0 + (uint32_t)q.slot * q_bytes;
             // boxes of q_box rows tile the request's N rows exactly (N = nbox * q_box)
-            for (int nc = 0; nc * a.q_box < N; ++nc)
-                tma_load_2d(qdst + nc * a.q_box * kHeadDim, &a.tmap_q, 0, it.i * N + nc * a.q_box,
-                            &B.qfull[qs]);
-            bulk_load(smem_u32(smem + a.off_w + qs * (uint32_t)N * 4), a.w + (long long)it.i * N,
-                      (uint32_t)N * 4, &B.qfull[qs]);
-            ++req;
+            for (int nc = 0; nc * q_box < N; ++nc)
+                tma_load_2d(qdst + (uint32_t)(nc * q_box * kHeadDim), tmap, 0, it.i * N + nc * q_box,
+                            &B.qfull[q.slot]);
+            bulk_load(w0 + (uint32_t)q.slot * w_bytes, w + (long long)it.i * N, w_bytes, &B.qfull[q.slot]);
+            q.advance();
         }
-        it.next(a);
+        it.next();
     }
 }
 
 // ---------------------------------------------------------------- gather + repack
 
-// Block-table entry of this lane's token in tile `t` (-1: no token).
-__device__ __forceinline__ int32_t table_entry(const MainArgs &a, const TileIter &t, int lane_tok)
-{
-    const int tok = t.m * kTileTokens + lane_tok;
-    if (t.nt == 0 || tok >= t.ctx)
-        return -1;
-    return __ldg(a.bt + (long long)t.i * a.W + tok / a.P);
-}
-
-static __device__ void gather_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int pw)
+// Gather warp gw: rows 32*gw .. 32*gw+31 of every tile. The copies of tile k
+// land in staging slot k % SG; gfull[slot] completes when every gather thread
+// has published its rows' metadata (release arrive) and its copies have landed
+// (cp.async arrive). The block-table entry of tile k travels by cp.async in
+// this thread's cp.async group k: groups 0..SG-2 carry only the first entries,
+// group SG-1+k carries the entry of tile k+SG-1 and the copies of tile k.
+static __device__ void gather_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int gw)
 {
     const Bars B(a, smem);
     const int lane = threadIdx.x & 31;
-    const int lane_tok = pw * 32 + lane;  // this lane's token row within a tile
+    const int row = gw * kTokPerWarp + lane;  // this lane's token row in a tile
     const uint64_t pol = a.l2_policy == 0   ? l2_evict_first_policy()
                          : a.l2_policy == 2 ? l2_evict_last_policy()
                                             : l2_evict_normal_policy();
-    const int count = (int)c.count, SG = a.SG;
-    uint8_t *stg = smem + (uint32_t)pw * (uint32_t)SG * kWarpSlotBytes;
-    // per-lane metadata of the tiles in the staging ring: bit 2 = row present,
-    // bits 0-1 = misalignment of the row in 4-byte words
-    uint8_t *meta = smem + a.off_meta + (uint32_t)pw * (uint32_t)SG * 32u;
-    float *sring = reinterpret_cast<float *>(smem + a.off_scale);
-
+    const uint8_t *const kv = a.kv;
+    const int32_t *const bt = a.bt;
+    const long long num_blocks = a.num_blocks, pool_bytes = a.pool_bytes;
+    const int P = a.P, W = a.W;
+    const bool p_pow2 = (P & (P - 1)) == 0;
+    const int p_shift = __ffs(P) - 1;
+    uint32_t *const status = a.status;
+    const int count = (int)c.count, SG = a.SG, DT = a.SG - 1;
+    uint8_t *const meta = smem + a.off_meta;                             // [SG][128]
+    int32_t *const tring = reinterpret_cast<int32_t *>(smem + a.off_tab);  // [SG][128]
+    const uint32_t stage0 = smem_u32(smem) + (uint32_t)(gw * kTokPerWarp) * kWinBytes;
+    auto page_of = [&](int tok) { return p_pow2 ? tok >> p_shift : tok / P; };
     TileIter iss, tab;
-    iss.init(a, c.i0, c.m0);
+    iss.init(a, c);
     tab = iss;
-    // block-table entries of the next three tiles to issue
-    int32_t e0 = -1, e1 = -1, e2 = -1;
-    if (count > 0)
-        e0 = table_entry(a, tab, lane_tok);
-    if (count > 1) {
-        tab.next(a);
-        e1 = table_entry(a, tab, lane_tok);
+    int tab_slot = 0;
+    auto prefetch_table = [&]() {  // entry of tab's tile into ring slot tab_slot
+        const int tok = tab.m * kTileTokens + row;
+        int32_t *dst = tring + tab_slot * kTileTokens + row;
+        if (tab.nt > 0 && tok < tab.ctx)
+            cp_async_4(smem_u32(dst), bt + (long long)tab.i * W + page_of(tok), 4u, pol);
+        else
+            *dst = -1;
+        tab.next();
+        if (++tab_slot == SG)
+            tab_slot = 0;
+    };
+    for (int kt = 0; kt < DT; ++kt) {
+        if (kt < count)
+            prefetch_table();
+        cp_async_commit();
     }
-    if (count > 2) {
-        tab.next(a);
-        e2 = table_entry(a, tab, lane_tok);
-    }
-
-    auto issue = [&](int ki) {
-        const int32_t b = e0;
-        e0 = e1;
-        e1 = e2;
-        if (ki + 3 < count) {
-            tab.next(a);
-            e2 = table_entry(a, tab, lane_tok);
+    Ring g(SG);
+    bool ok = true;
+    for (int ki = 0; ki < count; ++ki) {
+        if (!mbar_wait(&B.gempty[g.slot], g.phase ^ 1u, &c.abort)) {
+            ok = false;
+            break;
         }
-        const int t = iss.m * kTileTokens + lane_tok;
+        cp_async_wait_upto(DT - 1);  // group ki: the table entry of tile ki
+        const int32_t b = tring[g.slot * kTileTokens + row];
+        if (ki + DT < count)
+            prefetch_table();
+        const int t = iss.m * kTileTokens + row;
         long long w0 = 0;
         uint32_t m = 0;
-        bool tail_ok = true;
+        uint32_t last = 16;  // bytes of the window's last chunk inside the pool (4..16)
         if (t < iss.ctx) {
-            if (b >= 0 && (long long)b < a.num_blocks) {
-                const long long o = ((long long)b * a.P + (t % a.P)) * kKvRowBytes;
+            if (b >= 0 && (long long)b < num_blocks) {
+                const int in_page = p_pow2 ? (t & (P - 1)) : t - page_of(t) * P;
+                const long long o = ((long long)b * P + in_page) * kKvRowBytes;
                 w0 = o & ~15ll;
                 m = 4u | (uint32_t)((o >> 2) & 3);
-                tail_ok = w0 + kWinBytes <= a.pool_bytes;
+                last = (uint32_t)min(16ll, pool_bytes - (w0 + 128));
             } else {
-                atomicOr(a.status, 0x1u);
+                atomicOr(status, 0x1u);
             }
         }
-        const int slot = ki % SG;
-        meta[slot * 32 + lane] = (uint8_t)m;
-        const uint32_t sb = smem_u32(stg + (uint32_t)slot * kWarpSlotBytes);
+        meta[g.slot * kTileTokens + row] = (uint8_t)m;
+        const uint32_t sb = stage0 + (uint32_t)g.slot * kSlotBytes;
+        // 32 windows x 9 chunks = 288 copies: lane -> (token e / 9, chunk e % 9).
+        // The window's first 128 bytes start at or before the row, so lie in
+        // the pool; its last chunk may pass the end of the pool's last row and
+        // then reads only the bytes inside (zero fill for the rest).
 #pragma unroll
         for (int qq = 0; qq < 9; ++qq) {
             const int e = qq * 32 + lane;
             const int j = e / 9, ch = e - j * 9;
             const long long wj = __shfl_sync(kFullMask, w0, j);
             const uint32_t mj = __shfl_sync(kFullMask, m, j);
-            const bool tj = __shfl_sync(kFullMask, tail_ok, j);
-            if (mj & 4u) {
-                const uint32_t dst = sb + (uint32_t)j * kWinBytes + (uint32_t)ch * 16u;
-                const uint8_t *src = a.kv + wj + ch * 16;
-                if (ch < 8 || tj) {
-                    cp_async_16_hint(dst, src, pol);
-                } else {
-                    // last row of the pool: never read past its end
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const bool in = wj + 128 + 4 * (q4 + 1) <= a.pool_bytes;
-                        cp_async_4(dst + 4 * q4, in ? src + 4 * q4 : a.kv, in ? 4u : 0u, pol);
-                    }
-                }
-            }
+            const uint32_t lj = __shfl_sync(kFullMask, last, j);
+            if (mj & 4u)
+                cp_async_16_zfill(sb + (uint32_t)j * kWinBytes + (uint32_t)ch * 16u, kv + wj + ch * 16,
+                                  ch < 8 ? 16u : lj, pol);
         }
+        mbar_arrive(&B.gfull[g.slot]);            // metadata published
+        cp_async_arrive_noinc(&B.gfull[g.slot]);  // copies landed
         cp_async_commit();
-        iss.next(a);
-    };
+        iss.next();
+        g.advance();
+    }
+    cp_async_wait_all();
+    if (!ok)
+        raise_abort(a, c);
+}
 
-    // prologue: SG - 1 tiles in flight before the first repack. Tile k is this
-    // thread's cp.async group k, so tile kk has landed once at most
-    // (issued - kk - 1) groups are still pending.
-    int ki = 0;
-    for (; ki < SG - 1 && ki < count; ++ki)
-        issue(ki);
+// Repack warp rw: rows 32*rw .. 32*rw+31 of every tile, staging -> operand.
+// Lane l moves row 32*rw + l: its 144-byte window as nine 16-byte loads (rows
+// 144 bytes apart: eight lanes of a load phase hit distinct bank groups), a
+// shift by the row's misalignment in registers, and eight 16-byte stores into
+// the row's 128B-swizzled chunks (again conflict-free per phase).
+static __device__ void repack_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int rw)
+{
+    const Bars B(a, smem);
+    const int lane = threadIdx.x & 31;
+    const int count = (int)c.count;
+    const uint32_t r = (uint32_t)(rw * kTokPerWarp + lane);  // this lane's row
+    const uint8_t *const meta = smem + a.off_meta + r;
+    float *const sring = reinterpret_cast<float *>(smem + a.off_scale) + r;
+    uint8_t *const op_row = smem + a.off_op + r * 128u;
+    const uint8_t *const win0 = smem + r * kWinBytes;
+    Ring g(a.SG), st(a.S), sr(a.RS);
     bool ok = true;
     for (int kk = 0; kk < count; ++kk) {
-        if (ki < count) {
-            issue(ki);
-            ++ki;
-        }
-        cp_async_wait_upto(ki - kk - 1);
-        __syncwarp();
-        const int s = kk % a.S;
-        if (!mbar_wait(&B.op_empty[s], ((kk / a.S) & 1) ^ 1, &c.abort)) {
+        if (!mbar_wait(&B.gfull[g.slot], g.phase, &c.abort) ||
+            !mbar_wait(&B.op_empty[st.slot], st.phase ^ 1u, &c.abort)) {
             ok = false;
             break;
         }
-        const int slot = kk % SG;
-        const uint8_t *sb = stg + (uint32_t)slot * kWarpSlotBytes;
-        const uint32_t my_m = meta[slot * 32 + lane];
-        uint8_t *ob = smem + a.off_op + (uint32_t)s * kStageBytes;
-        const uint32_t chunk_off = (uint32_t)(lane & 3) * 4u;
-        const uint32_t chunk_id = (uint32_t)lane >> 2;
-#pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
-            const uint32_t mj = __shfl_sync(kFullMask, my_m, j);
-            uint32_t v = 0;
-            if (mj & 4u)
-                v = *reinterpret_cast<const uint32_t *>(sb + j * kWinBytes +
-                                                        ((mj & 3u) + (uint32_t)lane) * 4u);
-            const uint32_t r = (uint32_t)(pw * 32 + j);
-            *reinterpret_cast<uint32_t *>(ob + r * 128u + ((chunk_id ^ (r & 7u)) << 4) +
-                                          chunk_off) = v;
+        const uint32_t m = meta[g.slot * kTileTokens];
+        const uint4 *win = reinterpret_cast<const uint4 *>(win0 + (uint32_t)g.slot * kSlotBytes);
+        uint32_t w[36];
+#pragma unroll
+        for (int q = 0; q < 9; ++q) {
+            const uint4 v = win[q];
+            w[4 * q + 0] = v.x;
+            w[4 * q + 1] = v.y;
+            w[4 * q + 2] = v.z;
+            w[4 * q + 3] = v.w;
         }
-        float sc = 0.0f;
-        if (my_m & 4u)
-            sc = *reinterpret_cast<const float *>(sb + lane * kWinBytes + ((my_m & 3u) + 32u) * 4u);
-        sring[(kk % a.RS) * kTileTokens + lane_tok] = sc;
+        // word k of the row is window word k + (m & 3): shift by 1, then by 2
+        const bool s1 = (m & 1u) != 0, s2 = (m & 2u) != 0;
+#pragma unroll
+        for (int k = 0; k < 35; ++k)
+            w[k] = s1 ? w[k + 1] : w[k];
+#pragma unroll
+        for (int k = 0; k < 33; ++k)
+            w[k] = s2 ? w[k + 2] : w[k];
+        const bool valid = (m & 4u) != 0;
+        uint8_t *ob = op_row + (uint32_t)st.slot * kStageBytes;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = valid ? make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3])
+                                  : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(ob + (((uint32_t)ch ^ (r & 7u)) << 4)) = v;
+        }
+        sring[sr.slot * kTileTokens] = valid ? __uint_as_float(w[32]) : 0.0f;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&B.op_full[s]);
-            mbar_arrive(&B.sfull[kk % a.RS]);
+            mbar_arrive(&B.op_full[st.slot]);
+            mbar_arrive(&B.sfull[sr.slot]);
+            mbar_arrive(&B.gempty[g.slot]);
         }
+        g.advance();
+        st.advance();
+        sr.advance();
     }
-    cp_async_wait_all();
     if (!ok)
         raise_abort(a, c);
 }
@@ -402,45 +481,48 @@ static __device__ void gather_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, 
 static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
 {
     const Bars B(a, smem);
-    const int N = a.N, count = (int)c.count;
+    const int N = a.N, count = (int)c.count, cols = a.cols;
     const uint32_t tbase = c.tmem_base;
+    const uint32_t op0 = smem_u32(smem + a.off_op), q0 = smem_u32(smem + a.off_q);
+    const uint32_t q_bytes = (uint32_t)N * kHeadDim;
     TileIter it;
-    it.init(a, c.i0, c.m0);
-    uint32_t req = 0;
+    it.init(a, c);
+    Ring st(a.S), tb(a.NBUF), q(a.QS);
     bool ok = true;
     for (int kk = 0; kk < count; ++kk) {
-        const int s = kk % a.S, b = kk % a.NBUF;
-        const uint32_t qs = req % a.QS;
         const bool first = kk == 0 || it.m == 0;
-        if (first && !mbar_wait(&B.qfull[qs], (req / a.QS) & 1, &c.abort)) {
+        if (first && !mbar_wait(&B.qfull[q.slot], q.phase, &c.abort)) {
             ok = false;
             break;
         }
-        if (!mbar_wait(&B.op_full[s], (kk / a.S) & 1, &c.abort) ||
-            !mbar_wait(&B.tempty[b], ((kk / a.NBUF) & 1) ^ 1, &c.abort)) {
+        if (!mbar_wait(&B.op_full[st.slot], st.phase, &c.abort) ||
+            !mbar_wait(&B.tempty[tb.slot], tb.phase ^ 1u, &c.abort)) {
             ok = false;
             break;
         }
         tc_fence_after_sync();
-        const uint32_t abase = smem_u32(smem + a.off_op + (uint32_t)s * kStageBytes);
-        const uint32_t bbase = smem_u32(smem + a.off_q + qs * (uint32_t)N * kHeadDim);
+        const uint32_t abase = op0 + (uint32_t)st.slot * kStageBytes;
+        const uint32_t bbase = q0 + (uint32_t)q.slot * q_bytes;
+        const uint32_t dcol = tbase + (uint32_t)(tb.slot * cols);
 #pragma unroll
         for (int k4 = 0; k4 < kHeadDim / 32; ++k4) {
             const uint64_t ad = sw128_kmajor_desc(abase + k4 * 32);
             for (int nc = 0; nc * 256 < N; ++nc) {
                 const int nw = min(256, N - nc * 256);
                 const uint64_t bd = sw128_kmajor_desc(bbase + nc * 256 * kHeadDim + k4 * 32);
-                umma_e4m3(tbase + (uint32_t)(b * a.cols + nc * 256), ad, bd,
-                          idesc_e4m3_f32(128, nw), k4 > 0 ? 1u : 0u);
+                umma_e4m3(dcol + (uint32_t)(nc * 256), ad, bd, idesc_e4m3_f32(128, nw),
+                          k4 > 0 ? 1u : 0u);
             }
         }
-        umma_commit(&B.op_empty[s]);
-        umma_commit(&B.tfull[b]);
+        umma_commit(&B.op_empty[st.slot]);
+        umma_commit(&B.tfull[tb.slot]);
         if (kk == count - 1 || it.m == it.nt - 1) {
-            umma_commit(&B.qempty[qs]);
-            ++req;
+            umma_commit(&B.qempty[q.slot]);
+            q.advance();
         }
-        it.next(a);
+        it.next();
+        st.advance();
+        tb.advance();
     }
     if (!ok)
         raise_abort(a, c);
@@ -451,168 +533,162 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
 
 // ---------------------------------------------------------------- epilogue
 
-// Scores of rows j = g, g + E, ... for this thread's token: TMEM columns
-// [j*H, j*H + H) of the buffer. Releases the TMEM buffer after the last load.
-template <int H>
-__device__ __forceinline__ void epi_rows(uint32_t taddr, const float *wsl, float sc, int g, int E,
-                                         int nn, float (&logit)[2], uint64_t *tempty_bar,
-                                         int lane)
+// One epilogue chunk: CH consecutive TMEM columns of this thread's lane (32
+// lanes x CH columns per warp, tcgen05.ld of 16 columns at a time).
+template <int CH>
+__device__ __forceinline__ void epi_load(uint32_t taddr, uint32_t (&buf)[CH])
 {
-    constexpr int CH = H >= 32 ? 32 : 16;  // columns per chunk
-    constexpr int CPR = H / CH;            // chunks per row
-    constexpr int MAXC = 2 * CPR;
-    const int rows_here = (nn - g + E - 1) / E;  // 1 or 2
-    const int nchunks = rows_here * CPR;
-    const bool all_pos = __all_sync(kFullMask, !(sc < 0.0f));
-    const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
-    const float mag = fabsf(sc);
-    uint32_t buf[2][CH];
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    logit[0] = logit[1] = 0.f;
-
-    auto issue = [&](int c, uint32_t *dst) {
-        const int u = c / CPR, part = c % CPR;
-        const int j = g + u * E;
-        const uint32_t col = (uint32_t)(j * H + part * CH);
 #pragma unroll
-        for (int q = 0; q < CH / 16; ++q)
-            tmem_ld16(taddr + col + q * 16, dst + q * 16);
-    };
-    issue(0, buf[0]);
+    for (int q = 0; q < CH / 16; ++q)
+        tmem_ld16(taddr + q * 16, buf + q * 16);
+}
+
+template <int CH>
+__device__ __forceinline__ void epi_wait(uint32_t (&buf)[CH])
+{
     tmem_ld_wait();
 #pragma unroll
     for (int q = 0; q < CH / 16; ++q)
-        reg_fence16(buf[0] + q * 16);
+        reg_fence16(buf + q * 16);
+}
+
+// acc += sum over the chunk of w[h] * relu(+-x[h]) (flip: the scale's sign bit).
+template <int CH>
+__device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[CH], const float *w, uint32_t flip,
+                                               float (&acc)[4])
+{
+    const float4 *w4 = reinterpret_cast<const float4 *>(w);
 #pragma unroll
-    for (int c = 0; c < MAXC; ++c) {
-        if (c >= nchunks)
-            break;
-        if (c + 1 < nchunks) {
-            issue(c + 1, buf[(c + 1) & 1]);
-        } else {
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(tempty_bar);
-        }
-        const int u = c / CPR, part = c % CPR;
-        const int j = g + u * E;
-        const float4 *w4 = reinterpret_cast<const float4 *>(wsl + j * H + part * CH);
-        const uint32_t *x = buf[c & 1];
-        if (all_pos) {
-#pragma unroll
-            for (int h = 0; h < CH; h += 4) {
-                const float4 wv = w4[h / 4];
-                acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(x[h + 0]), 0.f), acc[0]);
-                acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(x[h + 1]), 0.f), acc[1]);
-                acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(x[h + 2]), 0.f), acc[2]);
-                acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(x[h + 3]), 0.f), acc[3]);
-            }
-        } else {
-#pragma unroll
-            for (int h = 0; h < CH; h += 4) {
-                const float4 wv = w4[h / 4];
-                acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(x[h + 0] ^ flip), 0.f), acc[0]);
-                acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(x[h + 1] ^ flip), 0.f), acc[1]);
-                acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(x[h + 2] ^ flip), 0.f), acc[2]);
-                acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(x[h + 3] ^ flip), 0.f), acc[3]);
-            }
-        }
-        if (part == CPR - 1) {
-            const float v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * mag;
-            if (u == 0)
-                logit[0] = v;
-            else
-                logit[1] = v;
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        }
-        if (c + 1 < nchunks) {
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < CH / 16; ++q)
-                reg_fence16(buf[(c + 1) & 1] + q * 16);
-        }
+    for (int h = 0; h < CH; h += 4) {
+        const float4 wv = w4[h / 4];
+        acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(x[h + 0] ^ flip), 0.f), acc[0]);
+        acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(x[h + 1] ^ flip), 0.f), acc[1]);
+        acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(x[h + 2] ^ flip), 0.f), acc[2]);
+        acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(x[h + 3] ^ flip), 0.f), acc[3]);
     }
 }
 
 template <int H>
-static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int g, int we)
+static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int we)
 {
     const Bars B(a, smem);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, qd = warp & 3;
     const int r = qd * 32 + lane;  // token row of the tile = TMEM lane
-    const int N = a.N, nn = a.nn, E = a.E;
+    const int N = a.N, nn = a.nn, cols = a.cols;
+    const long long mml = a.mml;
+    float *const logits = a.logits;
+    float *const clogits = a.clogits;
+    uint32_t *const hist = a.hist;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const uint32_t wtid = (uint32_t)(we * 32 + lane);
-    const uint32_t bar_id = 1u + (uint32_t)g;
-    const bool want_hist = a.hist != nullptr;
-    uint32_t *shist = reinterpret_cast<uint32_t *>(smem + a.off_hist) +
-                      (uint32_t)g * (uint32_t)a.rpw * kHistBins;
+    const uint32_t bar_id = 1u;
+    const bool want_hist = hist != nullptr;
+    uint32_t *const shist = reinterpret_cast<uint32_t *>(smem + a.off_hist);
+    const float *const scales = reinterpret_cast<const float *>(smem + a.off_scale) + r;
+    const float *const w_smem = reinterpret_cast<const float *>(smem + a.off_w);
+    const uint32_t tlane = c.tmem_base + ((uint32_t)(qd * 32) << 16);
     const uint64_t keep_pol = l2_evict_last_policy();
-    const int rows_here = (nn - g + E - 1) / E;
+    constexpr int CH = H >= 64 ? 32 : 16;  // TMEM columns per epilogue chunk
+    constexpr int CPR = H / CH;            // chunks per draft row
 
-    // -inf beyond the last tile of each row: this CTA's share of every row
-    if (a.logits) {
-        const int etid = g * 128 + (int)wtid, ethr = E * 128;
-        for (int rr = 0; rr < a.bs * nn; ++rr) {
-            const int cx = ctx_of(a, rr / nn);
-            const long long lo =
-                min((long long)(cx + kTileTokens - 1) / kTileTokens * kTileTokens, (long long)a.mml);
-            const long long L = a.mml - lo;
-            const long long s0 = lo + L * blockIdx.x / gridDim.x;
-            const long long s1 = lo + L * (blockIdx.x + 1) / gridDim.x;
-            float *row = a.logits + (long long)rr * a.mml;
-            for (long long t = s0 + etid; t < s1; t += ethr)
-                row[t] = NEG_INF;
+    // -inf beyond the last tile of each row: this CTA's share of every row.
+    // Each warp takes 32 rows at a time (one coalesced load of their context
+    // lengths), then writes the rows' shares one after another.
+    if (logits) {
+        const int rows = a.bs * nn;
+        for (int base = we * 32; base < rows; base += 4 * 32) {
+            const int my_row = base + lane;
+            const int my_cx = my_row < rows ? ctx_of(a, my_row / nn) : 0;
+            const int nr = min(32, rows - base);
+            for (int u = 0; u < nr; ++u) {
+                const int cx = __shfl_sync(kFullMask, my_cx, u);
+                const long long lo =
+                    min((long long)(cx + kTileTokens - 1) / kTileTokens * kTileTokens, mml);
+                const long long L = mml - lo;
+                const long long s0 = lo + L * blockIdx.x / gridDim.x;
+                const long long s1 = lo + L * (blockIdx.x + 1) / gridDim.x;
+                float *row = logits + (long long)(base + u) * mml;
+                for (long long t = s0 + lane; t < s1; t += 32)
+                    row[t] = NEG_INF;
+            }
         }
     }
     if (want_hist) {
-        for (int e = (int)wtid; e < a.rpw * kHistBins; e += 128)
+        for (int e = (int)wtid; e < nn * kHistBins; e += 128)
             shist[e] = 0;
         named_bar_sync(bar_id, 128);
     }
 
     const int count = (int)c.count;
     TileIter it;
-    it.init(a, c.i0, c.m0);
-    uint32_t req = 0;
+    it.init(a, c);
+    Ring tb(a.NBUF), q(a.QS), sr(a.RS);
     // Waits that fail (abort or time limit) skip the data work but keep the
     // work group's barrier schedule, so no warp is left waiting on another.
     for (int kk = 0; kk < count; ++kk) {
-        const int b = kk % a.NBUF;
-        const uint32_t qs = req % a.QS;
         const bool first = kk == 0 || it.m == 0;
         bool ok = true;
         if (first)
-            ok = mbar_wait(&B.qfull[qs], (req / a.QS) & 1, &c.abort);
-        const int sri = kk % a.RS;
-        ok = ok && mbar_wait(&B.sfull[sri], (uint32_t)(kk / a.RS) & 1u, &c.abort) &&
-             mbar_wait(&B.tfull[b], (kk / a.NBUF) & 1, &c.abort);
+            ok = mbar_wait(&B.qfull[q.slot], q.phase, &c.abort);
+        ok = ok && mbar_wait(&B.sfull[sr.slot], sr.phase, &c.abort) &&
+             mbar_wait(&B.tfull[tb.slot], tb.phase, &c.abort);
         if (ok) {
             tc_fence_after_sync();
-            const float sc =
-                reinterpret_cast<const float *>(smem + a.off_scale)[sri * kTileTokens + r];
+            const float sc = scales[sr.slot * kTileTokens];
             const int t = it.m * kTileTokens + r;
-            const float *wsl =
-                reinterpret_cast<const float *>(smem + a.off_w + qs * (uint32_t)N * 4);
-            const uint32_t taddr =
-                c.tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * a.cols);
-            float logit[2];
-            epi_rows<H>(taddr, wsl, sc, g, E, nn, logit, &B.tempty[b], lane);
-            for (int u = 0; u < rows_here; ++u) {
-                const int j = g + u * E;
+            const float *wsl = w_smem + q.slot * N;
+            const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
+            const float mag = fabsf(sc);
+            const uint32_t taddr = tlane + (uint32_t)(tb.slot * cols);
+            // Draft row j's score is sum_h w[j][h] * relu(sc * x[j][h]) =
+            // |sc| * sum_h w[j][h] * relu(+-x[j][h]), x in TMEM columns
+            // [j*H, j*H + H): CPR chunks of CH columns, two register buffers,
+            // the next chunk's load (of this row or the next) in flight while
+            // the current one is reduced.
+            uint32_t buf[2][CH];
+            epi_load<CH>(taddr, buf[0]);
+            epi_wait<CH>(buf[0]);
+            for (int j = 0; j < nn; ++j) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t tj = taddr + (uint32_t)(j * H);
+#pragma unroll
+                for (int part = 0; part < CPR; ++part) {
+                    // with CPR even the last part sits in buf[1], so buf[0]
+                    // can take the next row's first chunk
+                    const bool next_row = part + 1 == CPR && (CPR % 2 == 0) && j + 1 < nn;
+                    if (part + 1 < CPR)
+                        epi_load<CH>(tj + (uint32_t)((part + 1) * CH), buf[(part + 1) & 1]);
+                    else if (next_row)
+                        epi_load<CH>(tj + (uint32_t)H, buf[0]);
+                    epi_accumulate<CH>(buf[part & 1], wsl + j * H + part * CH, flip, acc);
+                    if (part + 1 < CPR)
+                        epi_wait<CH>(buf[(part + 1) & 1]);
+                    else if (next_row)
+                        epi_wait<CH>(buf[0]);
+                    else if (CPR % 2 != 0 && j + 1 < nn) {
+                        epi_load<CH>(tj + (uint32_t)H, buf[0]);
+                        epi_wait<CH>(buf[0]);
+                    }
+                }
+                if (j == nn - 1) {  // every TMEM read of this buffer has completed
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&B.tempty[tb.slot]);
+                }
+                const float lj = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * mag;
                 const long long row = (long long)it.i * nn + j;
                 const bool valid = t < valid_len(it.ctx, nn, j);
-                if (a.logits && t < a.mml)
-                    a.logits[row * a.mml + t] = valid ? logit[u] : NEG_INF;
-                if (a.clogits && valid)
-                    st_global_hint(a.clogits + row * a.mml + t, logit[u], keep_pol);
+                if (logits && t < mml)
+                    logits[row * mml + t] = valid ? lj : NEG_INF;
+                if (clogits && valid)
+                    st_global_hint(clogits + row * mml + t, lj, keep_pol);
                 if (want_hist) {
-                    const uint32_t bin = f32_order_key(logit[u]) >> kHistShift;
+                    const uint32_t bin = f32_order_key(lj) >> kHistShift;
                     const uint32_t grp =
                         __match_any_sync(kFullMask, valid ? bin : 0x10000u + (uint32_t)lane);
                     if (valid && (__ffs(grp) - 1) == lane)
-                        atomicAdd(shist + u * kHistBins + bin, (uint32_t)__popc(grp));
+                        atomicAdd(shist + j * kHistBins + bin, (uint32_t)__popc(grp));
                 }
             }
         } else {
@@ -621,12 +697,12 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
         if (kk == count - 1 || it.m == it.nt - 1) {
             if (want_hist) {
                 named_bar_sync(bar_id, 128);
-                for (int u = 0; u < rows_here; ++u) {
-                    const long long row = (long long)it.i * nn + g + u * E;
+                for (int u = 0; u < nn; ++u) {
+                    const long long row = (long long)it.i * nn + u;
                     for (int e = (int)wtid; e < kHistBins; e += 128) {
                         const uint32_t v = shist[u * kHistBins + e];
                         if (v) {
-                            atomicAdd(a.hist + row * kHistBins + e, v);
+                            atomicAdd(hist + row * kHistBins + e, v);
                             shist[u * kHistBins + e] = 0;
                         }
                     }
@@ -635,16 +711,18 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
             }
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&B.qempty[qs]);
-            ++req;
+                mbar_arrive(&B.qempty[q.slot]);
+            q.advance();
         }
-        it.next(a);
+        it.next();
+        tb.advance();
+        sr.advance();
     }
 }
 
 // ---------------------------------------------------------------- kernel
 
-constexpr int kMaxThreads = 32 * (kFirstEpiWarp + 8);
+constexpr int kMaxThreads = 32 * 16;
 
 template <int H>
 __global__ void __launch_bounds__(kMaxThreads, 1)
@@ -660,19 +738,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         ctl.abort = 0;
         const Bars B(a, smem);
         for (int s = 0; s < a.S; ++s) {
-            mbar_init(&B.op_full[s], kPRWarps);
+            mbar_init(&B.op_full[s], kRepackWarps);
             mbar_init(&B.op_empty[s], 1);
+        }
+        for (int g = 0; g < a.SG; ++g) {
+            mbar_init(&B.gfull[g], 2 * 32 * kGatherWarps);
+            mbar_init(&B.gempty[g], kRepackWarps);
         }
         for (int b = 0; b < a.NBUF; ++b) {
             mbar_init(&B.tfull[b], 1);
-            mbar_init(&B.tempty[b], 4 * a.E);
+            mbar_init(&B.tempty[b], 4);
         }
         for (int q = 0; q < a.QS; ++q) {
             mbar_init(&B.qfull[q], 1);
-            mbar_init(&B.qempty[q], 1 + 4 * a.E);
+            mbar_init(&B.qempty[q], 1 + 4);
         }
         for (int q = 0; q < a.RS; ++q)
-            mbar_init(&B.sfull[q], kPRWarps);
+            mbar_init(&B.sfull[q], kRepackWarps);
         mbar_init(B.done, 1);
         mbar_init_fence();
     }
@@ -683,6 +765,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     balance_schedule(
         a.bs, [&](int i) { return (long long)((ctx_of(a, i) + kTileTokens - 1) / kTileTokens); },
         ctl);
+    for (int n = threadIdx.x; n < kCtxCache; n += blockDim.x)
+        ctl.ctx[n] = ctl.i0 + n < a.bs ? ctx_of(a, ctl.i0 + n) : 0;
     if (blockIdx.x == 0) {
         const long long lim = min((long long)a.mml, (long long)a.W * a.P);
         for (int i = threadIdx.x; i < a.bs; i += blockDim.x) {
@@ -695,19 +779,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
 
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         if ((threadIdx.x & 31) == 0)
             mma_role(a, smem, ctl);
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == kQloadWarp) {
         if ((threadIdx.x & 31) == 0)
             qload_role(a, smem, ctl);
         __syncwarp();
-    } else if (warp < kFirstEpiWarp) {
-        gather_role(a, smem, ctl, warp - kFirstPRWarp);
-    } else {
-        const int e = warp - kFirstEpiWarp;
-        epilogue_role<H>(a, smem, ctl, e >> 2, e & 3);
+    } else if (warp < kQloadWarp) {
+        if ((warp & 2) == 0)
+            gather_role(a, smem, ctl, row_block_of(warp));
+        else
+            repack_role(a, smem, ctl, row_block_of(warp));
+    } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) {
+        epilogue_role<H>(a, smem, ctl, warp - kFirstEpiWarp);
     }
 
     tc_fence_before_sync();

@@ -120,6 +120,16 @@ __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, 
                  : "memory");
 }
 
+// 16-byte asynchronous copy that reads only the first src_bytes (1..16) bytes of
+// src and zero-fills the rest of the 16-byte destination.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src, uint32_t src_bytes,
+                                                  uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+                 "l"(src), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 // Expect `bytes` more transaction bytes on the barrier and arrive once.
@@ -158,6 +168,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 __device__ __forceinline__ void st_global_hint(float *p, float v, uint64_t policy)
 {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy)
+                 : "memory");
+}
+
+// Arrive on the mbarrier once all of this thread's prior cp.async copies have
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
 
