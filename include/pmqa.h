@@ -72,8 +72,9 @@ enum { PMQA_OP_LOGITS = 0, PMQA_OP_TOPK = 1, PMQA_OP_LOGITS_TOPK = 2 };
  * One decode-step problem, in the argument order of the reference function
  * (q, kv_cache, weights, context_lens, block_tables, max_model_len) plus sizes.
  *   q             fp8 e4m3fn [bs, next_n, heads, head_dim], contiguous, 16-byte aligned
- *   kv_cache      uint8 [num_blocks, block_size, head_dim + 4], contiguous, 4-byte aligned:
- *                 per token head_dim fp8 bytes then a little-endian fp32 scale
+ *   kv_cache      uint8 [num_blocks, block_size, head_dim + 4], contiguous, 16-byte
+ *                 aligned (rows are read as 16-byte aligned windows): per token
+ *                 head_dim fp8 bytes then a little-endian fp32 scale
  *   weights       fp32 [bs * next_n, heads], contiguous, 16-byte aligned
  *   context_lens  int32 [bs]
  *   block_tables  int32 [bs, max_blocks_per_seq], row-major; only the first

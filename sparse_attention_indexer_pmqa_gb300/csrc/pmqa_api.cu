@@ -95,7 +95,7 @@ int check_problem(const pmqa_problem *p)
         return PMQA_OK;
     if (!p->q || !p->kv_cache || !p->weights || !p->context_lens || !p->block_tables)
         return PMQA_ERR_INVALID_ARG;
-    if (!aligned(p->q, 16) || !aligned(p->weights, 16) || !aligned(p->kv_cache, 4) ||
+    if (!aligned(p->q, 16) || !aligned(p->weights, 16) || !aligned(p->kv_cache, 16) ||
         !aligned(p->context_lens, 4) || !aligned(p->block_tables, 4))
         return PMQA_ERR_INVALID_ARG;
     return PMQA_OK;

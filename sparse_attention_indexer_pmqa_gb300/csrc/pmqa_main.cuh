@@ -87,8 +87,8 @@ struct MainArgs {
 constexpr int kCtxCache = 512;  // context lengths of the CTA's first requests, in smem
 
 struct CtaCtl {
-    long long red[16];
-    int wsum[16];
+    long long red[32];  // per-warp partial sums (up to 32 warps)
+    int wsum[32];
     long long start, count;
     int i0, m0;
     int abort;
@@ -504,7 +504,8 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
         const uint32_t abase = op0 + (uint32_t)st.slot * kStageBytes;
         const uint32_t bbase = q0 + (uint32_t)q.slot * q_bytes;
         const uint32_t dcol = tbase + (uint32_t)(tb.slot * cols);
-#pragma unroll
+        // rolled: the issuing thread's loop stays small in the instruction cache
+#pragma unroll 1
         for (int k4 = 0; k4 < kHeadDim / 32; ++k4) {
             const uint64_t ad = sw128_kmajor_desc(abase + k4 * 32);
             for (int nc = 0; nc * 256 < N; ++nc) {
@@ -533,38 +534,83 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
 
 // ---------------------------------------------------------------- epilogue
 
-// One epilogue chunk: CH consecutive TMEM columns of this thread's lane (32
-// lanes x CH columns per warp, tcgen05.ld of 16 columns at a time).
-template <int CH>
-__device__ __forceinline__ void epi_load(uint32_t taddr, uint32_t (&buf)[CH])
-{
-#pragma unroll
-    for (int q = 0; q < CH / 16; ++q)
-        tmem_ld16(taddr + q * 16, buf + q * 16);
-}
+// One epilogue chunk: 16 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void epi_load(uint32_t taddr, uint32_t (&buf)[16]) { tmem_ld16(taddr, buf); }
 
-template <int CH>
-__device__ __forceinline__ void epi_wait(uint32_t (&buf)[CH])
+__device__ __forceinline__ void epi_wait(uint32_t (&buf)[16])
 {
     tmem_ld_wait();
-#pragma unroll
-    for (int q = 0; q < CH / 16; ++q)
-        reg_fence16(buf + q * 16);
+    reg_fence16(buf);
 }
 
-// acc += sum over the chunk of w[h] * relu(+-x[h]) (flip: the scale's sign bit).
-template <int CH>
-__device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[CH], const float *w, uint32_t flip,
+// acc += sum over a 16-column chunk of w[h] * relu(x[h]) (SIGNED: of
+// relu(-x[h]) when the thread's scale is negative, flip = its sign bit).
+// Packed fp32x2 multiply-adds; the weights come as float4 broadcasts.
+template <bool SIGNED>
+__device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[16], const float *w, uint32_t flip,
                                                float (&acc)[4])
 {
     const float4 *w4 = reinterpret_cast<const float4 *>(w);
 #pragma unroll
-    for (int h = 0; h < CH; h += 4) {
+    for (int h = 0; h < 16; h += 4) {
         const float4 wv = w4[h / 4];
-        acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(x[h + 0] ^ flip), 0.f), acc[0]);
-        acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(x[h + 1] ^ flip), 0.f), acc[1]);
-        acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(x[h + 2] ^ flip), 0.f), acc[2]);
-        acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(x[h + 3] ^ flip), 0.f), acc[3]);
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            v[u] = fmaxf(__uint_as_float(SIGNED ? (x[h + u] ^ flip) : x[h + u]), 0.f);
+        ffma2(acc[0], acc[1], wv.x, wv.y, v[0], v[1]);
+        ffma2(acc[2], acc[3], wv.z, wv.w, v[2], v[3]);
+    }
+}
+
+// All draft rows of one tile for this thread's token (TMEM lane): row j's
+// score sum_h w[j][h] * relu(sc * x[j][h]) = |sc| * sum_h w[j][h] *
+// relu(+-x[j][h]), x in TMEM columns [j*H, j*H + H), walked as 16-column
+// chunks in two register buffers with the next chunk (of this row or the
+// next) loading while the current one is reduced. Calls out(j, score) per
+// row; arrives on tempty once the last TMEM read has completed.
+template <int H, bool SIGNED, class Out>
+__device__ __forceinline__ void epi_tile(uint32_t taddr, const float *wsl, uint32_t flip, float mag,
+                                         int nn, uint64_t *tempty_bar, int lane, Out &&out)
+{
+    constexpr int CPR = H / 16;  // chunks per draft row
+    uint32_t b0[16], b1[16];
+    epi_load(taddr, b0);
+    epi_wait(b0);
+    for (int j = 0; j < nn; ++j) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t tj = taddr + (uint32_t)(j * H);
+        const float *wj = wsl + j * H;
+        const bool more_rows = j + 1 < nn;
+        // b0 holds chunk p of row j (p even) on entry of each pass
+#pragma unroll 1
+        for (int p = 0; p < CPR; p += 2) {
+            const bool has1 = p + 1 < CPR;
+            const bool next_here = p + 2 < CPR;
+            const bool has_next = next_here || more_rows;
+            const uint32_t next_addr = next_here ? tj + (uint32_t)((p + 2) * 16) : tj + (uint32_t)H;
+            if (has1) {
+                epi_load(tj + (uint32_t)((p + 1) * 16), b1);
+                epi_accumulate<SIGNED>(b0, wj + p * 16, flip, acc);
+                epi_wait(b1);
+                if (has_next)
+                    epi_load(next_addr, b0);
+                epi_accumulate<SIGNED>(b1, wj + (p + 1) * 16, flip, acc);
+            } else {
+                epi_accumulate<SIGNED>(b0, wj + p * 16, flip, acc);
+                if (has_next)
+                    epi_load(next_addr, b0);
+            }
+            if (has_next)
+                epi_wait(b0);
+        }
+        if (!more_rows) {  // every TMEM read of this buffer has completed
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(tempty_bar);
+        }
+        out(j, ((acc[0] + acc[1]) + (acc[2] + acc[3])) * mag);
     }
 }
 
@@ -581,6 +627,7 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
     uint32_t *const hist = a.hist;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const uint32_t wtid = (uint32_t)(we * 32 + lane);
+    constexpr int kEpiThreads = 128;
     const uint32_t bar_id = 1u;
     const bool want_hist = hist != nullptr;
     uint32_t *const shist = reinterpret_cast<uint32_t *>(smem + a.off_hist);
@@ -588,15 +635,13 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
     const float *const w_smem = reinterpret_cast<const float *>(smem + a.off_w);
     const uint32_t tlane = c.tmem_base + ((uint32_t)(qd * 32) << 16);
     const uint64_t keep_pol = l2_evict_last_policy();
-    constexpr int CH = H >= 64 ? 32 : 16;  // TMEM columns per epilogue chunk
-    constexpr int CPR = H / CH;            // chunks per draft row
 
     // -inf beyond the last tile of each row: this CTA's share of every row.
     // Each warp takes 32 rows at a time (one coalesced load of their context
     // lengths), then writes the rows' shares one after another.
     if (logits) {
         const int rows = a.bs * nn;
-        for (int base = we * 32; base < rows; base += 4 * 32) {
+        for (int base = we * 32; base < rows; base += kEpiThreads) {
             const int my_row = base + lane;
             const int my_cx = my_row < rows ? ctx_of(a, my_row / nn) : 0;
             const int nr = min(32, rows - base);
@@ -614,9 +659,9 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
         }
     }
     if (want_hist) {
-        for (int e = (int)wtid; e < nn * kHistBins; e += 128)
+        for (int e = (int)wtid; e < nn * kHistBins; e += kEpiThreads)
             shist[e] = 0;
-        named_bar_sync(bar_id, 128);
+        named_bar_sync(bar_id, kEpiThreads);
     }
 
     const int count = (int)c.count;
@@ -632,6 +677,8 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
             ok = mbar_wait(&B.qfull[q.slot], q.phase, &c.abort);
         ok = ok && mbar_wait(&B.sfull[sr.slot], sr.phase, &c.abort) &&
              mbar_wait(&B.tfull[tb.slot], tb.phase, &c.abort);
+        // one outcome per warp: the tile body uses warp-wide shuffles and votes
+        ok = __all_sync(kFullMask, ok);
         if (ok) {
             tc_fence_after_sync();
             const float sc = scales[sr.slot * kTileTokens];
@@ -640,43 +687,7 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
             const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
             const float mag = fabsf(sc);
             const uint32_t taddr = tlane + (uint32_t)(tb.slot * cols);
-            // Draft row j's score is sum_h w[j][h] * relu(sc * x[j][h]) =
-            // |sc| * sum_h w[j][h] * relu(+-x[j][h]), x in TMEM columns
-            // [j*H, j*H + H): CPR chunks of CH columns, two register buffers,
-            // the next chunk's load (of this row or the next) in flight while
-            // the current one is reduced.
-            uint32_t buf[2][CH];
-            epi_load<CH>(taddr, buf[0]);
-            epi_wait<CH>(buf[0]);
-            for (int j = 0; j < nn; ++j) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t tj = taddr + (uint32_t)(j * H);
-#pragma unroll
-                for (int part = 0; part < CPR; ++part) {
-                    // with CPR even the last part sits in buf[1], so buf[0]
-                    // can take the next row's first chunk
-                    const bool next_row = part + 1 == CPR && (CPR % 2 == 0) && j + 1 < nn;
-                    if (part + 1 < CPR)
-                        epi_load<CH>(tj + (uint32_t)((part + 1) * CH), buf[(part + 1) & 1]);
-                    else if (next_row)
-                        epi_load<CH>(tj + (uint32_t)H, buf[0]);
-                    epi_accumulate<CH>(buf[part & 1], wsl + j * H + part * CH, flip, acc);
-                    if (part + 1 < CPR)
-                        epi_wait<CH>(buf[(part + 1) & 1]);
-                    else if (next_row)
-                        epi_wait<CH>(buf[0]);
-                    else if (CPR % 2 != 0 && j + 1 < nn) {
-                        epi_load<CH>(tj + (uint32_t)H, buf[0]);
-                        epi_wait<CH>(buf[0]);
-                    }
-                }
-                if (j == nn - 1) {  // every TMEM read of this buffer has completed
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&B.tempty[tb.slot]);
-                }
-                const float lj = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * mag;
+            auto out = [&](int j, float lj) {
                 const long long row = (long long)it.i * nn + j;
                 const bool valid = t < valid_len(it.ctx, nn, j);
                 if (logits && t < mml)
@@ -690,16 +701,21 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
                     if (valid && (__ffs(grp) - 1) == lane)
                         atomicAdd(shist + j * kHistBins + bin, (uint32_t)__popc(grp));
                 }
-            }
+            };
+            // negative scales are legal but rare: a separate (cold) path
+            if (__all_sync(kFullMask, flip == 0u))
+                epi_tile<H, false>(taddr, wsl, flip, mag, nn, &B.tempty[tb.slot], lane, out);
+            else
+                epi_tile<H, true>(taddr, wsl, flip, mag, nn, &B.tempty[tb.slot], lane, out);
         } else {
             raise_abort(a, c);
         }
         if (kk == count - 1 || it.m == it.nt - 1) {
             if (want_hist) {
-                named_bar_sync(bar_id, 128);
+                named_bar_sync(bar_id, kEpiThreads);
                 for (int u = 0; u < nn; ++u) {
                     const long long row = (long long)it.i * nn + u;
-                    for (int e = (int)wtid; e < kHistBins; e += 128) {
+                    for (int e = (int)wtid; e < kHistBins; e += kEpiThreads) {
                         const uint32_t v = shist[u * kHistBins + e];
                         if (v) {
                             atomicAdd(hist + row * kHistBins + e, v);
@@ -707,7 +723,7 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
                         }
                     }
                 }
-                named_bar_sync(bar_id, 128);
+                named_bar_sync(bar_id, kEpiThreads);
             }
             __syncwarp();
             if (lane == 0)
@@ -723,6 +739,7 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
 // ---------------------------------------------------------------- kernel
 
 constexpr int kMaxThreads = 32 * 16;
+static_assert(kMaxThreads <= 32 * 32, "CtaCtl holds per-warp sums for at most 32 warps");
 
 template <int H>
 __global__ void __launch_bounds__(kMaxThreads, 1)

@@ -130,6 +130,19 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src,
                  : "memory");
 }
 
+// (a0, a1) += (w0, w1) * (x0, x1): one packed fp32x2 fused multiply-add.
+__device__ __forceinline__ void ffma2(float &a0, float &a1, float w0, float w1, float x0, float x1)
+{
+    asm("{\n\t.reg .b64 ra, rw, rx;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rw, {%2, %3};\n\t"
+        "mov.b64 rx, {%4, %5};\n\t"
+        "fma.rn.f32x2 ra, rw, rx, ra;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
 // ---------------------------------------------------------------- TMA
 
 // Expect `bytes` more transaction bytes on the barrier and arrive once.

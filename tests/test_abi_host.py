@@ -81,6 +81,7 @@ WS = ctypes.c_void_p(0x100000)
     (dict(q=0x10004), pmqa.PMQA_ERR_INVALID_ARG),
     (dict(weights=0x30008), pmqa.PMQA_ERR_INVALID_ARG),
     (dict(kv_cache=0x20002), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(kv_cache=0x20004), pmqa.PMQA_ERR_INVALID_ARG),
 ])
 def test_problem_validation(lib, kw, code):
     p = _problem(**kw)
