@@ -1,11 +1,13 @@
 #!/usr/bin/env python
 """Throughput of the fused FP8 paged MQA-logits + per-row top-k path on GB300.
 
-One step = one pmqa_logits_topk call over one decode batch (block-table KV
-gather, FP8 q.K^T on tensor cores, relu-weighted head sum with masks, per-row
-top-k). Inputs are synthetic (synth.config_problem) and resident in HBM; L2 is
-flushed (256 MB write) before every timed step, and each step is timed with
-CUDA events on the launching stream.
+One step = the fused call over one decode batch (block-table KV gather, FP8
+q.K^T on tensor cores, relu-weighted head sum with masks, per-row top-k),
+issued as its two launches (pmqa_logits_topk_stages SCORE, then SELECT) with a
+CUDA event before, between and after them on the launching stream, so the KV
+pass (the dominant kernel) is timed on its own. Inputs are synthetic
+(synth.config_problem) and resident in HBM; L2 is flushed (256 MB write)
+before every timed step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C0..C4] [--all]
     python bench.py --impl reference ...   # the CPU oracle on the same workload
@@ -125,7 +127,18 @@ def measured_traffic(workload: str):
     return float(rec["dram_bytes_per_launch"])
 
 
+def valid_positions(prob) -> int:
+    """Sum over query rows of the positions the causal window admits."""
+    total = 0
+    for c in prob.context_lens.tolist():
+        for j in range(prob.next_n):
+            total += max(0, min(c - prob.next_n + j + 1, c))
+    return total
+
+
 def algorithmic_bytes(prob, k: int, logits_written: bool = False) -> dict:
+    """Bytes the fused step must move at minimum: each KV row once (132 B per
+    token), the block-table entries, q, weights and lengths, and its outputs."""
     import numpy as np
 
     ctx = prob.context_lens.astype(np.int64)
@@ -140,6 +153,26 @@ def algorithmic_bytes(prob, k: int, logits_written: bool = False) -> dict:
     }
     if logits_written:
         parts["logits"] = 4 * rows * prob.max_model_len
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+def score_kernel_bytes(prob) -> dict:
+    """Algorithmic bytes of one launch of the KV pass (SCORE stage): every KV
+    row of every request once, its table entries, q, weights, lengths, and the
+    compact logits it writes for the selection (4 B per admitted position)."""
+    import numpy as np
+
+    ctx = prob.context_lens.astype(np.int64)
+    rows = prob.bs * prob.next_n
+    parts = {
+        "kv": 132 * int(ctx.sum()),
+        "block_table": 4 * int(((ctx + prob.block_size - 1) // prob.block_size).sum()),
+        "q": int(prob.q.size),
+        "weights": 4 * rows * prob.heads,
+        "context_lens": 4 * prob.bs,
+        "compact_logits": 4 * valid_positions(prob),
+    }
     parts["total"] = sum(parts.values())
     return parts
 
@@ -223,6 +256,25 @@ def time_steps(step, steps: int, flush) -> list:
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
+def time_staged_steps(stages, steps: int, flush):
+    """Per-step device times (ms) of a step made of several launches: events
+    before, between and after them; returns (step times, per-launch times)."""
+    import torch
+
+    n = len(stages)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    for ev in evs:
+        flush()
+        ev[0].record()
+        for i, st in enumerate(stages):
+            st()
+            ev[i + 1].record()
+    torch.cuda.synchronize()
+    total = [ev[0].elapsed_time(ev[n]) for ev in evs]
+    parts = [[ev[i].elapsed_time(ev[i + 1]) for ev in evs] for i in range(n)]
+    return total, parts
+
+
 def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
     import torch
 
@@ -241,19 +293,27 @@ def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
     def flush():
         flush_buf.zero_()
 
+    args_ = (d["q"], d["kv"], d["w"], d["ctx"], d["bt"], prob.max_model_len, k)
+
     def step():
-        pmqa.pmqa_logits_topk(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], prob.max_model_len, k,
-                              idx=idx, ws=ws)
+        pmqa.pmqa_logits_topk(*args_, idx=idx, ws=ws)
+
+    def stage_score():
+        pmqa.pmqa_logits_topk_stages(*args_, pmqa.PMQA_STAGE_SCORE, idx=idx, ws=ws)
+
+    def stage_select():
+        pmqa.pmqa_logits_topk_stages(*args_, pmqa.PMQA_STAGE_SELECT, idx=idx, ws=ws)
 
     for _ in range(args.warmup):
         flush()
-        step()
+        stage_score()
+        stage_select()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    times = time_steps(step, args.steps, flush)
+    times, (t_score, t_select) = time_staged_steps([stage_score, stage_select], args.steps, flush)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -264,7 +324,9 @@ def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
     ms = statistics.fmean(times)
     ms_max = max_over_ranks(ms, dist, device)
     out = {"prob": prob, "ms": ms_max, "ms_median": statistics.median(times), "wall_s": wall,
-           "times": times}
+           "times": times, "ms_score": max_over_ranks(statistics.fmean(t_score), dist, device),
+           "ms_select": max_over_ranks(statistics.fmean(t_select), dist, device),
+           "launches_per_step": 2}
 
     if with_paths:
         logits = torch.empty((rows, prob.max_model_len), dtype=torch.float32, device=device)
@@ -285,7 +347,9 @@ def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
         out["paths_ms"] = {
             "pmqa_logits": statistics.fmean(time_steps(step_logits, n, flush)),
             "pmqa_topk": statistics.fmean(time_steps(step_topk, n, flush)),
-            "pmqa_logits_topk": ms,
+            "pmqa_logits_topk (SCORE + SELECT)": ms,
+            "SCORE (KV pass)": out["ms_score"],
+            "SELECT": out["ms_select"],
         }
         del logits
 
@@ -308,7 +372,7 @@ def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
     return out
 
 
-def cpu_baseline(prob, min_seconds: float = 10.0, max_reps: int = 3):
+def cpu_baseline(prob, min_seconds: float = 10.0, max_reps: int = 60):
     """The oracle, as it stands, on the whole workload (logits + top-k)."""
     import oracle
 
@@ -352,7 +416,8 @@ def run_ours(args):
     value = tokens_all / (ms * 1e-3)
     peak, peak_kind = read_peak()
     ab = algorithmic_bytes(prob, prob.k)
-    achieved = ab["total"] / (res["ms"] * 1e-3) / 1e9
+    sb = score_kernel_bytes(prob)
+    achieved = sb["total"] / (res["ms_score"] * 1e-3) / 1e9
     traffic = measured_traffic(args.workload)
     line = {
         "metric": METRIC,
@@ -375,14 +440,15 @@ def run_ours(args):
             "l2": "flushed before every timed step (256 MB device write, not timed)",
             "parallelism": f"replicas x{world}",
         },
-        "hbm_gbs": achieved,
+        "hbm_gbs": ab["total"] / (ms * 1e-3) / 1e9,
         "kv_stream_gbs": ab["kv"] / (ms * 1e-3) / 1e9,
         "topk_rows_per_s": world * prob.rows / (ms * 1e-3),
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-            "kernel": "pmqa_main_kernel<64,true> (fused logits + top-k)",
-            "algorithmic_bytes_per_launch": ab,
+            "kernel": f"pmqa_main_kernel<{prob.heads}> (SCORE stage of the fused call)",
+            "kernel_ms": res["ms_score"],
+            "algorithmic_bytes_per_launch": sb,
         },
         "e2e": {
             "value": tokens_all / (res["e2e_ms"] * 1e-3), "unit": "tokens/s",
@@ -390,7 +456,7 @@ def run_ours(args):
             "note": "every input (q, whole KV pool, weights, lengths, tables) copied from "
                     "pinned host memory and the top-k indices read back, each step",
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": res["launches_per_step"] * args.steps,
         "paths_ms": res.get("paths_ms"),
         "ms_median": res["ms_median"],
     }
@@ -405,9 +471,12 @@ def run_ours(args):
                 r = bench_workload(wl, args, device, dist, with_e2e=False, with_paths=True)
             p = r["prob"]
             b = algorithmic_bytes(p, p.k)
+            sbw = score_kernel_bytes(p)
             per[wl] = {"ms": r["ms"], "tokens_per_s": p.total_ctx / (r["ms"] * 1e-3),
                        "gbs": b["total"] / (r["ms"] * 1e-3) / 1e9,
-                       "frac": b["total"] / (r["ms"] * 1e-3) / 1e9 / peak,
+                       "score_ms": r["ms_score"],
+                       "score_gbs": sbw["total"] / (r["ms_score"] * 1e-3) / 1e9,
+                       "score_frac": sbw["total"] / (r["ms_score"] * 1e-3) / 1e9 / peak,
                        "paths_ms": r.get("paths_ms")}
         line["workloads"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

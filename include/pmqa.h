@@ -135,6 +135,21 @@ int pmqa_logits_topk(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals
                      void *ws, size_t ws_bytes, pmqa_stream_t stream);
 
 /*
+ * pmqa_logits_topk in its two kernel launches, for callers that schedule or
+ * time them apart. stages: PMQA_STAGE_SCORE (the KV pass: logits into the
+ * workspace, or into logits when given, plus one key histogram per row),
+ * PMQA_STAGE_SELECT (the per-row selection from that state, which also clears
+ * it), or both (= pmqa_logits_topk). A SELECT call must follow the SCORE call
+ * with the same arguments and workspace, with no other call on that workspace
+ * in between; arguments are checked as for pmqa_logits_topk. The pages have no
+ * counterpart: the split is the fused call's own launch boundary.
+ */
+enum { PMQA_STAGE_SCORE = 1, PMQA_STAGE_SELECT = 2 };
+int pmqa_logits_topk_stages(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
+                            float *logits, void *ws, size_t ws_bytes, pmqa_stream_t stream,
+                            int32_t stages);
+
+/*
  * pmqa_logits_topk without a caller-supplied workspace. The pages have no
  * counterpart to this entry point: it exists for callers that are given device
  * buffers for their inputs and outputs but cannot allocate device memory of

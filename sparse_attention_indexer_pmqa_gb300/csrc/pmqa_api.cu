@@ -228,8 +228,11 @@ int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
 }
 
 int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals, float *logits,
-             void *ws, size_t ws_bytes, cudaStream_t stream)
+             void *ws, size_t ws_bytes, cudaStream_t stream,
+             int stages = PMQA_STAGE_SCORE | PMQA_STAGE_SELECT)
 {
+    if (stages < 1 || stages > (PMQA_STAGE_SCORE | PMQA_STAGE_SELECT))
+        return PMQA_ERR_INVALID_ARG;
     int rc = check_problem(p);
     if (rc != PMQA_OK)
         return rc;
@@ -288,20 +291,22 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
             sel_src = a.clogits;
         }
     }
-    int sms = 0;
-    if ((rc = sm_count(&sms)) != PMQA_OK)
-        return rc;
-    const int threads = kMaxThreads;
-    cudaError_t e;
-    switch (p->heads) {
-    case 16: e = launch_main_h16(a, sms, threads, stream); break;
-    case 32: e = launch_main_h32(a, sms, threads, stream); break;
-    case 64: e = launch_main_h64(a, sms, threads, stream); break;
-    default: e = launch_main_h128(a, sms, threads, stream); break;
+    if (stages & PMQA_STAGE_SCORE) {
+        int sms = 0;
+        if ((rc = sm_count(&sms)) != PMQA_OK)
+            return rc;
+        const int threads = kMaxThreads;
+        cudaError_t e;
+        switch (p->heads) {
+        case 16: e = launch_main_h16(a, sms, threads, stream); break;
+        case 32: e = launch_main_h32(a, sms, threads, stream); break;
+        case 64: e = launch_main_h64(a, sms, threads, stream); break;
+        default: e = launch_main_h128(a, sms, threads, stream); break;
+        }
+        if (e != cudaSuccess)
+            return PMQA_ERR_CUDA;
     }
-    if (e != cudaSuccess)
-        return PMQA_ERR_CUDA;
-    if (!fused)
+    if (!fused || !(stages & PMQA_STAGE_SELECT))
         return PMQA_OK;
     const SelectArgs s = select_args(sel_src, p->context_lens, p->bs, p->next_n, p->max_model_len,
                                      k, idx, vals, ws, L);
@@ -351,6 +356,13 @@ int pmqa_logits_topk(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals
                      void *ws, size_t ws_bytes, pmqa_stream_t stream)
 {
     return run_main(p, true, k, idx, vals, logits, ws, ws_bytes, stream);
+}
+
+int pmqa_logits_topk_stages(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
+                            float *logits, void *ws, size_t ws_bytes, pmqa_stream_t stream,
+                            int32_t stages)
+{
+    return run_main(p, true, k, idx, vals, logits, ws, ws_bytes, stream, stages);
 }
 
 int pmqa_topk(const float *logits, const int32_t *context_lens, int32_t bs, int32_t next_n,

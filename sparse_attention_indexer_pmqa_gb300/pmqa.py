@@ -29,9 +29,13 @@ PMQA_OP_LOGITS = 0
 PMQA_OP_TOPK = 1
 PMQA_OP_LOGITS_TOPK = 2
 
+PMQA_STAGE_SCORE = 1
+PMQA_STAGE_SELECT = 2
+
 EXPORTED = (
     "pmqa_workspace_bytes", "pmqa_workspace_init", "pmqa_logits", "pmqa_topk",
-    "pmqa_logits_topk", "pmqa_logits_topk_noalloc", "pmqa_read_device_status",
+    "pmqa_logits_topk", "pmqa_logits_topk_stages", "pmqa_logits_topk_noalloc",
+    "pmqa_read_device_status",
     "pmqa_status_string", "pmqa_version",
 )
 
@@ -87,6 +91,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pmqa_logits": ([PP, V, V, SZ, V], ctypes.c_int),
         "pmqa_topk": ([V, V, I32, I32, I32, I32, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_logits_topk": ([PP, I32, V, V, V, V, SZ, V], ctypes.c_int),
+        "pmqa_logits_topk_stages": ([PP, I32, V, V, V, V, SZ, V, I32], ctypes.c_int),
         "pmqa_logits_topk_noalloc": ([PP, I32, V, V, V, V], ctypes.c_int),
         "pmqa_read_device_status": ([V, V], ctypes.c_int),
         "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -209,6 +214,18 @@ def pmqa_logits_topk(q, kv_cache, weights, context_lens, block_tables, max_model
     _check(load().pmqa_logits_topk(ctypes.byref(p), k, _ptr(idx), _ptr(vals), _ptr(logits),
                                    _ptr(ws), ws.numel(), _stream(stream)), "pmqa_logits_topk")
     return (idx, vals) if want_vals or vals is not None else idx
+
+
+def pmqa_logits_topk_stages(q, kv_cache, weights, context_lens, block_tables, max_model_len: int,
+                            k: int, stages: int, *, idx, ws, vals=None, logits=None,
+                            stream=None):
+    """One or both launches of the fused call (PMQA_STAGE_SCORE, then
+    PMQA_STAGE_SELECT with the same arguments and workspace)."""
+    p = make_problem(q, kv_cache, weights, context_lens, block_tables, max_model_len)
+    _check(load().pmqa_logits_topk_stages(ctypes.byref(p), k, _ptr(idx), _ptr(vals), _ptr(logits),
+                                          _ptr(ws), ws.numel(), _stream(stream), stages),
+           "pmqa_logits_topk_stages")
+    return idx
 
 
 def pmqa_logits_topk_noalloc(q, kv_cache, weights, context_lens, block_tables,

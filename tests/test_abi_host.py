@@ -90,6 +90,20 @@ def test_problem_validation(lib, kw, code):
                                 1 << 20, None) == code
 
 
+def test_stage_flags(lib):
+    p = _problem()
+    need = pmqa.pmqa_workspace_bytes(2, 1, 64, 16, pmqa.PMQA_OP_LOGITS_TOPK)
+    I = ctypes.c_void_p(0x70000)
+    for bad in (0, 4, -1):
+        assert lib.pmqa_logits_topk_stages(ctypes.byref(p), 16, I, None, None, WS, need, None,
+                                           bad) == pmqa.PMQA_ERR_INVALID_ARG
+    # the usual argument checks run for every stage choice
+    assert lib.pmqa_logits_topk_stages(ctypes.byref(p), 16, None, None, None, WS, need, None,
+                                       pmqa.PMQA_STAGE_SELECT) == pmqa.PMQA_ERR_INVALID_ARG
+    assert lib.pmqa_logits_topk_stages(ctypes.byref(p), 16, I, None, None, WS, need - 1, None,
+                                       pmqa.PMQA_STAGE_SCORE) == pmqa.PMQA_ERR_WORKSPACE
+
+
 def test_null_problem_and_outputs(lib):
     assert lib.pmqa_logits(None, ctypes.c_void_p(0x60000), WS, 1 << 20, None) == -1
     p = _problem()

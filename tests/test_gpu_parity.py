@@ -159,6 +159,29 @@ def test_workspace_is_reusable(cuda_lib):
     assert cuda_lib.pmqa_read_device_status(ws) == 0
 
 
+def test_stages_match_the_fused_call(cuda_lib):
+    """SCORE then SELECT (two calls) selects what the fused call selects."""
+    prob = make_problem(3, 2, 64, 16, [3000, 1500, 2049], 4096, seed=12, table="perm")
+    d = dev(prob)
+    k = 1024
+    ws = cuda_lib.workspace(3, 2, 4096, k, cuda_lib.PMQA_OP_LOGITS_TOPK)
+    i_f, v_f = gpu_fused(cuda_lib, prob, k, d=d, ws=ws)
+    idx = torch.empty((6, k), dtype=torch.int32, device="cuda")
+    vals = torch.empty((6, k), dtype=torch.float32, device="cuda")
+    args = (d["q"], d["kv"], d["w"], d["ctx"], d["bt"], prob.max_model_len, k)
+    cuda_lib.pmqa_logits_topk_stages(*args, cuda_lib.PMQA_STAGE_SCORE, idx=idx, vals=vals, ws=ws)
+    cuda_lib.pmqa_logits_topk_stages(*args, cuda_lib.PMQA_STAGE_SELECT, idx=idx, vals=vals, ws=ws)
+    torch.cuda.synchronize()
+    i_s, v_s = idx.cpu().numpy(), vals.cpu().numpy()
+    for r in range(6):  # same set, same values (order within a row may differ)
+        o_f, o_s = np.argsort(i_f[r]), np.argsort(i_s[r])
+        assert np.array_equal(i_f[r][o_f], i_s[r][o_s])
+        assert np.array_equal(v_f[r][o_f], v_s[r][o_s])
+    _, r64, tol = oracle_all(prob)
+    check_topk_rows(i_s, r64, tol, prob.context_lens, 2, k, vals=v_s)
+    assert cuda_lib.pmqa_read_device_status(ws) == 0
+
+
 def test_bad_table_entry_sets_status_without_fault(cuda_lib):
     prob = make_problem(2, 1, 64, 1, [300, 200], 512, seed=9)
     prob.block_tables[1, 10] = prob.num_blocks + 7
