@@ -28,7 +28,7 @@ constexpr int kVersion = 200;  // 0.2.0
 constexpr uint32_t kMaxDynSmem = 232448 - ((uint32_t)sizeof(CtaCtl) + 127u) / 128u * 128u;
 constexpr uint32_t kMinMainSmem = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr size_t kWsAlign = 256;
-constexpr int kSelChunk = 8192;  // positions per selection CTA
+constexpr int kSelChunk = kSelThreads * kSelPer;  // positions per selection CTA (8192)
 // Tuning constants of the main kernel (compile time; -D overrides in tuning builds).
 #ifndef PMQA_MAX_STAGING
 #define PMQA_MAX_STAGING 8

@@ -10,9 +10,11 @@
 // kernel, or by pmqa_hist_kernel). The select kernel reads the histogram,
 // finds the bin b* holding the k-th largest key and makes one pass over the
 // row: entries in bins above b* are written straight to the output, entries
-// in b* go to a per-row tie list. The last CTA of the row (an arrival counter,
-// no waiting) resolves the tie list exactly with two more digits (11 and 10
-// bits), pads the output and returns the row's workspace state to zero.
+// in b* go to a per-row candidate list; each CTA takes its output ranges with
+// one atomic per list. The last CTA of the row (an arrival counter, no
+// waiting) resolves the candidates exactly with two more digits (11 and 10
+// bits), from shared memory when they fit, pads the output and returns the
+// row's workspace state to zero.
 #pragma once
 
 #include <cstdint>
@@ -73,10 +75,15 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_hist_kernel(const __grid_con
             atomicAdd(a.hist + (long long)row * kHistBins + e, h[e]);
 }
 
+constexpr int kSelPer = 32;      // positions per thread: one CTA covers 256 * 32 = 8192
+constexpr int kTieCap = 4096;    // tie entries resolved from shared memory
+
 struct SelShared {
     uint32_t h[kHistBins];
     uint32_t wsum[kSelThreads / 32];
-    uint32_t bstar, above, digit, above2, eq_taken, last;
+    uint32_t bstar, above, digit, above2, eq_taken, last, base_sel, base_tie;
+    int32_t tpos[kTieCap];   // tie positions of the row (last CTA)
+    uint32_t tkey[kTieCap];  // their order keys
 };
 
 // Find the bin b of h[0..nbins) (scanning from the top) where the running
@@ -126,16 +133,52 @@ __device__ void find_bin(SelShared &s, const uint32_t *h, int nbins, uint32_t ne
     __syncthreads();
 }
 
+// Exclusive prefix over the CTA of a per-thread count; returns this thread's
+// offset, the CTA total in *total. Every thread calls.
+__device__ uint32_t cta_exclusive_scan(SelShared &s, uint32_t x, uint32_t *total)
+{
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    __syncthreads();
+    if (lane == 31)
+        s.wsum[wid] = incl;
+    __syncthreads();
+    uint32_t woff = 0, all = 0;
+    for (int w = 0; w < kSelThreads / 32; ++w) {
+        woff += w < wid ? s.wsum[w] : 0;
+        all += s.wsum[w];
+    }
+    *total = all;
+    return woff + incl - x;
+}
+
+__device__ __forceinline__ float f32_from_order_key(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// One CTA = up to 8192 positions of one row. The CTA holds its positions'
+// logits in registers (all loads in flight at once), counts the sure winners
+// (key bin above b*) and the candidates (bin b*), takes its output ranges
+// with one atomic each and writes them. The last CTA of the row resolves the
+// candidates from shared memory.
 __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_constant__ SelectArgs a)
 {
     __shared__ SelShared s;
-    const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+    const int row = blockIdx.y, tid = threadIdx.x;
     const int n = sel_valid_len(a, row);
     const uint32_t keff = (uint32_t)min(a.k, n);
     const float NEG_INF = -__int_as_float(0x7f800000);
     const long long rbase = (long long)row * a.mml;
     int32_t *orow = a.idx + (long long)row * a.k;
     float *vrow = a.vals ? a.vals + (long long)row * a.k : nullptr;
+    uint32_t *const status = a.status;
 
     // threshold bin of the k-th largest key
     for (int e = tid; e < kHistBins; e += kSelThreads)
@@ -155,50 +198,57 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     }
     const uint32_t bstar = s.bstar;
 
-    // one pass over this CTA's positions
+    // this CTA's positions, all loads first
     const long long t0 = (long long)blockIdx.x * a.chunk;
     const long long t1 = min(t0 + a.chunk, (long long)n);
-    if (keff > 0) {
-        for (long long base = t0; base < t1; base += kSelThreads) {
-            const long long t = base + tid;
-            float v = 0.f;
-            uint32_t bin = kHistBins + 1;
-            if (t < t1) {
-                v = __ldcg(a.logits + rbase + t);
-                bin = f32_order_key(v) >> kHistShift;
-            }
-            const bool sel = bin != kHistBins + 1 && bin > bstar && bin < kHistBins;
-            const bool tie = bin == bstar;
-            const uint32_t ms = __ballot_sync(kFullMask, sel);
-            if (ms) {
-                uint32_t b0 = 0;
-                if (lane == 0)
-                    b0 = atomicAdd(a.sel_cnt + row, (uint32_t)__popc(ms));
-                b0 = __shfl_sync(kFullMask, b0, 0);
-                if (sel) {
-                    const uint32_t o = b0 + __popc(ms & ((1u << lane) - 1u));
-                    if (o < keff) {
-                        orow[o] = (int32_t)t;
-                        if (vrow)
-                            vrow[o] = v;
-                    } else {
-                        atomicOr(a.status, 0x8u);
-                    }
+    float v[kSelPer];
+    uint32_t nsel = 0, ntie = 0;
+    if (keff > 0 && t0 < t1) {
+#pragma unroll
+        for (int u = 0; u < kSelPer; ++u) {
+            const long long t = t0 + u * kSelThreads + tid;
+            v[u] = t < t1 ? __ldcg(a.logits + rbase + t) : NEG_INF;
+        }
+#pragma unroll
+        for (int u = 0; u < kSelPer; ++u) {
+            const long long t = t0 + u * kSelThreads + tid;
+            const uint32_t bin = f32_order_key(v[u]) >> kHistShift;
+            nsel += (t < t1 && bin > bstar) ? 1u : 0u;
+            ntie += (t < t1 && bin == bstar) ? 1u : 0u;
+        }
+    }
+    uint32_t tot_sel, tot_tie;
+    uint32_t o_sel = cta_exclusive_scan(s, nsel, &tot_sel);
+    uint32_t o_tie = cta_exclusive_scan(s, ntie, &tot_tie);
+    if (tid == 0) {
+        s.base_sel = tot_sel ? atomicAdd(a.sel_cnt + row, tot_sel) : 0u;
+        s.base_tie = tot_tie ? atomicAdd(a.tie_cnt + row, tot_tie) : 0u;
+    }
+    __syncthreads();
+    if (nsel | ntie) {
+        o_sel += s.base_sel;
+        o_tie += s.base_tie;
+#pragma unroll
+        for (int u = 0; u < kSelPer; ++u) {
+            const long long t = t0 + u * kSelThreads + tid;
+            if (t >= t1)
+                continue;
+            const uint32_t bin = f32_order_key(v[u]) >> kHistShift;
+            if (bin > bstar) {
+                if (o_sel < keff) {
+                    orow[o_sel] = (int32_t)t;
+                    if (vrow)
+                        vrow[o_sel] = v[u];
+                } else {
+                    atomicOr(status, 0x8u);
                 }
-            }
-            const uint32_t mt = __ballot_sync(kFullMask, tie);
-            if (mt) {
-                uint32_t b0 = 0;
-                if (lane == 0)
-                    b0 = atomicAdd(a.tie_cnt + row, (uint32_t)__popc(mt));
-                b0 = __shfl_sync(kFullMask, b0, 0);
-                if (tie) {
-                    const uint32_t o = b0 + __popc(mt & ((1u << lane) - 1u));
-                    if (o < (uint32_t)a.mml)
-                        a.ties[rbase + o] = (int32_t)t;
-                    else
-                        atomicOr(a.status, 0x8u);
-                }
+                ++o_sel;
+            } else if (bin == bstar) {
+                if (o_tie < (uint32_t)a.mml)
+                    a.ties[rbase + o_tie] = (int32_t)t;
+                else
+                    atomicOr(status, 0x8u);
+                ++o_tie;
             }
         }
     }
@@ -214,40 +264,52 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     __threadfence();
     const uint32_t above = s.above;
     const uint32_t need = keff > above ? keff - above : 0u;
-    const uint32_t ntie = keff > 0 ? min(__ldcg(a.tie_cnt + row), (uint32_t)a.mml) : 0u;
+    const uint32_t ntie_row = keff > 0 ? min(__ldcg(a.tie_cnt + row), (uint32_t)a.mml) : 0u;
     const int32_t *tl = a.ties + rbase;
     if (keff > 0 && __ldcg(a.sel_cnt + row) != above)
-        atomicOr(a.status, 0x8u);
-    if (need >= ntie) {
-        // every tie is selected
-        for (uint32_t e = tid; e < ntie && above + e < keff; e += kSelThreads) {
+        atomicOr(status, 0x8u);
+    if (need >= ntie_row) {
+        // every candidate is selected
+        for (uint32_t e = tid; e < ntie_row && above + e < keff; e += kSelThreads) {
             const int32_t t = __ldcg(tl + e);
             orow[above + e] = t;
             if (vrow)
                 vrow[above + e] = __ldcg(a.logits + rbase + t);
         }
-        if (need > ntie)
-            atomicOr(a.status, 0x8u);
+        if (need > ntie_row)
+            atomicOr(status, 0x8u);
     } else if (need > 0) {
-        // second digit: key bits 20..10 of the tie entries
+        // Candidates' order keys: from shared memory when they fit, else
+        // re-read from the logits on every pass.
+        const bool cached = ntie_row <= (uint32_t)kTieCap;
+        if (cached) {
+            for (uint32_t e = tid; e < ntie_row; e += kSelThreads) {
+                const int32_t t = __ldcg(tl + e);
+                s.tpos[e] = t;
+                s.tkey[e] = f32_order_key(__ldcg(a.logits + rbase + t));
+            }
+        }
+        auto key_of = [&](uint32_t e) -> uint32_t {
+            return cached ? s.tkey[e] : f32_order_key(__ldcg(a.logits + rbase + __ldcg(tl + e)));
+        };
+        auto pos_of = [&](uint32_t e) -> int32_t { return cached ? s.tpos[e] : __ldcg(tl + e); };
+        // second digit: key bits 20..10 of the candidates
         for (int e = tid; e < kHistBins; e += kSelThreads)
             s.h[e] = 0;
         __syncthreads();
-        for (uint32_t e = tid; e < ntie; e += kSelThreads) {
-            const uint32_t key = f32_order_key(__ldcg(a.logits + rbase + __ldcg(tl + e)));
-            atomicAdd(&s.h[(key >> 10) & 2047u], 1u);
-        }
+        for (uint32_t e = tid; e < ntie_row; e += kSelThreads)
+            atomicAdd(&s.h[(key_of(e) >> 10) & 2047u], 1u);
         __syncthreads();
         find_bin(s, s.h, kHistBins, need);
         const uint32_t d2 = s.digit, above2 = s.above2;
         const uint32_t need2 = need - above2;
         __syncthreads();
-        // third digit: key bits 9..0 of the entries in sub-bin d2
+        // third digit: key bits 9..0 of the candidates in sub-bin d2
         for (int e = tid; e < 1024; e += kSelThreads)
             s.h[e] = 0;
         __syncthreads();
-        for (uint32_t e = tid; e < ntie; e += kSelThreads) {
-            const uint32_t key = f32_order_key(__ldcg(a.logits + rbase + __ldcg(tl + e)));
+        for (uint32_t e = tid; e < ntie_row; e += kSelThreads) {
+            const uint32_t key = key_of(e);
             if (((key >> 10) & 2047u) == d2)
                 atomicAdd(&s.h[key & 1023u], 1u);
         }
@@ -258,24 +320,22 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
         const uint32_t eq_need = need2 - above3;
         if (tid == 0) {
             s.eq_taken = 0;
-            s.above = 0;  // reused as the output cursor within the tie range
+            s.above = 0;  // reused as the output cursor within the candidate range
         }
         __syncthreads();
-        for (uint32_t e = tid; e < ntie; e += kSelThreads) {
-            const int32_t t = __ldcg(tl + e);
-            const float v = __ldcg(a.logits + rbase + t);
-            const uint32_t key = f32_order_key(v);
+        for (uint32_t e = tid; e < ntie_row; e += kSelThreads) {
+            const uint32_t key = key_of(e);
             bool take = key > T;
             if (key == T)
                 take = atomicAdd(&s.eq_taken, 1u) < eq_need;
             if (take) {
                 const uint32_t o = above + atomicAdd(&s.above, 1u);
                 if (o < keff) {
-                    orow[o] = t;
+                    orow[o] = pos_of(e);
                     if (vrow)
-                        vrow[o] = v;
+                        vrow[o] = f32_from_order_key(key);
                 } else {
-                    atomicOr(a.status, 0x8u);
+                    atomicOr(status, 0x8u);
                 }
             }
         }
