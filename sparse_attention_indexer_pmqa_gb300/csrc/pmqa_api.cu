@@ -135,7 +135,7 @@ bool main_layout(int heads, int nn, bool with_hist, MainArgs &a)
             a.off_tab = off;
             off += (uint32_t)(SG * kTileTokens * 4);
             a.off_bar = off;
-            off += (uint32_t)(2 * a.S + 2 * a.NBUF + 2 * QS + RS + 2 * SG + 1) * 8u;
+            off += (uint32_t)(a.S + RS + a.NBUF + 2 * QS + RS + 2 * SG + 1) * 8u;
             off = (uint32_t)align_up(off, 16);
             a.off_hist = off;
             if (with_hist)

@@ -232,14 +232,19 @@ struct Ring {
     }
 };
 
+// mdone[k % RS] completes (one tcgen05.commit) when the MMAs of tile k have
+// finished: the epilogue waits for tile k's accumulator there and the repack
+// for tile k - S's operand stage. RS = S + NBUF is deep enough that neither
+// waiter can see a later phase of the same barrier: the MMA of tile k + RS
+// needs the repack of tile k + RS and the epilogue of tile k + S, neither of
+// which can have happened while a waiter is still at tile k.
 struct Bars {
-    uint64_t *op_full, *op_empty, *tfull, *tempty, *qfull, *qempty, *sfull, *gfull, *gempty, *done;
+    uint64_t *op_full, *mdone, *tempty, *qfull, *qempty, *sfull, *gfull, *gempty, *done;
     __device__ Bars(const MainArgs &a, uint8_t *smem)
     {
         op_full = reinterpret_cast<uint64_t *>(smem + a.off_bar);
-        op_empty = op_full + a.S;
-        tfull = op_empty + a.S;
-        tempty = tfull + a.NBUF;
+        mdone = op_full + a.S;
+        tempty = mdone + a.RS;
         qfull = tempty + a.NBUF;
         qempty = qfull + a.QS;
         sfull = qempty + a.QS;
@@ -425,14 +430,16 @@ static __device__ void repack_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, 
     float *const sring = reinterpret_cast<float *>(smem + a.off_scale) + r;
     uint8_t *const op_row = smem + a.off_op + r * 128u;
     const uint8_t *const win0 = smem + r * kWinBytes;
-    Ring g(a.SG), st(a.S), sr(a.RS);
+    Ring g(a.SG), st(a.S), sr(a.RS), rel(a.RS);  // rel: tile kk - S (stage release)
     bool ok = true;
     for (int kk = 0; kk < count; ++kk) {
         if (!mbar_wait(&B.gfull[g.slot], g.phase, &c.abort) ||
-            !mbar_wait(&B.op_empty[st.slot], st.phase ^ 1u, &c.abort)) {
+            (kk >= a.S && !mbar_wait(&B.mdone[rel.slot], rel.phase, &c.abort))) {
             ok = false;
             break;
         }
+        if (kk >= a.S)
+            rel.advance();
         const uint32_t m = meta[g.slot * kTileTokens];
         const uint4 *win = reinterpret_cast<const uint4 *>(win0 + (uint32_t)g.slot * kSlotBytes);
         uint32_t w[36];
@@ -487,7 +494,7 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
     const uint32_t q_bytes = (uint32_t)N * kHeadDim;
     TileIter it;
     it.init(a, c);
-    Ring st(a.S), tb(a.NBUF), q(a.QS);
+    Ring st(a.S), tb(a.NBUF), q(a.QS), md(a.RS);
     bool ok = true;
     for (int kk = 0; kk < count; ++kk) {
         const bool first = kk == 0 || it.m == 0;
@@ -515,8 +522,7 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
                           k4 > 0 ? 1u : 0u);
             }
         }
-        umma_commit(&B.op_empty[st.slot]);
-        umma_commit(&B.tfull[tb.slot]);
+        umma_commit(&B.mdone[md.slot]);
         if (kk == count - 1 || it.m == it.nt - 1) {
             umma_commit(&B.qempty[q.slot]);
             q.advance();
@@ -524,6 +530,7 @@ static __device__ void mma_role(const MainArgs &a, uint8_t *smem, CtaCtl &c)
         it.next();
         st.advance();
         tb.advance();
+        md.advance();
     }
     if (!ok)
         raise_abort(a, c);
@@ -676,7 +683,7 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
         if (first)
             ok = mbar_wait(&B.qfull[q.slot], q.phase, &c.abort);
         ok = ok && mbar_wait(&B.sfull[sr.slot], sr.phase, &c.abort) &&
-             mbar_wait(&B.tfull[tb.slot], tb.phase, &c.abort);
+             mbar_wait(&B.mdone[sr.slot], sr.phase, &c.abort);
         // one outcome per warp: the tile body uses warp-wide shuffles and votes
         ok = __all_sync(kFullMask, ok);
         if (ok) {
@@ -694,13 +701,10 @@ static __device__ void epilogue_role(const MainArgs &a, uint8_t *smem, CtaCtl &c
                     logits[row * mml + t] = valid ? lj : NEG_INF;
                 if (clogits && valid)
                     st_global_hint(clogits + row * mml + t, lj, keep_pol);
-                if (want_hist) {
-                    const uint32_t bin = f32_order_key(lj) >> kHistShift;
-                    const uint32_t grp =
-                        __match_any_sync(kFullMask, valid ? bin : 0x10000u + (uint32_t)lane);
-                    if (valid && (__ffs(grp) - 1) == lane)
-                        atomicAdd(shist + j * kHistBins + bin, (uint32_t)__popc(grp));
-                }
+                // plain shared-memory atomics: the hardware merges same-bin
+                // lanes far more cheaply than a match/vote aggregation
+                if (want_hist && valid)
+                    atomicAdd(shist + j * kHistBins + (f32_order_key(lj) >> kHistShift), 1u);
             };
             // negative scales are legal but rare: a separate (cold) path
             if (__all_sync(kFullMask, flip == 0u))
@@ -754,24 +758,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (threadIdx.x == 0) {
         ctl.abort = 0;
         const Bars B(a, smem);
-        for (int s = 0; s < a.S; ++s) {
+        for (int s = 0; s < a.S; ++s)
             mbar_init(&B.op_full[s], kRepackWarps);
-            mbar_init(&B.op_empty[s], 1);
-        }
         for (int g = 0; g < a.SG; ++g) {
             mbar_init(&B.gfull[g], 2 * 32 * kGatherWarps);
             mbar_init(&B.gempty[g], kRepackWarps);
         }
-        for (int b = 0; b < a.NBUF; ++b) {
-            mbar_init(&B.tfull[b], 1);
+        for (int b = 0; b < a.NBUF; ++b)
             mbar_init(&B.tempty[b], 4);
-        }
         for (int q = 0; q < a.QS; ++q) {
             mbar_init(&B.qfull[q], 1);
             mbar_init(&B.qempty[q], 1 + 4);
         }
-        for (int q = 0; q < a.RS; ++q)
+        for (int q = 0; q < a.RS; ++q) {
             mbar_init(&B.sfull[q], kRepackWarps);
+            mbar_init(&B.mdone[q], 1);
+        }
         mbar_init(B.done, 1);
         mbar_init_fence();
     }

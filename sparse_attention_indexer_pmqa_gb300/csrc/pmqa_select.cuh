@@ -40,6 +40,7 @@ struct SelectArgs {
 };
 
 constexpr int kSelThreads = 256;
+constexpr int kSelPer = 32;  // positions per thread: one CTA covers 256 * 32 = 8192
 
 __device__ __forceinline__ int sel_valid_len(const SelectArgs &a, int row)
 {
@@ -51,7 +52,7 @@ __device__ __forceinline__ int sel_valid_len(const SelectArgs &a, int row)
 __global__ void __launch_bounds__(kSelThreads) pmqa_hist_kernel(const __grid_constant__ SelectArgs a)
 {
     __shared__ uint32_t h[kHistBins];
-    const int row = blockIdx.y, lane = threadIdx.x & 31;
+    const int row = blockIdx.y;
     const int n = sel_valid_len(a, row);
     const long long t0 = (long long)blockIdx.x * a.chunk;
     const long long t1 = min(t0 + a.chunk, (long long)n);
@@ -61,13 +62,18 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_hist_kernel(const __grid_con
         h[e] = 0;
     __syncthreads();
     const float *src = a.logits + (long long)row * a.mml;
-    for (long long base = t0; base < t1; base += kSelThreads) {
-        const long long t = base + threadIdx.x;
-        const bool in = t < t1;
-        const uint32_t bin = in ? f32_order_key(__ldcs(src + t)) >> kHistShift : 0u;
-        const uint32_t grp = __match_any_sync(kFullMask, in ? bin : 0x10000u + (uint32_t)lane);
-        if (in && (__ffs(grp) - 1) == lane)
-            atomicAdd(&h[bin], (uint32_t)__popc(grp));
+    // all of this CTA's loads in flight first, then plain shared atomics
+    float v[kSelPer];
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) {
+        const long long t = t0 + u * kSelThreads + threadIdx.x;
+        v[u] = t < t1 ? __ldcg(src + t) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) {
+        const long long t = t0 + u * kSelThreads + threadIdx.x;
+        if (t < t1)
+            atomicAdd(&h[f32_order_key(v[u]) >> kHistShift], 1u);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < kHistBins; e += kSelThreads)
@@ -75,7 +81,6 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_hist_kernel(const __grid_con
             atomicAdd(a.hist + (long long)row * kHistBins + e, h[e]);
 }
 
-constexpr int kSelPer = 32;      // positions per thread: one CTA covers 256 * 32 = 8192
 constexpr int kTieCap = 4096;    // tie entries resolved from shared memory
 
 struct SelShared {
