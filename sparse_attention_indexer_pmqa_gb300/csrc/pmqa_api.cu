@@ -283,6 +283,7 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     a.logits = logits;
     a.status = reinterpret_cast<uint32_t *>(wsb);
     a.l2_policy = PMQA_L2_POLICY;
+    a.page_mode = (p->block_size % 4 == 0) ? 1 : 0;
     float *sel_src = logits;
     if (fused) {
         a.hist = reinterpret_cast<uint32_t *>(wsb + L.hist);

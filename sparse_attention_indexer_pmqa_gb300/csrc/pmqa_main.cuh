@@ -78,6 +78,7 @@ struct MainArgs {
     uint32_t *hist;    // per-row key histograms [rows, 2048], or null
     uint32_t *status;
     int l2_policy;     // KV stream: 0 evict_first, 1 evict_normal, 2 evict_last
+    int page_mode;     // block_size % 4 == 0: rows move as page runs by bulk copy
     // shared-memory / pipeline layout, computed on the host
     int N, S, SG, NBUF, QS, RS, cols, tmem_cols;
     int q_box;  // rows per q TMA box: N / ceil(N / 256)
@@ -340,6 +341,8 @@ static __device__ void gather_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, 
     uint8_t *const meta = smem + a.off_meta;                             // [SG][128]
     int32_t *const tring = reinterpret_cast<int32_t *>(smem + a.off_tab);  // [SG][128]
     const uint32_t stage0 = smem_u32(smem) + (uint32_t)(gw * kTokPerWarp) * kWinBytes;
+    const uint32_t page0 = smem_u32(smem) + (uint32_t)(gw * kTokPerWarp) * (uint32_t)kKvRowBytes;
+    const bool page_mode = a.page_mode != 0;
     auto page_of = [&](int tok) { return p_pow2 ? tok >> p_shift : tok / P; };
     TileIter iss, tab;
     iss.init(a, c);
@@ -373,6 +376,50 @@ static __device__ void gather_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, 
         if (ki + DT < count)
             prefetch_table();
         const int t = iss.m * kTileTokens + row;
+        if (page_mode) {
+            // Page runs: consecutive rows of one page lie back to back in the
+            // pool, so each run goes as one bulk copy (TMA engine, no
+            // per-thread copies). Rows land at row * 132 in the slot. A run
+            // starts at a multiple of 4 rows of its page (block starts and page
+            // starts are), and its length is rounded up to whole 4-row groups
+            // inside the same page, so source, destination and size keep the
+            // 16-byte rule; the extra rows lie past the context and are masked.
+            bool v = false;
+            uint32_t tok = 0;
+            if (t < iss.ctx) {
+                if (b >= 0 && (long long)b < num_blocks) {
+                    const int in_page = p_pow2 ? (t & (P - 1)) : t - page_of(t) * P;
+                    tok = (uint32_t)((long long)b * P + in_page);
+                    v = true;
+                } else {
+                    atomicOr(status, 0x1u);
+                }
+            }
+            meta[g.slot * kTileTokens + row] = (uint8_t)(v ? 4u | ((uint32_t)row & 3u) : 0u);
+            const uint32_t vmask = __ballot_sync(kFullMask, v);
+            const uint32_t tprev = __shfl_up_sync(kFullMask, tok, 1);
+            const bool start =
+                v && (lane == 0 || !((vmask >> (lane - 1)) & 1u) || tok != tprev + 1u);
+            const uint32_t smask = __ballot_sync(kFullMask, start);
+            uint32_t bytes = 0;
+            if (start) {
+                const uint32_t later = lane == 31 ? 0u : (smask | ~vmask) & (~0u << (lane + 1));
+                const int end = later ? __ffs(later) - 1 : 32;
+                bytes = (uint32_t)(((end - lane) + 3) & ~3) * (uint32_t)kKvRowBytes;
+            }
+            const uint32_t total = __reduce_add_sync(kFullMask, bytes);
+            __syncwarp();  // every lane's metadata before the arrive
+            if (lane == 0)
+                mbar_arrive_expect_tx(&B.gfull[g.slot], total);
+            __syncwarp();
+            if (start)
+                bulk_load(page0 + (uint32_t)g.slot * kSlotBytes + (uint32_t)lane * kKvRowBytes,
+                          kv + (unsigned long long)tok * kKvRowBytes, bytes, &B.gfull[g.slot]);
+            cp_async_commit();  // keeps the table prefetch group count in step
+            iss.next();
+            g.advance();
+            continue;
+        }
         long long w0 = 0;
         uint32_t m = 0;
         uint32_t last = 16;  // bytes of the window's last chunk inside the pool (4..16)
@@ -425,11 +472,19 @@ static __device__ void repack_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, 
     const Bars B(a, smem);
     const int lane = threadIdx.x & 31;
     const int count = (int)c.count;
-    const uint32_t r = (uint32_t)(rw * kTokPerWarp + lane);  // this lane's row
+    // This lane's row: lanes 8k..8k+7 of a load/store phase take rows
+    // 4a + ((a/2 + k) mod 4), a = 0..7, so the eight 16-byte accesses of a
+    // phase hit distinct bank groups both when reading windows (rows 144 or
+    // 132 bytes apart) and when writing the swizzled operand rows.
+    const uint32_t pa = (uint32_t)lane & 7u, pk = (uint32_t)lane >> 3;
+    const uint32_t r = (uint32_t)(rw * kTokPerWarp) + 4u * pa + (((pa >> 1) + pk) & 3u);
     const uint8_t *const meta = smem + a.off_meta + r;
     float *const sring = reinterpret_cast<float *>(smem + a.off_scale) + r;
     uint8_t *const op_row = smem + a.off_op + r * 128u;
-    const uint8_t *const win0 = smem + r * kWinBytes;
+    // the row's 16-byte aligned window: its own 144-byte slot, or (page runs)
+    // the aligned bytes around row * 132
+    const uint8_t *const win0 =
+        smem + (a.page_mode ? (r * (uint32_t)kKvRowBytes) & ~15u : r * kWinBytes);
     Ring g(a.SG), st(a.S), sr(a.RS), rel(a.RS);  // rel: tile kk - S (stage release)
     bool ok = true;
     for (int kk = 0; kk < count; ++kk) {
@@ -555,7 +610,7 @@ __device__ __forceinline__ void epi_wait(uint32_t (&buf)[16])
 // Packed fp32x2 multiply-adds; the weights come as float4 broadcasts.
 template <bool SIGNED>
 __device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[16], const float *w, uint32_t flip,
-                                               float (&acc)[4])
+                                               float (&acc)[8])
 {
     const float4 *w4 = reinterpret_cast<const float4 *>(w);
 #pragma unroll
@@ -565,8 +620,10 @@ __device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[16], const fl
 #pragma unroll
         for (int u = 0; u < 4; ++u)
             v[u] = fmaxf(__uint_as_float(SIGNED ? (x[h + u] ^ flip) : x[h + u]), 0.f);
-        ffma2(acc[0], acc[1], wv.x, wv.y, v[0], v[1]);
-        ffma2(acc[2], acc[3], wv.z, wv.w, v[2], v[3]);
+        // four independent fp32x2 accumulator pairs: short dependency chains
+        float *a = acc + ((h / 4) & 1) * 4;
+        ffma2(a[0], a[1], wv.x, wv.y, v[0], v[1]);
+        ffma2(a[2], a[3], wv.z, wv.w, v[2], v[3]);
     }
 }
 
@@ -585,7 +642,7 @@ __device__ __forceinline__ void epi_tile(uint32_t taddr, const float *wsl, uint3
     epi_load(taddr, b0);
     epi_wait(b0);
     for (int j = 0; j < nn; ++j) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const uint32_t tj = taddr + (uint32_t)(j * H);
         const float *wj = wsl + j * H;
         const bool more_rows = j + 1 < nn;
@@ -617,7 +674,8 @@ __device__ __forceinline__ void epi_tile(uint32_t taddr, const float *wsl, uint3
             if (lane == 0)
                 mbar_arrive(tempty_bar);
         }
-        out(j, ((acc[0] + acc[1]) + (acc[2] + acc[3])) * mag);
+        out(j, (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]))) *
+                   mag);
     }
 }
 
@@ -761,7 +819,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         for (int s = 0; s < a.S; ++s)
             mbar_init(&B.op_full[s], kRepackWarps);
         for (int g = 0; g < a.SG; ++g) {
-            mbar_init(&B.gfull[g], 2 * 32 * kGatherWarps);
+            // window copies: a release arrive and a cp.async arrive per gather
+            // thread; page runs: one expect-tx arrive per gather warp
+            mbar_init(&B.gfull[g], a.page_mode ? kGatherWarps : 2 * 32 * kGatherWarps);
             mbar_init(&B.gempty[g], kRepackWarps);
         }
         for (int b = 0; b < a.NBUF; ++b)

@@ -314,9 +314,12 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t *r)
                  : "memory");
 }
 
+// No memory clobber: the wait orders TMEM loads only (their destination
+// registers are tied to it through reg_fence16), and shared/global loads that
+// do not depend on it may still be scheduled across it.
 __device__ __forceinline__ void tmem_ld_wait()
 {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;");
 }
 
 // Register a dependency of r on the preceding tcgen05.wait::ld.
@@ -325,9 +328,7 @@ __device__ __forceinline__ void reg_fence16(uint32_t *r)
     asm volatile(""
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                    "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
 // Named barrier over `count` threads (a multiple of 32).
