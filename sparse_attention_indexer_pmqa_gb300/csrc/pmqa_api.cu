@@ -30,12 +30,6 @@ constexpr uint32_t kMinMainSmem = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr size_t kWsAlign = 256;
 constexpr int kSelChunk = kSelThreads * kSelPer;  // positions per selection CTA (8192)
 // Tuning constants of the main kernel (compile time; -D overrides in tuning builds).
-#ifndef PMQA_MAX_STAGING
-#define PMQA_MAX_STAGING 8
-#endif
-#ifndef PMQA_OP_STAGES
-#define PMQA_OP_STAGES 3
-#endif
 #ifndef PMQA_L2_POLICY
 #define PMQA_L2_POLICY 0
 #endif
@@ -101,54 +95,35 @@ int check_problem(const pmqa_problem *p)
     return PMQA_OK;
 }
 
-// Shared-memory and pipeline layout of the main kernel: the deepest staging
-// ring that fits, preferring two query slots at equal depth.
-bool main_layout(int heads, int nn, bool with_hist, MainArgs &a)
+// Shared-memory and TMEM layout of the main kernel: four warpgroup regions
+// (staging slot + operand tile), then the query and weight slots (two when
+// they fit) and the mbarriers. Each warpgroup owns cols TMEM columns.
+bool main_layout(int heads, int nn, MainArgs &a)
 {
     const int N = heads * nn;
     a.N = N;
     int cols = 32;
-    while (cols < N)
+    while (cols < N && cols < kPassCols)
         cols <<= 1;
-    if (cols > 512)
-        return false;
     a.cols = cols;
-    a.NBUF = std::min(8, 512 / cols);
-    a.tmem_cols = a.NBUF * cols;
-    a.S = PMQA_OP_STAGES;
-    for (int SG = PMQA_MAX_STAGING; SG >= 3; --SG) {
-        for (int QS = 2; QS >= 1; --QS) {
-            const int RS = a.S + a.NBUF;
-            uint32_t off = (uint32_t)SG * kSlotBytes;  // staging ring
-            a.off_op = off;
-            off += (uint32_t)a.S * kStageBytes;
-            a.off_q = off;
-            off += (uint32_t)(QS * N * kHeadDim);
-            a.off_w = off;
-            off += (uint32_t)(QS * N * 4);
-            off = (uint32_t)align_up(off, 16);
-            a.off_scale = off;
-            off += (uint32_t)RS * kTileTokens * 4u;
-            a.off_meta = off;
-            off += (uint32_t)(SG * kTileTokens);
-            off = (uint32_t)align_up(off, 16);
-            a.off_tab = off;
-            off += (uint32_t)(SG * kTileTokens * 4);
-            a.off_bar = off;
-            off += (uint32_t)(a.S + RS + a.NBUF + 2 * QS + RS + 2 * SG + 1) * 8u;
-            off = (uint32_t)align_up(off, 16);
-            a.off_hist = off;
-            if (with_hist)
-                off += (uint32_t)(nn * kHistBins * 4);
-            const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
-            if (total > kMaxDynSmem)
-                continue;
-            a.SG = SG;
-            a.QS = QS;
-            a.RS = RS;
-            a.smem_bytes = total;
-            return true;
-        }
+    a.tmem_cols = kGroups * cols;
+    for (int QS = 2; QS >= 1; --QS) {
+        uint32_t off = 0;
+        a.off_grp = off;
+        off += (uint32_t)kGroups * kGroupBytes;
+        a.off_q = off;  // 1024-byte aligned: 128B-swizzled TMA boxes
+        off += (uint32_t)(QS * N * kHeadDim);
+        a.off_w = off;
+        off += (uint32_t)(QS * N * 4);
+        off = (uint32_t)align_up(off, 16);
+        a.off_bar = off;
+        off += (uint32_t)(QS + kGroups + kNumWarps) * 8u;
+        const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
+        if (total > kMaxDynSmem)
+            continue;
+        a.QS = QS;
+        a.smem_bytes = total;
+        return true;
     }
     return false;
 }
@@ -255,7 +230,7 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     if (ws_bytes < L.total)
         return PMQA_ERR_WORKSPACE;
     MainArgs a{};
-    if (!main_layout(p->heads, p->next_n, fused, a))
+    if (!main_layout(p->heads, p->next_n, a))
         return PMQA_ERR_UNSUPPORTED;
     if (fused && rows > 65535)
         return PMQA_ERR_UNSUPPORTED;

@@ -55,24 +55,68 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` pass, instead of returning at once to spin.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete. Returns false if the
-// CTA-wide abort flag (when given) was raised or the time limit passed.
+// CTA-wide abort flag (when given) was raised or the time limit passed. A
+// waiting warp sleeps in the barrier unit rather than spinning, so it takes
+// no issue slots from the warps that do the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           const volatile int *abort_flag)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 100000u))
             return true;
-        if ((it & 31u) == 0) {
-            if (abort_flag != nullptr && *abort_flag)
-                return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs)
-                return false;
-        }
+        if (abort_flag != nullptr && *abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs)
+            return false;
     }
+}
+
+// ---------------------------------------------------------------- shared memory
+
+// Explicit shared-memory accesses by 32-bit shared address. Volatile: they keep
+// their order against the barrier, copy-wait and tcgen05 statements around
+// them.
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- cp.async
@@ -329,6 +373,42 @@ __device__ __forceinline__ void reg_fence16(uint32_t *r)
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                    "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+// 32 consecutive TMEM columns of this thread's lane (32x32b shape, x32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+// NC (16 or 32) consecutive TMEM columns of this thread's lane, and the
+// matching register fence after tmem_ld_wait.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[NC])
+{
+    static_assert(NC == 16 || NC == 32, "16 or 32 columns");
+    if constexpr (NC == 16)
+        tmem_ld16(taddr, r);
+    else
+        tmem_ld32(taddr, r);
+}
+
+template <int NC>
+__device__ __forceinline__ void reg_fence_cols(uint32_t (&r)[NC])
+{
+    reg_fence16(r);
+    if constexpr (NC == 32)
+        reg_fence16(r + 16);
 }
 
 // Named barrier over `count` threads (a multiple of 32).
