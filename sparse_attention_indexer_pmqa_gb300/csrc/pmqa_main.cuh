@@ -317,68 +317,87 @@ __device__ __forceinline__ float acc_sum(float (&acc)[8])
     return s;
 }
 
-// Draft rows j0 .. j0 + nr - 1 for this thread's token (TMEM lane): row j's
+// Draft rows j0 .. j0 + NR - 1 for this thread's token (TMEM lane): row j's
 // score is |sc| * sum_h w[j][h] * relu(+-x[j][h]), x in TMEM columns
 // [(j - j0) * H, (j - j0) * H + H) from taddr, weights w[j][h] at shared
-// address wsl + 4 * ((j - j0) * H + h). The columns are read 16 at a
-// time into two register buffers, the next chunk loading while the current
-// one is reduced. Calls out(j, score) per row once every TMEM read of the pass
-// has completed.
-template <int H, bool SIGNED, class Out>
+// address wsl + 4 * ((j - j0) * H + h). The NR * H / 16 chunks of 16 columns
+// alternate between two register buffers, the next chunk loading while the
+// current one is reduced. Calls out(j, score) per row once every TMEM read of
+// the pass has completed.
+template <int H, int NR, bool SIGNED, class Out>
 __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t flip, float mag,
-                                         int j0, int nr, Out &&out)
+                                         int j0, Out &&out)
 {
     constexpr int NC = 16;
     constexpr int CPR = H / NC;  // chunks per draft row
-    const int total = nr * CPR;
-    uint32_t b0[NC], b1[NC];
+    constexpr int TOTAL = NR * CPR;
+    uint32_t b[2][NC];
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float res[kMaxRows];
-    tmem_ld_cols<NC>(taddr, b0);
+    float res[NR];
+    tmem_ld_cols<NC>(taddr, b[0]);
     tmem_ld_wait();
-    reg_fence_cols<NC>(b0);
-#pragma unroll 1
-    for (int ch = 0; ch < total; ch += 2) {
-        // b0 holds chunk ch
-        const bool has1 = ch + 1 < total, has2 = ch + 2 < total;
-        if (has1)
-            tmem_ld_cols<NC>(taddr + (uint32_t)((ch + 1) * NC), b1);
-        epi_accumulate<NC, SIGNED>(b0, wsl + (uint32_t)(ch * NC * 4), flip, acc);
-        if ((ch + 1) % CPR == 0) {
-            const float v = acc_sum(acc) * mag;
-            const int j = ch / CPR;
+    reg_fence_cols<NC>(b[0]);
 #pragma unroll
-            for (int u = 0; u < kMaxRows; ++u)
-                if (u == j)
-                    res[u] = v;
-        }
-        if (has1) {
+    for (int ch = 0; ch < TOTAL; ++ch) {
+        if (ch + 1 < TOTAL)
+            tmem_ld_cols<NC>(taddr + (uint32_t)((ch + 1) * NC), b[(ch + 1) & 1]);
+        epi_accumulate<NC, SIGNED>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), flip, acc);
+        if ((ch + 1) % CPR == 0)
+            res[ch / CPR] = acc_sum(acc) * mag;
+        if (ch + 1 < TOTAL) {
             tmem_ld_wait();
-            reg_fence_cols<NC>(b1);
-            if (has2)
-                tmem_ld_cols<NC>(taddr + (uint32_t)((ch + 2) * NC), b0);
-            epi_accumulate<NC, SIGNED>(b1, wsl + (uint32_t)((ch + 1) * NC * 4), flip, acc);
-            if ((ch + 2) % CPR == 0) {
-                const float v = acc_sum(acc) * mag;
-                const int j = (ch + 1) / CPR;
-#pragma unroll
-                for (int u = 0; u < kMaxRows; ++u)
-                    if (u == j)
-                        res[u] = v;
-            }
-            if (has2) {
-                tmem_ld_wait();
-                reg_fence_cols<NC>(b0);
-            }
+            reg_fence_cols<NC>(b[(ch + 1) & 1]);
         }
     }
 #pragma unroll
-    for (int u = 0; u < kMaxRows; ++u)
-        if (u < nr)
-            out(j0 + u, res[u]);
+    for (int u = 0; u < NR; ++u)
+        out(j0 + u, res[u]);
+}
+
+
+// epi_rows for nr (1 .. RPP) rows, the scale's sign known warp-wide (all_pos)
+// or per thread.
+template <int H, int RPP, class Out>
+__device__ __forceinline__ void epi_dispatch(int nr, bool all_pos, uint32_t taddr, uint32_t wsl,
+                                             uint32_t flip, float mag, int j0, Out &out)
+{
+    if (nr == RPP) {
+        if (all_pos)
+            epi_rows<H, RPP, false>(taddr, wsl, flip, mag, j0, out);
+        else
+            epi_rows<H, RPP, true>(taddr, wsl, flip, mag, j0, out);
+    } else if constexpr (RPP > 1) {
+        epi_dispatch<H, RPP - 1>(nr, all_pos, taddr, wsl, flip, mag, j0, out);
+    }
 }
 
 // ---------------------------------------------------------------- warpgroup
+
+// Position in the CTA's tile range: `cur` is tile kk. step(n) moves n tiles on
+// and counts the request ends it passes (the last tile of a request, and the
+// range's last tile).
+struct Walk {
+    TilePos cur;
+    int kk;
+    __device__ int step(const ReqCtx &rc, int n, int count)
+    {
+        // common case: the n tiles left behind lie inside one request and
+        // before the range's last tile
+        if (cur.m + n < cur.nt && kk + n < count) {
+            cur.m += n;
+            kk += n;
+            return 0;
+        }
+        int ends = 0;
+        for (int u = 0; u < n; ++u) {
+            if (kk < count && (cur.m == cur.nt - 1 || kk == count - 1))
+                ++ends;
+            cur.next(rc);
+            ++kk;
+        }
+        return ends;
+    }
+};
 
 // Warpgroup g, warp quadrant qd (warp % 4): CTA tiles g, g + 4, g + 8, ...
 // Shared memory is addressed through 32-bit shared addresses throughout.
@@ -400,6 +419,7 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     const uint8_t *const kv = a.kv;
     const int32_t *const bt = a.bt;
     const long long num_blocks = a.num_blocks, pool_bytes = a.pool_bytes;
+    const bool pool32 = pool_bytes < (1ll << 31) - 1024;  // every byte offset fits in 31 bits
     const int P = a.P, W = a.W;
     const bool p_pow2 = (P & (P - 1)) == 0;
     const int p_shift = __ffs(P) - 1;
@@ -409,7 +429,8 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     // shared memory: the group's staging slot, then its operand tile
     const uint32_t sbase = smem_u32(smem);
     const uint32_t stage = sbase + a.off_grp + (uint32_t)g * kGroupBytes;
-    const uint32_t win = stage + (page_mode ? (R * (uint32_t)kKvRowBytes) & ~15u : R * kWinBytes);
+    // window mode: row R's 16-byte aligned window; page runs: the row itself
+    const uint32_t win = stage + (page_mode ? R * (uint32_t)kKvRowBytes : R * kWinBytes);
     // operand row R is 128-byte aligned: chunk ch sits at opx ^ (ch << 4)
     const uint32_t opx = (stage + kSlotBytes + R * 128u) ^ ((R & 7u) << 4);
     const uint32_t wstage = stage + (uint32_t)(qd * 32) * kWinBytes;  // this warp's 32 windows
@@ -423,8 +444,8 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     const uint64_t adesc = sw128_kmajor_desc(stage + kSlotBytes);
     const uint64_t bdesc0 = sw128_kmajor_desc(sbase + a.off_q);
     const uint32_t q_units = (uint32_t)N * kHeadDim >> 4;
-    const int rpp = min(nn, kPassCols / H);
-    const int npass = (nn + rpp - 1) / rpp;
+    constexpr int kRpp = kPassCols / H < kMaxRows ? kPassCols / H : kMaxRows;  // rows per pass
+    const int npass = (nn + kRpp - 1) / kRpp;
     // copy e = qq * 32 + lane of a warp's 288 window chunks: window e / 9,
     // chunk e % 9; bit qq of last9 marks chunk 8 (the window's last)
     uint32_t last9 = 0;
@@ -441,8 +462,6 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
 
     ReqCtx rc;
     rc.init(a, c);
-    TilePos it;  // tile kk of the walk
-    it.init(rc, c);
 
     // Block-table entry of this thread's row in tile p (-1 past the context).
     auto table_entry = [&](const TilePos &p) -> int32_t {
@@ -489,7 +508,7 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             __syncwarp();
             if (start)
                 bulk_load(stage + R * (uint32_t)kKvRowBytes, kv + o, bytes, run_bar);
-            return v ? 4u | (R & 3u) : 0u;
+            return v ? 4u : 0u;
         }
         // Window j of the warp starts at wstage + 144 j = wstage + 16 (9 j),
         // so copy e lands at wstage + 16 e and reads kv + (w0_j - 144 j) + 16 e.
@@ -498,39 +517,42 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
         // chunk may pass the end of the pool and then reads only the bytes
         // inside.
         const long long w0 = o & ~15ll;
-        const long long wrel = w0 - (long long)kWinBytes * lane;
         const uint32_t last = v ? (uint32_t)min(16ll, pool_bytes - (w0 + 128)) : 0u;
         const uint32_t ml = (v ? 0x100u : 0u) | last;
+        if (pool32) {
+            const int wrel = (int)w0 - (int)kWinBytes * lane;
 #pragma unroll
-        for (int qq = 0; qq < 9; ++qq) {
-            const uint32_t e = (uint32_t)(qq * 32 + lane);
-            const int j = (int)((e * 7282u) >> 16);  // e / 9 for e < 288
-            const long long wj = __shfl_sync(kFullMask, wrel, j);
-            const uint32_t mj = __shfl_sync(kFullMask, ml, j);
-            if (mj & 0x100u)
-                cp_async_16_zfill(wstage + 16u * e, kv + (wj + 16ll * e),
-                                  ((last9 >> qq) & 1u) ? (mj & 0xFFu) : 16u, pol);
+            for (int qq = 0; qq < 9; ++qq) {
+                const uint32_t e = (uint32_t)(qq * 32 + lane);
+                const int j = (int)((e * 7282u) >> 16);  // e / 9 for e < 288
+                const int wj = __shfl_sync(kFullMask, wrel, j);
+                const uint32_t mj = __shfl_sync(kFullMask, ml, j);
+                if (mj & 0x100u)
+                    cp_async_16_zfill(wstage + 16u * e, kv + (uint32_t)(wj + 16 * (int)e),
+                                      ((last9 >> qq) & 1u) ? (mj & 0xFFu) : 16u, pol);
+            }
+        } else {
+            const long long wrel = w0 - (long long)kWinBytes * lane;
+#pragma unroll
+            for (int qq = 0; qq < 9; ++qq) {
+                const uint32_t e = (uint32_t)(qq * 32 + lane);
+                const int j = (int)((e * 7282u) >> 16);
+                const long long wj = __shfl_sync(kFullMask, wrel, j);
+                const uint32_t mj = __shfl_sync(kFullMask, ml, j);
+                if (mj & 0x100u)
+                    cp_async_16_zfill(wstage + 16u * e, kv + (wj + 16ll * e),
+                                      ((last9 >> qq) & 1u) ? (mj & 0xFFu) : 16u, pol);
+            }
         }
         return v ? 4u | ((uint32_t)(o >> 2) & 3u) : 0u;
     };
 
-    // prologue: copies of the group's first tile, table entries of its second
-    TilePos nx = it;  // the group's next tile to gather
-    nx.skip(rc, g);
-    int kg = g;  // CTA tile index of the group's current tile
-    uint32_t meta = 0;
-    if (kg < count)
-        meta = issue(nx, table_entry(nx));
-    cp_async_commit();
-    nx.skip(rc, kGroups);
-    int32_t b_nx = kg + kGroups < count ? table_entry(nx) : -1;
-
-    uint32_t run_phase = 0, mma_phase = 0;
-    int q_slot = 0;          // query slot of request req_n (requests cycle through QS slots)
+    // query slots: request n of the range sits in slot n % QS
+    int q_slot = 0;
     uint32_t q_phase = 0;
-    bool have_q = false;     // the group has waited for the current request's query slot
-    int loads = 0;           // query loads issued (thread 0)
-    ReqWalk nxt;             // next request whose query is to be loaded (thread 0)
+    bool have_q = false;  // the group has waited for the current request's query slot
+    int loads = 0;        // query loads issued (thread 0)
+    ReqWalk nxt;          // next request whose query is to be loaded (thread 0)
     nxt.init(rc, c);
     if (threadIdx.x == 0)
         for (int n = 0; n < QS; ++n) {
@@ -540,111 +562,10 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             }
             nxt.advance(rc);
         }
-
-    for (int kk = 0; kk < count; ++kk) {
-        if (kk == kg) {
-            // 1. the tile's rows have landed
-            bool ok = true;
-            if (page_mode) {
-                ok = mbar_wait(run_bar, run_phase, &c.abort);
-                run_phase ^= 1u;
-            } else {
-                cp_async_wait_group<0>();
-            }
-            __syncwarp();
-            // 2. repack row R: window words -> operand row, scale -> register
-            uint32_t wv[36];
-#pragma unroll
-            for (int q = 0; q < 9; ++q) {
-                const uint4 x = lds128(win + 16u * q);
-                wv[4 * q + 0] = x.x;
-                wv[4 * q + 1] = x.y;
-                wv[4 * q + 2] = x.z;
-                wv[4 * q + 3] = x.w;
-            }
-            // row word k is window word k + (meta & 3): shift by 1, then by 2.
-            // Rows past the context keep whatever the window holds: their
-            // scores are masked.
-            const bool s1 = (meta & 1u) != 0, s2 = (meta & 2u) != 0;
-#pragma unroll
-            for (int k = 0; k < 35; ++k)
-                wv[k] = s1 ? wv[k + 1] : wv[k];
-#pragma unroll
-            for (int k = 0; k < 33; ++k)
-                wv[k] = s2 ? wv[k + 2] : wv[k];
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                sts128(opx ^ ((uint32_t)ch << 4), wv[4 * ch], wv[4 * ch + 1], wv[4 * ch + 2], wv[4 * ch + 3]);
-            const float sc = (meta & 4u) ? __uint_as_float(wv[32]) : 0.0f;
-            __syncwarp();  // every lane has read its window before the slot is refilled
-            // 3. the group's next tile: copies now, table entries of the one after
-            kg += kGroups;
-            if (kg < count)
-                meta = issue(nx, b_nx);
-            cp_async_commit();
-            nx.skip(rc, kGroups);
-            b_nx = kg + kGroups < count ? table_entry(nx) : -1;
-            // operand visible to the tensor core; the previous tile's TMEM reads done
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            named_bar_sync(wg_bar, 128);
-            tc_fence_after_sync();
-            if (!have_q) {
-                ok = mbar_wait(&B.qfull[q_slot], q_phase, &c.abort) && ok;
-                have_q = true;
-            }
-            const uint32_t wsl = w_base + (uint32_t)q_slot * w_slot_bytes;
-            const int t = it.m * kTileTokens + (int)R;
-            const int lim0 = it.ctx - nn + 1;  // draft row j admits t < lim0 + j
-            const long long obase = (long long)it.i * nn * mml + t;
-            const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
-            const float mag = fabsf(sc);
-            auto out = [&](int j, float lj) {
-                const bool vj = t < lim0 + j;
-                const long long o = obase + (long long)j * mml;
-                if (logits && t < mml)
-                    logits[o] = vj ? lj : NEG_INF;
-                if (clogits && vj)
-                    st_global_hint(clogits + o, lj, keep_pol);
-                if (hist && vj)
-                    atomicAdd(hist + ((long long)it.i * nn + j) * kHistBins + (f32_order_key(lj) >> kHistShift),
-                              1u);
-            };
-            const bool all_pos = __all_sync(kFullMask, flip == 0u);
-            for (int p = 0; p < npass; ++p) {
-                const int j0 = p * rpp, nr = min(rpp, nn - j0);
-                if (elected) {
-                    const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
-                                                            ((uint32_t)(j0 * H * kHeadDim) >> 4));
-                    const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
-#pragma unroll
-                    for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
-                        umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
-                    umma_commit(&B.mma[g]);
-                }
-                __syncwarp();
-                ok = mbar_wait(&B.mma[g], mma_phase, &c.abort) && ok;
-                mma_phase ^= 1u;
-                tc_fence_after_sync();
-                // one outcome per warp: the tile body uses warp-wide shuffles and votes
-                if (__all_sync(kFullMask, ok)) {
-                    const uint32_t wj0 = wsl + (uint32_t)(j0 * H * 4);
-                    if (all_pos)
-                        epi_rows<H, false>(tacc, wj0, flip, mag, j0, nr, out);
-                    else
-                        epi_rows<H, true>(tacc, wj0, flip, mag, j0, nr, out);
-                } else {
-                    raise_abort(a, c);
-                }
-                if (p + 1 < npass) {  // the next pass reuses the columns
-                    tc_fence_before_sync();
-                    named_bar_sync(wg_bar, 128);
-                    tc_fence_after_sync();
-                }
-            }
-        }
-        if (kk == count - 1 || it.last_of_request()) {
-            // every group is done with the request: its query slot is free
+    // Request ends passed: every group meets the others there in order, then
+    // thread 0 loads the query of the request QS ahead into the freed slot.
+    auto pass_ends = [&](int ends) {
+        for (int u = 0; u < ends; ++u) {
             named_bar_sync(kCtaBarrier, kMaxThreads);
             if (threadIdx.x == 0) {
                 if (nxt.valid(count) && !aborted(c)) {
@@ -659,7 +580,129 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             }
             have_q = false;
         }
-        it.next(rc);
+    };
+
+    Walk w;  // the group's current tile
+    w.cur.init(rc, c);
+    w.kk = 0;
+    pass_ends(w.step(rc, g, count));
+    Walk nx = w;  // the group's next tile to gather
+    uint32_t meta = 0;
+    if (w.kk < count)
+        meta = issue(w.cur, table_entry(w.cur));
+    cp_async_commit();
+    nx.step(rc, kGroups, count);
+    int32_t b_nx = nx.kk < count ? table_entry(nx.cur) : -1;
+    uint32_t run_phase = 0, mma_phase = 0;
+
+    while (w.kk < count) {
+        // 1. the tile's rows have landed
+        bool ok = true;
+        if (page_mode) {
+            ok = mbar_wait(run_bar, run_phase, &c.abort);
+            run_phase ^= 1u;
+        } else {
+            cp_async_wait_group<0>();
+        }
+        __syncwarp();
+        // 2. repack row R into the operand; scale -> register. Rows past the
+        // context keep whatever the slot holds: their scores are masked.
+        float sc;
+        if (page_mode) {
+            // rows 132 bytes apart: word k of the 32 lanes' rows sits in bank
+            // (R + k) mod 32, so 4-byte loads are conflict-free
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                sts128(opx ^ ((uint32_t)ch << 4), lds32(win + 16u * ch), lds32(win + 16u * ch + 4u),
+                       lds32(win + 16u * ch + 8u), lds32(win + 16u * ch + 12u));
+            sc = (meta & 4u) ? __uint_as_float(lds32(win + 128u)) : 0.0f;
+        } else {
+            uint32_t wv[36];
+#pragma unroll
+            for (int q = 0; q < 9; ++q) {
+                const uint4 x = lds128(win + 16u * q);
+                wv[4 * q + 0] = x.x;
+                wv[4 * q + 1] = x.y;
+                wv[4 * q + 2] = x.z;
+                wv[4 * q + 3] = x.w;
+            }
+            // row word k is window word k + (meta & 3): shift by 1, then by 2
+            const bool s1 = (meta & 1u) != 0, s2 = (meta & 2u) != 0;
+#pragma unroll
+            for (int k = 0; k < 35; ++k)
+                wv[k] = s1 ? wv[k + 1] : wv[k];
+#pragma unroll
+            for (int k = 0; k < 33; ++k)
+                wv[k] = s2 ? wv[k + 2] : wv[k];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                sts128(opx ^ ((uint32_t)ch << 4), wv[4 * ch], wv[4 * ch + 1], wv[4 * ch + 2], wv[4 * ch + 3]);
+            sc = (meta & 4u) ? __uint_as_float(wv[32]) : 0.0f;
+        }
+        __syncwarp();  // every lane has read its row before the slot is refilled
+        // 3. the group's next tile: copies now, table entries of the one after
+        if (nx.kk < count)
+            meta = issue(nx.cur, b_nx);
+        cp_async_commit();
+        nx.step(rc, kGroups, count);
+        b_nx = nx.kk < count ? table_entry(nx.cur) : -1;
+        // operand visible to the tensor core; the previous tile's TMEM reads done
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        named_bar_sync(wg_bar, 128);
+        tc_fence_after_sync();
+        if (!have_q) {
+            ok = mbar_wait(&B.qfull[q_slot], q_phase, &c.abort) && ok;
+            have_q = true;
+        }
+        const uint32_t wsl = w_base + (uint32_t)q_slot * w_slot_bytes;
+        const TilePos &it = w.cur;
+        const int t = it.m * kTileTokens + (int)R;
+        const int lim0 = it.ctx - nn + 1;  // draft row j admits t < lim0 + j
+        const long long obase = (long long)it.i * nn * mml + t;
+        uint32_t *const hrow = hist ? hist + (long long)it.i * nn * kHistBins : nullptr;
+        const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
+        const float mag = fabsf(sc);
+        auto out = [&](int j, float lj) {
+            const bool vj = t < lim0 + j;
+            const long long o = obase + (long long)j * mml;
+            if (logits && t < mml)
+                logits[o] = vj ? lj : NEG_INF;
+            if (clogits && vj)
+                st_global_hint(clogits + o, lj, keep_pol);
+            if (hrow && vj)
+                atomicAdd(hrow + j * kHistBins + (f32_order_key(lj) >> kHistShift), 1u);
+        };
+        const bool all_pos = __all_sync(kFullMask, flip == 0u);
+        for (int p = 0; p < npass; ++p) {
+            const int j0 = p * kRpp, nr = min(kRpp, nn - j0);
+            if (elected) {
+                const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
+                                                        ((uint32_t)(j0 * H * kHeadDim) >> 4));
+                const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
+#pragma unroll
+                for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
+                    umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
+                umma_commit(&B.mma[g]);
+            }
+            __syncwarp();
+            ok = mbar_wait(&B.mma[g], mma_phase, &c.abort) && ok;
+            mma_phase ^= 1u;
+            tc_fence_after_sync();
+            // one outcome per warp: the tile body uses warp-wide votes
+            if (__all_sync(kFullMask, ok)) {
+                const uint32_t wj0 = wsl + (uint32_t)(j0 * H * 4);
+                epi_dispatch<H, kRpp>(nr, all_pos, tacc, wj0, flip, mag, j0, out);
+            } else {
+                raise_abort(a, c);
+            }
+            if (p + 1 < npass) {  // the next pass reuses the columns
+                tc_fence_before_sync();
+                named_bar_sync(wg_bar, 128);
+                tc_fence_after_sync();
+            }
+        }
+        pass_ends(w.step(rc, kGroups, count));
     }
     cp_async_wait_all();
     // after an abort, query loads nobody consumed land before the CTA exits (bounded)

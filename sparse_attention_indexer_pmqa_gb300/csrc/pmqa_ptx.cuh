@@ -104,6 +104,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ float4 lds128f(uint32_t addr)
 {
     float4 v;
