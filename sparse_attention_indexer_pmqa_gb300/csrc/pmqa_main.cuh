@@ -25,7 +25,8 @@
 //      TMEM columns, at most 128 columns (whole draft rows) per pass;
 //   5. each thread reads its lane of the accumulators (tcgen05.ld), forms
 //      sum_h w[j][h] * relu(x) per draft row, scales, masks, and writes full
-//      logits rows and/or compact logits plus key histogram counts.
+//      logits rows and/or the compact logits plus the per-row key histogram
+//      (global atomics) that the selection reads.
 // At the end of each request the four warpgroups meet at a CTA barrier and
 // thread 0 loads the query and weights of the request QS ahead into the slot
 // just freed (TMA). Every wait is bounded.
@@ -68,7 +69,7 @@ struct MainArgs {
     int bs, nn, P, W, mml;
     float *logits;     // full rows [rows, mml], or null
     float *clogits;    // compact logits (valid positions only) for the selection, or null
-    uint32_t *hist;    // per-row key histograms [rows, 2048], or null
+    uint32_t *hist;    // per-row histograms of the top 11 bits of the order keys [rows, 2048], or null
     uint32_t *status;
     int l2_policy;     // KV stream: 0 evict_first, 1 evict_normal, 2 evict_last
     int page_mode;     // block_size % 4 == 0: rows move as page runs by bulk copy

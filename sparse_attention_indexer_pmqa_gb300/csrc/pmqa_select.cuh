@@ -35,7 +35,7 @@ struct SelectArgs {
     uint32_t *arrive;   // [rows]
     int32_t *ties;      // [rows, mml]
     uint32_t *status;
-    int splits;  // CTAs per row (gridDim.x)
+    int splits;  // CTAs per row in the grid (gridDim.x); a row uses ceil(valid_len / chunk)
     int chunk;   // positions per CTA
 };
 
@@ -184,6 +184,10 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     int32_t *orow = a.idx + (long long)row * a.k;
     float *vrow = a.vals ? a.vals + (long long)row * a.k : nullptr;
     uint32_t *const status = a.status;
+    // the row's CTAs: enough to cover its valid positions (one when it has none)
+    const int row_ctas = n > 0 ? (n + a.chunk - 1) / a.chunk : 1;
+    if ((int)blockIdx.x >= row_ctas)
+        return;
 
     // threshold bin of the k-th largest key
     for (int e = tid; e < kHistBins; e += kSelThreads)
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     __threadfence();
     __syncthreads();
     if (tid == 0)
-        s.last = atomicAdd(a.arrive + row, 1u) == (uint32_t)(a.splits - 1) ? 1u : 0u;
+        s.last = atomicAdd(a.arrive + row, 1u) == (uint32_t)(row_ctas - 1) ? 1u : 0u;
     __syncthreads();
     if (!s.last)
         return;
