@@ -298,7 +298,7 @@ __device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[NC], uint32_t
 {
 #pragma unroll
     for (int h = 0; h < NC; h += 4) {
-        const float4 wv = lds128f(w + (uint32_t)(h * 4));
+        const float4 wv = lds128f_nv(w + (uint32_t)(h * 4));
         float v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -656,7 +656,8 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             ok = mbar_wait(&B.qfull[q_slot], q_phase, &c.abort) && ok;
             have_q = true;
         }
-        const uint32_t wsl = w_base + (uint32_t)q_slot * w_slot_bytes;
+        // weights of the request: valid after the query-slot wait above
+        const uint32_t wsl = launder_u32(w_base + (uint32_t)q_slot * w_slot_bytes);
         const TilePos &it = w.cur;
         const int t = it.m * kTileTokens + (int)R;
         const int lim0 = it.ctx - nn + 1;  // draft row j admits t < lim0 + j

@@ -120,6 +120,25 @@ __device__ __forceinline__ float4 lds128f(uint32_t addr)
     return v;
 }
 
+// Non-volatile: for data that stays fixed while it is read (the weights of a
+// request). The compiler may schedule these loads freely between the
+// statements that order them: derive the address from launder_u32 after the
+// wait that makes the data valid.
+__device__ __forceinline__ float4 lds128f_nv(uint32_t addr)
+{
+    float4 v;
+    asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+// An opaque copy of x, produced in program order among the volatile statements.
+__device__ __forceinline__ uint32_t launder_u32(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
