@@ -28,7 +28,7 @@ constexpr int kVersion = 200;  // 0.2.0
 constexpr uint32_t kMaxDynSmem = 232448 - ((uint32_t)sizeof(CtaCtl) + 127u) / 128u * 128u;
 constexpr uint32_t kMinMainSmem = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr size_t kWsAlign = 256;
-constexpr int kSelChunk = kSelThreads * kSelPer;  // positions per selection CTA (8192)
+constexpr int kSelChunk = kSelThreads * kSelPer;  // positions per selection CTA (4096)
 // Tuning constants of the main kernel (compile time; -D overrides in tuning builds).
 #ifndef PMQA_L2_POLICY
 #define PMQA_L2_POLICY 0
@@ -37,8 +37,9 @@ constexpr int kSelChunk = kSelThreads * kSelPer;  // positions per selection CTA
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace: status word | per-row counters | per-row histograms | tie lists
-// | compact logits (fused only). Everything before the tie lists must be zero
-// when a call starts; every call leaves it zero again (status word aside).
+// of (position, order key) | compact logits (fused only). Everything before
+// the tie lists must be zero when a call starts; every call leaves it zero
+// again (status word aside).
 struct WsLayout {
     size_t sel_cnt, tie_cnt, arrive, hist, ties, clogits, total;
 };
@@ -57,7 +58,7 @@ bool ws_layout(long long rows, long long mml, int op, WsLayout *L)
     L->arrive = L->tie_cnt + r4;
     L->hist = L->arrive + r4;
     L->ties = L->hist + (size_t)rows * kHistBins * 4;
-    L->clogits = L->ties + align_up((size_t)rows * (size_t)mml * 4, kWsAlign);
+    L->clogits = L->ties + align_up((size_t)rows * (size_t)mml * 8, kWsAlign);
     L->total = op == PMQA_OP_LOGITS_TOPK ? L->clogits + (size_t)rows * (size_t)mml * 4 : L->clogits;
     return true;
 }
@@ -182,7 +183,7 @@ SelectArgs select_args(const float *logits, const int32_t *ctx, int bs, int nn, 
     s.tie_cnt = reinterpret_cast<uint32_t *>(b + L.tie_cnt);
     s.arrive = reinterpret_cast<uint32_t *>(b + L.arrive);
     s.hist = reinterpret_cast<uint32_t *>(b + L.hist);
-    s.ties = reinterpret_cast<int32_t *>(b + L.ties);
+    s.ties = reinterpret_cast<uint2 *>(b + L.ties);
     s.chunk = kSelChunk;
     s.splits = (mml + kSelChunk - 1) / kSelChunk;
     return s;

@@ -33,14 +33,14 @@ struct SelectArgs {
     uint32_t *sel_cnt;  // [rows]
     uint32_t *tie_cnt;  // [rows]
     uint32_t *arrive;   // [rows]
-    int32_t *ties;      // [rows, mml]
+    uint2 *ties;        // [rows, mml] candidates: (position, order key)
     uint32_t *status;
     int splits;  // CTAs per row in the grid (gridDim.x); a row uses ceil(valid_len / chunk)
     int chunk;   // positions per CTA
 };
 
 constexpr int kSelThreads = 256;
-constexpr int kSelPer = 32;  // positions per thread: one CTA covers 256 * 32 = 8192
+constexpr int kSelPer = 16;  // positions per thread: one CTA covers 256 * 16 = 4096
 
 __device__ __forceinline__ int sel_valid_len(const SelectArgs &a, int row)
 {
@@ -86,6 +86,7 @@ constexpr int kTieCap = 4096;    // tie entries resolved from shared memory
 struct SelShared {
     uint32_t h[kHistBins];
     uint32_t wsum[kSelThreads / 32];
+    uint32_t wsel[kSelThreads / 32], wtie[kSelThreads / 32];  // per-warp counts, then offsets
     uint32_t bstar, above, digit, above2, eq_taken, last, base_sel, base_tie;
     int32_t tpos[kTieCap];   // tie positions of the row (last CTA)
     uint32_t tkey[kTieCap];  // their order keys
@@ -168,7 +169,7 @@ __device__ __forceinline__ float f32_from_order_key(uint32_t key)
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// One CTA = up to 8192 positions of one row. The CTA holds its positions'
+// One CTA = up to 4096 positions of one row. The CTA holds its positions'
 // logits in registers (all loads in flight at once), counts the sure winners
 // (key bin above b*) and the candidates (bin b*), takes its output ranges
 // with one atomic each and writes them. The last CTA of the row resolves the
@@ -189,6 +190,16 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     if ((int)blockIdx.x >= row_ctas)
         return;
 
+    // this CTA's positions: all loads in flight first
+    const long long t0 = (long long)blockIdx.x * a.chunk;
+    const long long t1 = min(t0 + a.chunk, (long long)n);
+    float v[kSelPer];
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) {
+        const long long t = t0 + u * kSelThreads + tid;
+        v[u] = (keff > 0 && t < t1) ? __ldcg(a.logits + rbase + t) : NEG_INF;
+    }
+
     // threshold bin of the k-th largest key
     for (int e = tid; e < kHistBins; e += kSelThreads)
         s.h[e] = __ldcg(a.hist + (long long)row * kHistBins + e);
@@ -207,58 +218,69 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     }
     const uint32_t bstar = s.bstar;
 
-    // this CTA's positions, all loads first
-    const long long t0 = (long long)blockIdx.x * a.chunk;
-    const long long t1 = min(t0 + a.chunk, (long long)n);
-    float v[kSelPer];
-    uint32_t nsel = 0, ntie = 0;
-    if (keff > 0 && t0 < t1) {
-#pragma unroll
-        for (int u = 0; u < kSelPer; ++u) {
-            const long long t = t0 + u * kSelThreads + tid;
-            v[u] = t < t1 ? __ldcg(a.logits + rbase + t) : NEG_INF;
-        }
+    // bit u of msel / mtie: position u of this thread is a winner / candidate
+    uint32_t msel = 0, mtie = 0;
+    if (keff > 0) {
 #pragma unroll
         for (int u = 0; u < kSelPer; ++u) {
             const long long t = t0 + u * kSelThreads + tid;
             const uint32_t bin = f32_order_key(v[u]) >> kHistShift;
-            nsel += (t < t1 && bin > bstar) ? 1u : 0u;
-            ntie += (t < t1 && bin == bstar) ? 1u : 0u;
+            msel |= (t < t1 && bin > bstar) ? 1u << u : 0u;
+            mtie |= (t < t1 && bin == bstar) ? 1u << u : 0u;
         }
     }
-    uint32_t tot_sel, tot_tie;
-    uint32_t o_sel = cta_exclusive_scan(s, nsel, &tot_sel);
-    uint32_t o_tie = cta_exclusive_scan(s, ntie, &tot_tie);
-    if (tid == 0) {
-        s.base_sel = tot_sel ? atomicAdd(a.sel_cnt + row, tot_sel) : 0u;
-        s.base_tie = tot_tie ? atomicAdd(a.tie_cnt + row, tot_tie) : 0u;
+    // output ranges: the CTA's from one atomic per list, each warp's after the
+    // warps before it
+    const int lane = tid & 31, wid = tid >> 5;
+    const uint32_t wsel = __reduce_add_sync(kFullMask, (uint32_t)__popc(msel));
+    const uint32_t wtie = __reduce_add_sync(kFullMask, (uint32_t)__popc(mtie));
+    if (lane == 0) {
+        s.wsel[wid] = wsel;
+        s.wtie[wid] = wtie;
     }
     __syncthreads();
-    if (nsel | ntie) {
-        o_sel += s.base_sel;
-        o_tie += s.base_tie;
+    if (tid == 0) {
+        uint32_t as = 0, at = 0;
+        for (int w = 0; w < kSelThreads / 32; ++w) {
+            const uint32_t xs = s.wsel[w], xt = s.wtie[w];
+            s.wsel[w] = as;
+            s.wtie[w] = at;
+            as += xs;
+            at += xt;
+        }
+        s.base_sel = as ? atomicAdd(a.sel_cnt + row, as) : 0u;
+        s.base_tie = at ? atomicAdd(a.tie_cnt + row, at) : 0u;
+    }
+    __syncthreads();
+    if (wsel | wtie) {
+        // position u of the warp's 32 lanes is 32 consecutive t: a warp writes
+        // its winners (and candidates) of each u as one contiguous run
+        uint32_t o_sel = s.base_sel + s.wsel[wid], o_tie = s.base_tie + s.wtie[wid];
+        const uint32_t lt = (1u << lane) - 1u;
+        uint2 *const trow = a.ties + rbase;
 #pragma unroll
         for (int u = 0; u < kSelPer; ++u) {
-            const long long t = t0 + u * kSelThreads + tid;
-            if (t >= t1)
-                continue;
-            const uint32_t bin = f32_order_key(v[u]) >> kHistShift;
-            if (bin > bstar) {
-                if (o_sel < keff) {
-                    orow[o_sel] = (int32_t)t;
+            const bool is_sel = (msel >> u) & 1u, is_tie = (mtie >> u) & 1u;
+            const uint32_t bs = __ballot_sync(kFullMask, is_sel), bt = __ballot_sync(kFullMask, is_tie);
+            const int32_t t = (int32_t)(t0 + u * kSelThreads + tid);
+            if (is_sel) {
+                const uint32_t o = o_sel + __popc(bs & lt);
+                if (o < keff) {
+                    orow[o] = t;
                     if (vrow)
-                        vrow[o_sel] = v[u];
+                        vrow[o] = v[u];
                 } else {
                     atomicOr(status, 0x8u);
                 }
-                ++o_sel;
-            } else if (bin == bstar) {
-                if (o_tie < (uint32_t)a.mml)
-                    a.ties[rbase + o_tie] = (int32_t)t;
+            } else if (is_tie) {
+                const uint32_t o = o_tie + __popc(bt & lt);
+                if (o < (uint32_t)a.mml)
+                    trow[o] = make_uint2((uint32_t)t, f32_order_key(v[u]));
                 else
                     atomicOr(status, 0x8u);
-                ++o_tie;
             }
+            o_sel += __popc(bs);
+            o_tie += __popc(bt);
         }
     }
 
@@ -274,34 +296,32 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     const uint32_t above = s.above;
     const uint32_t need = keff > above ? keff - above : 0u;
     const uint32_t ntie_row = keff > 0 ? min(__ldcg(a.tie_cnt + row), (uint32_t)a.mml) : 0u;
-    const int32_t *tl = a.ties + rbase;
+    const uint2 *tl = a.ties + rbase;
     if (keff > 0 && __ldcg(a.sel_cnt + row) != above)
         atomicOr(status, 0x8u);
     if (need >= ntie_row) {
         // every candidate is selected
         for (uint32_t e = tid; e < ntie_row && above + e < keff; e += kSelThreads) {
-            const int32_t t = __ldcg(tl + e);
-            orow[above + e] = t;
+            const uint2 c = __ldcg(tl + e);
+            orow[above + e] = (int32_t)c.x;
             if (vrow)
-                vrow[above + e] = __ldcg(a.logits + rbase + t);
+                vrow[above + e] = f32_from_order_key(c.y);
         }
         if (need > ntie_row)
             atomicOr(status, 0x8u);
     } else if (need > 0) {
-        // Candidates' order keys: from shared memory when they fit, else
-        // re-read from the logits on every pass.
+        // Candidates (position, key): from shared memory when they fit, else
+        // re-read from the list on every pass.
         const bool cached = ntie_row <= (uint32_t)kTieCap;
         if (cached) {
             for (uint32_t e = tid; e < ntie_row; e += kSelThreads) {
-                const int32_t t = __ldcg(tl + e);
-                s.tpos[e] = t;
-                s.tkey[e] = f32_order_key(__ldcg(a.logits + rbase + t));
+                const uint2 c = __ldcg(tl + e);
+                s.tpos[e] = (int32_t)c.x;
+                s.tkey[e] = c.y;
             }
         }
-        auto key_of = [&](uint32_t e) -> uint32_t {
-            return cached ? s.tkey[e] : f32_order_key(__ldcg(a.logits + rbase + __ldcg(tl + e)));
-        };
-        auto pos_of = [&](uint32_t e) -> int32_t { return cached ? s.tpos[e] : __ldcg(tl + e); };
+        auto key_of = [&](uint32_t e) -> uint32_t { return cached ? s.tkey[e] : __ldcg(tl + e).y; };
+        auto pos_of = [&](uint32_t e) -> int32_t { return cached ? s.tpos[e] : (int32_t)__ldcg(tl + e).x; };
         // second digit: key bits 20..10 of the candidates
         for (int e = tid; e < kHistBins; e += kSelThreads)
             s.h[e] = 0;

@@ -47,7 +47,7 @@ def test_workspace_sizes(lib):
     rows, mml = 8, 1000
     counters = 256 + 3 * 256  # status word, then three 256-aligned per-row counter arrays
     hist = rows * 2048 * 4  # per-row key histograms
-    ties = -(-rows * mml * 4 // 256) * 256
+    ties = -(-rows * mml * 8 // 256) * 256  # tie lists of (position, key)
     topk = pmqa.pmqa_workspace_bytes(4, 2, mml, 2048, pmqa.PMQA_OP_TOPK)
     assert topk == counters + hist + ties
     fused = pmqa.pmqa_workspace_bytes(4, 2, mml, 2048, pmqa.PMQA_OP_LOGITS_TOPK)
