@@ -687,9 +687,13 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
                     umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
                 umma_commit(&B.mma[g]);
             }
-            __syncwarp();
-            ok = mbar_wait(&B.mma[g], mma_phase, &c.abort) && ok;
+            // the elected thread waits for the MMAs; the rest of the group
+            // sleeps on the named barrier meanwhile
+            bool mma_ok = true;
+            if (elected)
+                mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
             mma_phase ^= 1u;
+            ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
             tc_fence_after_sync();
             // one outcome per warp: the tile body uses warp-wide votes
             if (__all_sync(kFullMask, ok)) {

@@ -81,8 +81,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
         return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 100000u))
-            return true;
+        // a few sleeps between the checks of the abort flag and the clock
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k)
+            if (mbar_try_wait_sleep(bar, parity, 100000u))
+                return true;
         if (abort_flag != nullptr && *abort_flag)
             return false;
         if (global_timer_ns() - t0 > kWaitLimitNs)
@@ -441,6 +444,22 @@ __device__ __forceinline__ void reg_fence_cols(uint32_t (&r)[NC])
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also returns whether `pred` held in every participating
+// thread.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "bar.red.and.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
+        : "memory");
+    return r != 0;
 }
 
 }  // namespace pmqa
