@@ -83,6 +83,35 @@ def test_fused_topk_small(cuda_lib, case, k):
     check_logits(logits.cpu().numpy(), ref, tol)
 
 
+# Shapes the prior art on the pages mishandled or rejected: block sizes other
+# than 1 and 64 (256 with a partial last page; sizes that are not powers of two;
+# sizes that are not multiples of 4, which move as 16-byte windows rather than
+# page runs), three draft rows, and heads 32 and 128 with them.
+BLOCKS = [
+    # bs, next_n, heads, block_size, context lengths, max_model_len
+    (2, 1, 64, 256, [300, 1000], 1024),
+    (1, 3, 32, 256, [2100], 2304),
+    (2, 3, 32, 3, [100, 250], 256),
+    (2, 2, 64, 6, [77, 300], 384),
+    (3, 3, 128, 12, [50, 129, 260], 384),
+    (2, 3, 64, 32, [513, 97], 640),
+    (2, 2, 16, 5, [128, 333], 384),
+]
+
+
+@pytest.mark.parametrize("case", BLOCKS, ids=lambda c: f"bs{c[0]}nn{c[1]}H{c[2]}P{c[3]}")
+def test_block_sizes_and_draft_rows(cuda_lib, case):
+    bs, nn, H, P, ctx, mml = case
+    prob = make_problem(bs, nn, H, P, ctx, mml, seed=sum(ctx) + 7 * P, table="perm", extra_blocks=3)
+    ref, r64, tol = oracle_all(prob)
+    check_logits(gpu_logits(cuda_lib, prob), ref, tol)
+    for k in (7, 2048):
+        logits = torch.empty((bs * nn, mml), dtype=torch.float32, device="cuda")
+        idx, vals = gpu_fused(cuda_lib, prob, k, logits=logits)
+        check_topk_rows(idx, r64, tol, prob.context_lens, nn, k, vals=vals)
+        check_logits(logits.cpu().numpy(), ref, tol)
+
+
 @pytest.mark.parametrize("ties", [False, True])
 @pytest.mark.parametrize("k", [1, 5, 300, 2048])
 def test_standalone_topk_exact(cuda_lib, k, ties):
