@@ -1,4 +1,5 @@
-"""CPU oracle for the FP8 paged MQA-logits indexer and its per-row top-k.
+"""CPU oracle for the FP8 MQA-logits indexer (paged decode and non-paged
+prefill) and its per-row top-k.
 
 TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg import this package. The product library never
@@ -53,6 +54,9 @@ def _load():
         lib.pmqa_ref_topk.argtypes = [P, ctypes.c_int64, P, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, P, ctypes.c_int]
         lib.pmqa_ref_topk.restype = ctypes.c_int
+        lib.pmqa_ref_mqa_logits.argtypes = [P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int]
+        lib.pmqa_ref_mqa_logits.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -102,6 +106,35 @@ def logits(prob, *, want64: bool = False, want_tol: bool = False, nthreads: int 
                              nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle pmqa_ref_logits failed with %d" % rc)
+    return out, out64, tol
+
+
+def mqa_logits(prob, *, want64: bool = False, want_tol: bool = False,
+               nthreads: int | None = None):
+    """Prefill (non-paged) logits: (fp32 [m, n], fp64 or None, tolerance or None).
+
+    ``prob`` carries numpy arrays q [m, heads, 128], k [n, 128], k_scale [n],
+    weights [m, heads], ks [m] and ke [m].
+    """
+    lib = _load()
+    q = np.ascontiguousarray(prob.q, dtype=np.uint8)
+    k = np.ascontiguousarray(prob.k, dtype=np.uint8)
+    sc = np.ascontiguousarray(prob.k_scale, dtype=np.float32)
+    w = np.ascontiguousarray(prob.weights, dtype=np.float32)
+    ks = np.ascontiguousarray(prob.ks, dtype=np.int32)
+    ke = np.ascontiguousarray(prob.ke, dtype=np.int32)
+    m, heads = q.shape[0], q.shape[1]
+    n = k.shape[0]
+    assert k.shape[1] == q.shape[2] and sc.shape == (n,) and w.shape == (m, heads)
+    assert ks.shape == (m,) and ke.shape == (m,)
+    out = np.empty((m, n), dtype=np.float32)
+    out64 = np.empty((m, n), dtype=np.float64) if want64 else None
+    tol = np.empty((m, n), dtype=np.float64) if want_tol else None
+    rc = lib.pmqa_ref_mqa_logits(_ptr(q), _ptr(k), _ptr(sc), _ptr(w), _ptr(ks), _ptr(ke), m, n,
+                                 heads, q.shape[2], _ptr(out), _ptr(out64), _ptr(tol),
+                                 nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle pmqa_ref_mqa_logits failed with %d" % rc)
     return out, out64, tol
 
 

@@ -381,3 +381,143 @@ int pmqa_ref_topk(const double *vals, int64_t width, const int32_t *context_lens
     pthread_mutex_destroy(&J.lock);
     return J.error ? -4 : 0;
 }
+
+/* ---- prefill logits: contiguous keys, a key range per query row ------------
+ * Source: the page "[Bug] aiter ops triton attention pa", section "Observations
+ * while narrowing it down", which names the prefill indexer `fp8_mqa_logits`
+ * (heads 32, head dimension 128, up to 8192 keys; query lengths M up to 4096)
+ * beside the paged decode kernel. The pages
+ * give its name and shapes only; its arithmetic is read here as the decode
+ * definition above with the paging removed and the causal window replaced by
+ * one key range per query row:
+ *   k_n[d]       = e4m3fn(k[n][d]),  s_n = k_scale[n]
+ *   logits[m][n] = sum_h w[m][h] * relu(s_n * sum_d q[m][h][d] * k_n[d])
+ *                  for max(ks[m], 0) <= n < min(ke[m], N), else -inf.
+ * Same exact double arithmetic, rounding and tolerance as pmqa_ref_logits.
+ */
+
+typedef struct {
+    const uint8_t *q, *k;
+    const float *ks_scale, *w;
+    const int32_t *ks, *ke;
+    int64_t m, n;
+    int heads;
+    float *out;
+    double *out64, *tol;
+    double table[256];
+    int64_t next_row;
+    pthread_mutex_t lock;
+    int error;
+} mqa_job;
+
+static void mqa_row(mqa_job *J, int64_t r, double *qd)
+{
+    const int H = J->heads;
+    int64_t lo = J->ks[r], hi = J->ke[r];
+    if (lo < 0)
+        lo = 0;
+    if (hi > J->n)
+        hi = J->n;
+    for (int h = 0; h < H; ++h)
+        for (int d = 0; d < PMQA_REF_HEAD_DIM; ++d)
+            qd[(int64_t)h * PMQA_REF_HEAD_DIM + d] =
+                J->table[J->q[((int64_t)r * H + h) * PMQA_REF_HEAD_DIM + d]];
+    const float *w = J->w + r * H;
+    double kd[PMQA_REF_HEAD_DIM];
+    for (int64_t t = lo; t < hi; ++t) {
+        const uint8_t *krow = J->k + t * PMQA_REF_HEAD_DIM;
+        for (int d = 0; d < PMQA_REF_HEAD_DIM; ++d)
+            kd[d] = J->table[krow[d]];
+        const double s = (double)J->ks_scale[t];
+        double sum = 0.0, mag = 0.0;
+        for (int h = 0; h < H; ++h) {
+            const double *qh = qd + (int64_t)h * PMQA_REF_HEAD_DIM;
+            double dot = 0.0;
+            for (int d = 0; d < PMQA_REF_HEAD_DIM; ++d)
+                dot += qh[d] * kd[d];
+            const double x = dot * s;
+            sum += (double)w[h] * relu(x);
+            mag += fabs((double)w[h]) * fabs(x);
+        }
+        const int64_t o = r * J->n + t;
+        J->out[o] = (float)sum;
+        if (J->out64)
+            J->out64[o] = sum;
+        if (J->tol)
+            J->tol[o] = 1e-3 * (1.0 + mag);
+    }
+}
+
+static void *mqa_worker(void *arg)
+{
+    mqa_job *J = (mqa_job *)arg;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)J->heads * PMQA_REF_HEAD_DIM);
+    if (!qd) {
+        J->error = 1;
+        return NULL;
+    }
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int64_t r = J->next_row++;
+        pthread_mutex_unlock(&J->lock);
+        if (r >= J->m || J->error)
+            break;
+        mqa_row(J, r, qd);
+    }
+    free(qd);
+    return NULL;
+}
+
+/*
+ * q        [m, heads, 128] e4m3fn bytes
+ * k        [n, 128] e4m3fn bytes; k_scale [n] fp32
+ * weights  [m, heads] fp32; ks, ke [m] int32 (the row's key range [ks, ke))
+ * out      [m, n] fp32 (written entirely); out64, tol same shape in double, or NULL
+ * Returns 0, -1 for bad sizes, -4 when out of memory.
+ */
+int pmqa_ref_mqa_logits(const uint8_t *q, const uint8_t *k, const float *k_scale,
+                        const float *weights, const int32_t *ks, const int32_t *ke, int64_t m,
+                        int64_t n, int heads, int head_dim, float *out, double *out64, double *tol,
+                        int nthreads)
+{
+    if (m < 0 || n < 0 || heads < 1 || head_dim != PMQA_REF_HEAD_DIM)
+        return -1;
+    const int64_t total = m * n;
+    for (int64_t e = 0; e < total; ++e) {
+        out[e] = -INFINITY;
+        if (out64)
+            out64[e] = -INFINITY;
+        if (tol)
+            tol[e] = 0.0;
+    }
+    mqa_job J;
+    memset(&J, 0, sizeof J);
+    J.q = q;
+    J.k = k;
+    J.ks_scale = k_scale;
+    J.w = weights;
+    J.ks = ks;
+    J.ke = ke;
+    J.m = m;
+    J.n = n;
+    J.heads = heads;
+    J.out = out;
+    J.out64 = out64;
+    J.tol = tol;
+    pmqa_ref_e4m3fn_table(J.table);
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1)
+        nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int started = 0;
+    for (int t = 0; th && t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, mqa_worker, &J) == 0)
+            ++started;
+    if (started == 0)
+        mqa_worker(&J);
+    for (int t = 0; t < started; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return J.error ? -4 : 0;
+}

@@ -7,8 +7,13 @@ oracle and the CUDA path take their inputs from here.
 
 from .inputs import (  # noqa: F401
     CONFIGS,
+    PREFILL_CONFIGS,
+    PrefillProblem,
     Problem,
     config_problem,
+    make_prefill,
     make_problem,
     pack_kv,
+    prefill_config,
+    prefill_ranges,
 )

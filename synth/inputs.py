@@ -268,3 +268,118 @@ __all__ = [
     "HEAD_DIM", "ROW_BYTES", "Problem", "make_problem", "config_problem", "CONFIGS",
     "pack_kv", "to_e4m3fn_bytes", "random_logits", "ceil_div",
 ]
+
+
+# ---------------------------------------------------------------- prefill
+
+
+@dataclasses.dataclass
+class PrefillProblem:
+    """Non-paged (prefill) indexer problem.
+
+    * q        uint8 [m, heads, 128]  fp8 e4m3fn bit patterns
+    * k        uint8 [n, 128]         fp8 e4m3fn bit patterns
+    * k_scale  float32 [n]
+    * weights  float32 [m, heads]
+    * ks, ke   int32 [m]: query row r reads keys ks[r] <= t < ke[r]
+    """
+    q: np.ndarray
+    k: np.ndarray
+    k_scale: np.ndarray
+    weights: np.ndarray
+    ks: np.ndarray
+    ke: np.ndarray
+    heads: int
+    name: str = "custom"
+
+    @property
+    def m(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def n(self) -> int:
+        return int(self.k.shape[0])
+
+    @property
+    def pairs(self) -> int:
+        """(query row, key) pairs inside the rows' ranges."""
+        lo = np.clip(self.ks.astype(np.int64), 0, self.n)
+        hi = np.clip(self.ke.astype(np.int64), 0, self.n)
+        return int(np.maximum(hi - lo, 0).sum())
+
+
+def prefill_ranges(m: int, n: int, kind: str, rng: np.random.Generator, segments: int = 4):
+    """Key ranges [ks, ke) of m query rows over n keys.
+
+    causal:  the query rows are the last m positions of one sequence of n
+             tokens; row r reads keys 0 .. n - m + r.
+    packed:  ``segments`` sequences packed back to back (query and key position
+             p are the same token, so m == n); row r reads from its sequence's
+             start up to itself.
+    random:  independent ranges, some empty, some reaching outside [0, n).
+    full:    every row reads every key.
+    """
+    if kind == "causal":
+        ke = n - m + np.arange(m, dtype=np.int64) + 1
+        ks = np.zeros(m, dtype=np.int64)
+        ke = np.clip(ke, 0, None)
+    elif kind == "packed":
+        assert m == n
+        cuts = np.sort(rng.choice(np.arange(1, n), size=min(segments - 1, max(n - 1, 0)),
+                                  replace=False)) if n > 1 else np.zeros(0, dtype=np.int64)
+        starts = np.concatenate([[0], cuts]).astype(np.int64)
+        seg = np.searchsorted(starts, np.arange(n), side="right") - 1
+        ks = starts[seg]
+        ke = np.arange(n, dtype=np.int64) + 1
+    elif kind == "random":
+        a = rng.integers(-8, n + 8, size=m)
+        b = rng.integers(-8, n + 8, size=m)
+        ks, ke = np.minimum(a, b), np.maximum(a, b)
+        empty = rng.random(m) < 0.1
+        ke[empty] = ks[empty]
+    elif kind == "full":
+        ks = np.zeros(m, dtype=np.int64)
+        ke = np.full(m, n, dtype=np.int64)
+    else:
+        raise ValueError(kind)
+    return ks.astype(np.int32), ke.astype(np.int32)
+
+
+def make_prefill(m: int, n: int, heads: int, *, ranges: str = "causal", seed: int = 0,
+                 poison: bool = True, scale_range=(0.01, 0.1), name: str = "custom",
+                 rng: np.random.Generator | None = None) -> PrefillProblem:
+    """Draw one prefill problem with the decode recipe's value distributions.
+
+    Keys that no row's range covers are poisoned (fp8 NaN bytes, NaN scale)."""
+    rng = np.random.default_rng(seed) if rng is None else rng
+    q = to_e4m3fn_bytes(rng.standard_normal((m, heads, HEAD_DIM), dtype=np.float32))
+    k = to_e4m3fn_bytes(rng.standard_normal((n, HEAD_DIM), dtype=np.float32))
+    lo, hi = scale_range
+    k_scale = rng.uniform(lo, hi, size=n).astype(np.float32)
+    weights = rng.standard_normal((m, heads), dtype=np.float32)
+    ks, ke = prefill_ranges(m, n, ranges, rng)
+    if poison and n > 0:
+        cover = np.zeros(n + 1, dtype=np.int64)
+        a = np.clip(ks.astype(np.int64), 0, n)
+        b = np.clip(ke.astype(np.int64), 0, n)
+        keep = b > a
+        np.add.at(cover, a[keep], 1)
+        np.add.at(cover, b[keep], -1)
+        unused = np.cumsum(cover)[:n] == 0
+        k[unused] = FP8_NAN
+        k_scale[unused] = np.float32("nan")
+    return PrefillProblem(q=q, k=k, k_scale=k_scale, weights=weights, ks=ks, ke=ke,
+                          heads=heads, name=name)
+
+
+# Prefill workloads: the query rows are the last M positions of an N-token
+# sequence (causal ranges), heads 32, head dimension 128.
+PREFILL_CONFIGS = {
+    "PF0": dict(desc="prefill M512 N1024 H32 causal", m=512, n=1024, heads=32),
+    "PF1": dict(desc="prefill M4096 N8192 H32 causal", m=4096, n=8192, heads=32),
+}
+
+
+def prefill_config(name: str, seed: int = 0) -> PrefillProblem:
+    c = PREFILL_CONFIGS[name]
+    return make_prefill(c["m"], c["n"], c["heads"], ranges="causal", seed=seed, name=name)
