@@ -65,8 +65,9 @@ enum {
 #define PMQA_DEV_TIMEOUT 0x4u      /* a pipeline wait exceeded its limit; results are invalid */
 #define PMQA_DEV_OVERFLOW 0x8u     /* top-k candidate storage exceeded; results are invalid */
 
-/* Workspace-size selector for pmqa_workspace_bytes. */
-enum { PMQA_OP_LOGITS = 0, PMQA_OP_TOPK = 1, PMQA_OP_LOGITS_TOPK = 2 };
+/* Workspace-size selector for pmqa_workspace_bytes. PMQA_OP_MQA_LOGITS (the
+   prefill entry point) needs only the status word: 256 bytes for any size. */
+enum { PMQA_OP_LOGITS = 0, PMQA_OP_TOPK = 1, PMQA_OP_LOGITS_TOPK = 2, PMQA_OP_MQA_LOGITS = 3 };
 
 /*
  * One decode-step problem, in the argument order of the reference function
@@ -170,6 +171,46 @@ int pmqa_logits_topk_stages(const pmqa_problem *p, int32_t k, int32_t *idx, floa
  */
 int pmqa_logits_topk_noalloc(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
                              float *logits, pmqa_stream_t stream);
+
+/*
+ * Prefill (non-paged) logits. Source: the page "[Bug] aiter ops triton
+ * attention pa", section "Observations while narrowing it down", which names
+ * the prefill indexer `fp8_mqa_logits` (heads 32, head_dim 128, up to 8192 keys,
+ * query lengths up to 4096) beside the paged decode kernel. The pages give only
+ * its name and shapes; it is read as the decode definition with the paging
+ * removed and one key range per query row:
+ *   logits[r][t] = sum_h weights[r][h] * relu(k_scale[t] * dot(q[r][h], k_t))
+ *                  for max(ks[r], 0) <= t < min(ke[r], n), else -inf,
+ * for every query row r < m and key t < n.
+ *   q        fp8 e4m3fn [m, heads, head_dim], contiguous, 16-byte aligned
+ *   k        fp8 e4m3fn [n, head_dim], contiguous, 16-byte aligned
+ *   k_scale  fp32 [n], 4-byte aligned
+ *   weights  fp32 [m, heads], contiguous, 16-byte aligned
+ *   ks, ke   int32 [m]: row r's key range [ks[r], ke[r]); values outside [0, n]
+ *            are clamped, ks >= ke gives an all -inf row
+ * head_dim must be 128 and heads one of 16, 32, 64, 128; m * heads < 2^31.
+ */
+typedef struct pmqa_mqa_problem {
+    const void *q;
+    const void *k;
+    const float *k_scale;
+    const float *weights;
+    const int32_t *ks;
+    const int32_t *ke;
+    int32_t m;
+    int32_t n;
+    int32_t heads;
+    int32_t head_dim;
+} pmqa_mqa_problem;
+
+/*
+ * logits: fp32 [m, n], 4-byte aligned; every entry is written. ws: at least
+ * pmqa_workspace_bytes(..., PMQA_OP_MQA_LOGITS) = 256 bytes, 256-byte aligned
+ * and zero-filled before first use; only its status word is used (a pipeline
+ * wait that ran out sets PMQA_DEV_TIMEOUT).
+ */
+int pmqa_mqa_logits(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_bytes,
+                    pmqa_stream_t stream);
 
 /*
  * Synchronise the stream, return the device status bits recorded since the

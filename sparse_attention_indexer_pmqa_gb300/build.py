@@ -1,7 +1,8 @@
 """Build libpmqa.so in-tree with nvcc for sm_103a (GB300).
 
-Six translation units compile in parallel (the C ABI, the allocation-free
-entry point and one per supported head count) and link into one shared library
+Ten translation units compile in parallel (the C ABI, the allocation-free
+entry point, and the decode and the prefill kernel once per supported head
+count) and link into one shared library
 with the CUDA runtime linked statically, so the library loads on a machine
 without a GPU too.
 """
@@ -35,6 +36,8 @@ def _sources():
              ("pmqa_noalloc", os.path.join(CSRC, "pmqa_noalloc.cu"), [])]
     for h in HEADS:
         units.append((f"pmqa_main_h{h}", os.path.join(CSRC, "pmqa_main_inst.cu"),
+                      [f"-DPMQA_HEADS={h}"]))
+        units.append((f"pmqa_prefill_h{h}", os.path.join(CSRC, "pmqa_prefill_inst.cu"),
                       [f"-DPMQA_HEADS={h}"]))
     return units, deps
 

@@ -9,6 +9,7 @@
 
 #include "../../include/pmqa.h"
 #include "pmqa_main.cuh"
+#include "pmqa_prefill.cuh"
 #include "pmqa_select.cuh"
 
 namespace pmqa {
@@ -16,6 +17,10 @@ cudaError_t launch_main_h16(const MainArgs &, int, int, cudaStream_t);
 cudaError_t launch_main_h32(const MainArgs &, int, int, cudaStream_t);
 cudaError_t launch_main_h64(const MainArgs &, int, int, cudaStream_t);
 cudaError_t launch_main_h128(const MainArgs &, int, int, cudaStream_t);
+cudaError_t launch_prefill_h16(const PfArgs &, int, int, cudaStream_t);
+cudaError_t launch_prefill_h32(const PfArgs &, int, int, cudaStream_t);
+cudaError_t launch_prefill_h64(const PfArgs &, int, int, cudaStream_t);
+cudaError_t launch_prefill_h128(const PfArgs &, int, int, cudaStream_t);
 size_t fused_ws_zero_bytes(int bs, int next_n);
 }  // namespace pmqa
 
@@ -23,7 +28,7 @@ using namespace pmqa;
 
 namespace {
 
-constexpr int kVersion = 200;  // 0.2.0
+constexpr int kVersion = 300;  // 0.3.0
 // 227 KB per CTA, shared between the static CtaCtl block and the dynamic layout
 constexpr uint32_t kMaxDynSmem = 232448 - ((uint32_t)sizeof(CtaCtl) + 127u) / 128u * 128u;
 constexpr uint32_t kMinMainSmem = 120 * 1024;  // > half an SM: one CTA per SM
@@ -148,16 +153,16 @@ EncodeTiledFn encode_tiled()
     return fn;
 }
 
-// q viewed as [bs * N rows, 128 bytes]; box [128 bytes, q_box rows]; 128B swizzle.
-// q_box = N / ceil(N / 256) <= 256 rows, so whole boxes cover one request exactly.
-bool encode_q_map(CUtensorMap *m, const void *q, long long rows, int q_box)
+// A [rows, 128 bytes] fp8 matrix as a 2-D tensor map; box [128 bytes, box_rows
+// rows]; 128B swizzle (the K-major operand layout). Rows past the end read as zeros.
+bool encode_rows_map(CUtensorMap *m, const void *q, long long rows, int box_rows)
 {
     EncodeTiledFn fn = encode_tiled();
     if (!fn)
         return false;
     const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
-    const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)q_box};
+    const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(q), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -241,7 +246,9 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     a.q_box = a.N / nbox;
     if (a.q_box * nbox != a.N || a.q_box % 8 != 0)
         return PMQA_ERR_UNSUPPORTED;
-    if (!encode_q_map(&a.tmap_q, p->q, rows * p->heads, a.q_box))
+    // q as [bs * N rows, 128 bytes]; q_box = N / ceil(N / 256) <= 256 rows, so
+    // whole boxes cover one request exactly
+    if (!encode_rows_map(&a.tmap_q, p->q, rows * p->heads, a.q_box))
         return PMQA_ERR_CUDA;
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     a.q = static_cast<const uint8_t *>(p->q);
@@ -290,6 +297,87 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     return launch_select(s, false, stream);
 }
 
+// Shared-memory layout of the prefill kernel: a ring of S key stages, QS query
+// slots of 4 * G query rows (512 Q rows of 128 bytes) and their weights, the
+// mbarriers and the per-stage counters.
+bool pf_layout(int heads, PfArgs &a)
+{
+    a.G = kPassCols / heads;
+    a.SGR = kGroups * a.G;
+    const uint32_t N = (uint32_t)(a.SGR * heads);
+    for (int S = kPfMaxStages; S >= 2; --S)
+        for (int QS = 2; QS >= 1; --QS) {
+            uint32_t off = 0;
+            a.off_k = off;  // 1024-byte aligned stages
+            off += (uint32_t)S * kStageBytes;
+            a.off_q = off;
+            off += (uint32_t)QS * N * kHeadDim;
+            a.off_w = off;
+            off += (uint32_t)QS * N * 4u;
+            off = (uint32_t)align_up(off, 16);
+            a.off_bar = off;
+            off += (uint32_t)(S + QS + kGroups) * 8u + (uint32_t)S * 4u;
+            const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
+            if (total > kMaxDynSmem)
+                continue;
+            a.S = S;
+            a.QS = QS;
+            a.smem_bytes = total;
+            return true;
+        }
+    return false;
+}
+
+int run_prefill(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_bytes,
+                cudaStream_t stream)
+{
+    if (!p || p->m < 0 || p->n < 0 || p->heads < 1 || p->head_dim < 1)
+        return PMQA_ERR_INVALID_ARG;
+    if (p->head_dim != kHeadDim || !supported_heads(p->heads))
+        return PMQA_ERR_UNSUPPORTED;
+    if ((long long)p->m * p->heads >= (1ll << 31))
+        return PMQA_ERR_UNSUPPORTED;
+    if (!ws || !aligned(ws, kWsAlign))
+        return PMQA_ERR_INVALID_ARG;
+    if (ws_bytes < kWsAlign)
+        return PMQA_ERR_WORKSPACE;
+    if (p->m == 0 || p->n == 0)
+        return PMQA_OK;
+    if (!p->q || !p->k || !p->k_scale || !p->weights || !p->ks || !p->ke || !logits)
+        return PMQA_ERR_INVALID_ARG;
+    if (!aligned(p->q, 16) || !aligned(p->k, 16) || !aligned(p->weights, 16) ||
+        !aligned(p->k_scale, 4) || !aligned(p->ks, 4) || !aligned(p->ke, 4) || !aligned(logits, 4))
+        return PMQA_ERR_INVALID_ARG;
+    PfArgs a{};
+    if (!pf_layout(p->heads, a))
+        return PMQA_ERR_UNSUPPORTED;
+    const int N = a.SGR * p->heads;
+    a.q_box = N / ((N + 255) / 256);
+    if (!encode_rows_map(&a.tmap_q, p->q, (long long)p->m * p->heads, a.q_box) ||
+        !encode_rows_map(&a.tmap_k, p->k, p->n, kTileTokens))
+        return PMQA_ERR_CUDA;
+    a.k_scale = p->k_scale;
+    a.w = p->weights;
+    a.ks = p->ks;
+    a.ke = p->ke;
+    a.logits = logits;
+    a.status = static_cast<uint32_t *>(ws);
+    a.m = p->m;
+    a.n = p->n;
+    a.n_sg = (p->m + a.SGR - 1) / a.SGR;
+    int sms = 0, rc;
+    if ((rc = sm_count(&sms)) != PMQA_OK)
+        return rc;
+    cudaError_t e;
+    switch (p->heads) {
+    case 16: e = launch_prefill_h16(a, sms, kMaxThreads, stream); break;
+    case 32: e = launch_prefill_h32(a, sms, kMaxThreads, stream); break;
+    case 64: e = launch_prefill_h64(a, sms, kMaxThreads, stream); break;
+    default: e = launch_prefill_h128(a, sms, kMaxThreads, stream); break;
+    }
+    return e == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
+}
+
 }  // namespace
 
 namespace pmqa {
@@ -308,6 +396,8 @@ extern "C" {
 size_t pmqa_workspace_bytes(int32_t bs, int32_t next_n, int32_t max_model_len, int32_t k, int op)
 {
     (void)k;
+    if (op == PMQA_OP_MQA_LOGITS)
+        return kWsAlign;
     if (bs < 0 || next_n < 1 || max_model_len < 1)
         return 0;
     WsLayout L;
@@ -366,6 +456,12 @@ int pmqa_topk(const float *logits, const int32_t *context_lens, int32_t bs, int3
     const SelectArgs s =
         select_args(logits, context_lens, bs, next_n, max_model_len, k, idx, vals, ws, L);
     return launch_select(s, true, stream);
+}
+
+int pmqa_mqa_logits(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_bytes,
+                    pmqa_stream_t stream)
+{
+    return run_prefill(p, logits, ws, ws_bytes, stream);
 }
 
 int pmqa_read_device_status(void *ws, pmqa_stream_t stream)

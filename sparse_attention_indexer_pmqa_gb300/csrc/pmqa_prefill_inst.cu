@@ -1,0 +1,28 @@
+// pmqa_prefill_inst.cu -- the prefill kernel for one head count per
+// translation unit (-DPMQA_HEADS=16, 32, 64 or 128), compiled in parallel.
+#include <cuda_runtime.h>
+
+#include "pmqa_prefill.cuh"
+
+#ifndef PMQA_HEADS
+#error "PMQA_HEADS must be defined"
+#endif
+
+#define PMQA_CAT2(a, b) a##b
+#define PMQA_CAT(a, b) PMQA_CAT2(a, b)
+
+namespace pmqa {
+
+cudaError_t PMQA_CAT(launch_prefill_h, PMQA_HEADS)(const PfArgs &a, int grid, int threads,
+                                                   cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(pmqa_prefill_kernel<PMQA_HEADS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)a.smem_bytes);
+    if (e != cudaSuccess)
+        return e;
+    pmqa_prefill_kernel<PMQA_HEADS><<<grid, threads, a.smem_bytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace pmqa

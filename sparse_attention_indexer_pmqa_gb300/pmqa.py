@@ -28,6 +28,7 @@ PMQA_DEV_OVERFLOW = 0x8
 PMQA_OP_LOGITS = 0
 PMQA_OP_TOPK = 1
 PMQA_OP_LOGITS_TOPK = 2
+PMQA_OP_MQA_LOGITS = 3
 
 PMQA_STAGE_SCORE = 1
 PMQA_STAGE_SELECT = 2
@@ -35,7 +36,7 @@ PMQA_STAGE_SELECT = 2
 EXPORTED = (
     "pmqa_workspace_bytes", "pmqa_workspace_init", "pmqa_logits", "pmqa_topk",
     "pmqa_logits_topk", "pmqa_logits_topk_stages", "pmqa_logits_topk_noalloc",
-    "pmqa_read_device_status",
+    "pmqa_mqa_logits", "pmqa_read_device_status",
     "pmqa_status_string", "pmqa_version",
 )
 
@@ -66,6 +67,23 @@ class Problem(ctypes.Structure):
     ]
 
 
+class MqaProblem(ctypes.Structure):
+    """Mirror of struct pmqa_mqa_problem."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("weights", ctypes.c_void_p),
+        ("ks", ctypes.c_void_p),
+        ("ke", ctypes.c_void_p),
+        ("m", ctypes.c_int32),
+        ("n", ctypes.c_int32),
+        ("heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+    ]
+
+
 _lib = None
 
 
@@ -85,6 +103,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     PP = ctypes.POINTER(Problem)
+    PM = ctypes.POINTER(MqaProblem)
     sig = {
         "pmqa_workspace_bytes": ([I32, I32, I32, I32, ctypes.c_int], SZ),
         "pmqa_workspace_init": ([V, SZ, V], ctypes.c_int),
@@ -93,6 +112,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pmqa_logits_topk": ([PP, I32, V, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_logits_topk_stages": ([PP, I32, V, V, V, V, SZ, V, I32], ctypes.c_int),
         "pmqa_logits_topk_noalloc": ([PP, I32, V, V, V, V], ctypes.c_int),
+        "pmqa_mqa_logits": ([PM, V, V, SZ, V], ctypes.c_int),
         "pmqa_read_device_status": ([V, V], ctypes.c_int),
         "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pmqa_version": ([], ctypes.c_int),
@@ -237,6 +257,32 @@ def pmqa_logits_topk_noalloc(q, kv_cache, weights, context_lens, block_tables,
     _check(load().pmqa_logits_topk_noalloc(ctypes.byref(p), k, _ptr(idx), _ptr(vals), _ptr(logits),
                                            _stream(stream)), "pmqa_logits_topk_noalloc")
     return idx
+
+
+def make_mqa_problem(q, k, k_scale, weights, ks, ke) -> MqaProblem:
+    """Fill a pmqa_mqa_problem from tensors shaped as in the C header."""
+    m, heads, head_dim = q.shape
+    n = k.shape[0]
+    assert k.shape[1] == head_dim and k_scale.shape[0] == n
+    for t in (q, k, k_scale, weights, ks, ke):
+        assert t.is_cuda and t.is_contiguous()
+    return MqaProblem(q=q.data_ptr(), k=k.data_ptr(), k_scale=k_scale.data_ptr(),
+                      weights=weights.data_ptr(), ks=ks.data_ptr(), ke=ke.data_ptr(),
+                      m=m, n=n, heads=heads, head_dim=head_dim)
+
+
+def pmqa_mqa_logits(q, k, k_scale, weights, ks, ke, *, out=None, ws=None, stream=None):
+    """Prefill logits fp32 [m, n] over the rows' key ranges [ks, ke)."""
+    import torch
+
+    p = make_mqa_problem(q, k, k_scale, weights, ks, ke)
+    if out is None:
+        out = torch.empty((p.m, p.n), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(0, 1, 1, 0, PMQA_OP_MQA_LOGITS, q.device, stream)
+    _check(load().pmqa_mqa_logits(ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "pmqa_mqa_logits")
+    return out
 
 
 def pmqa_read_device_status(ws, stream=None) -> int:

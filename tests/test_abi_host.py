@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert pmqa.pmqa_version() == 200
+    assert pmqa.pmqa_version() == 300
     assert pmqa.status_string(0) == "ok"
     assert pmqa.status_string(-3) == "workspace too small"
     assert pmqa.status_string(12345) == "unknown status"
@@ -147,3 +147,42 @@ def test_workspace_init_checks(lib):
     assert lib.pmqa_workspace_init(None, 1024, None) == -1
     assert lib.pmqa_workspace_init(ctypes.c_void_p(0x100004), 1024, None) == -1
     assert lib.pmqa_read_device_status(None, None) == -1
+
+
+def _mqa(**kw):
+    base = dict(q=0x10000, k=0x20000, k_scale=0x30000, weights=0x40000, ks=0x50000,
+                ke=0x58000, m=8, n=256, heads=32, head_dim=128)
+    base.update(kw)
+    return pmqa.MqaProblem(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=64), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(heads=48), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(m=1 << 27, heads=16), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(m=-1), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(n=-1), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(heads=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(q=None), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(ke=None), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(q=0x10008), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(k=0x20004), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(weights=0x40004), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(k_scale=0x30002), pmqa.PMQA_ERR_INVALID_ARG),
+])
+def test_mqa_problem_validation(lib, kw, code):
+    p = _mqa(**kw)
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), ctypes.c_void_p(0x60000), WS, 256, None) == code
+
+
+def test_mqa_workspace_and_empty_shapes(lib):
+    assert pmqa.pmqa_workspace_bytes(0, 0, 0, 0, pmqa.PMQA_OP_MQA_LOGITS) == 256
+    p = _mqa()
+    out = ctypes.c_void_p(0x60000)
+    assert lib.pmqa_mqa_logits(None, out, WS, 256, None) == -1
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), None, WS, 256, None) == -1
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), out, WS, 255, None) == pmqa.PMQA_ERR_WORKSPACE
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), out, ctypes.c_void_p(0x100010), 256, None) == -1
+    # nothing to compute: no pointer is needed and nothing is launched
+    assert lib.pmqa_mqa_logits(ctypes.byref(_mqa(m=0, q=None)), None, WS, 256, None) == 0
+    assert lib.pmqa_mqa_logits(ctypes.byref(_mqa(n=0, k=None)), None, WS, 256, None) == 0
