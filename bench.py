@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--prefill", action="store_true",
+                    help="also time the prefill (non-paged) logits on PF1 (on with --all)")
     return ap.parse_args(argv)
 
 
@@ -92,6 +94,17 @@ def sum_over_ranks(x: float, dist, device=None) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def read_tensor_peak():
+    """Dense fp8 tensor peak (TFLOP/s): the measured bf16 cuBLAS burst figure
+    times the nominal fp8 / bf16 ratio of 2, or the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "measured bf16_tflops x 2 (fp8/bf16)"
+    except (OSError, KeyError, ValueError):
+        return 2.0 * 1900.0, "fallback bf16 1900 TFLOP/s x 2 (fp8/bf16)"
 
 
 def read_peak():
@@ -372,6 +385,57 @@ def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
     return out
 
 
+def bench_prefill(name, args, device):
+    """Prefill logits (pmqa_mqa_logits) on one prefill workload: every step
+    writes the whole [m, n] logits matrix; L2 flushed before each step."""
+    import torch
+
+    from sparse_attention_indexer_pmqa_gb300 import pmqa
+    from synth import PREFILL_CONFIGS, prefill_config
+
+    p = prefill_config(name)
+    q = torch.from_numpy(p.q).to(device).view(torch.float8_e4m3fn)
+    k = torch.from_numpy(p.k).to(device).view(torch.float8_e4m3fn)
+    sc = torch.from_numpy(p.k_scale).to(device)
+    w = torch.from_numpy(p.weights).to(device)
+    ks = torch.from_numpy(p.ks).to(device)
+    ke = torch.from_numpy(p.ke).to(device)
+    out = torch.empty((p.m, p.n), dtype=torch.float32, device=device)
+    ws = pmqa.workspace(p.m, 1, p.n, 0, pmqa.PMQA_OP_MQA_LOGITS, device)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    def step():
+        pmqa.pmqa_mqa_logits(q, k, sc, w, ks, ke, out=out, ws=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    times = time_steps(step, min(args.steps, 100), flush)
+    status = pmqa.pmqa_read_device_status(ws)
+    if status:
+        raise RuntimeError(f"device status {status:#x} during the prefill steps")
+    ms = statistics.fmean(times)
+    pairs = p.pairs
+    flops = 2.0 * p.heads * 128 * pairs
+    peak, peak_kind = read_tensor_peak()
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {
+        "workload": f"{name}: {PREFILL_CONFIGS[name]['desc']}",
+        "ms": ms, "ms_median": statistics.median(times),
+        "pairs": pairs, "pairs_per_s": pairs / (ms * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "peak_source": peak_kind,
+                     "algorithmic_flops_per_launch": flops,
+                     "kernel": f"pmqa_prefill_kernel<{p.heads}>"},
+        "out_gbs": p.m * p.n * 4 / (ms * 1e-3) / 1e9,
+        "launches": 1,
+    }
+
+
 def cpu_baseline(prob, min_seconds: float = 10.0, max_reps: int = 60):
     """The oracle, as it stands, on the whole workload (logits + top-k)."""
     import oracle
@@ -479,6 +543,8 @@ def run_ours(args):
                        "score_frac": sbw["total"] / (r["ms_score"] * 1e-3) / 1e9 / peak,
                        "paths_ms": r.get("paths_ms")}
         line["workloads"] = per
+    if args.all or args.prefill:
+        line["prefill"] = bench_prefill("PF1", args, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob)
     if rank == 0:

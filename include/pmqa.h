@@ -65,8 +65,9 @@ enum {
 #define PMQA_DEV_TIMEOUT 0x4u      /* a pipeline wait exceeded its limit; results are invalid */
 #define PMQA_DEV_OVERFLOW 0x8u     /* top-k candidate storage exceeded; results are invalid */
 
-/* Workspace-size selector for pmqa_workspace_bytes. PMQA_OP_MQA_LOGITS (the
-   prefill entry point) needs only the status word: 256 bytes for any size. */
+/* Workspace-size selector for pmqa_workspace_bytes. For PMQA_OP_MQA_LOGITS (the
+   prefill entry point) bs is the number of query rows m and the other sizes
+   are ignored. */
 enum { PMQA_OP_LOGITS = 0, PMQA_OP_TOPK = 1, PMQA_OP_LOGITS_TOPK = 2, PMQA_OP_MQA_LOGITS = 3 };
 
 /*
@@ -205,9 +206,10 @@ typedef struct pmqa_mqa_problem {
 
 /*
  * logits: fp32 [m, n], 4-byte aligned; every entry is written. ws: at least
- * pmqa_workspace_bytes(..., PMQA_OP_MQA_LOGITS) = 256 bytes, 256-byte aligned
- * and zero-filled before first use; only its status word is used (a pipeline
- * wait that ran out sets PMQA_DEV_TIMEOUT).
+ * pmqa_workspace_bytes(m, 1, n, 0, PMQA_OP_MQA_LOGITS) bytes (256 + 8 per 4
+ * query rows, rounded up to 256), 256-byte aligned, zero-filled before first
+ * use; it holds the status word (a pipeline wait that ran out sets
+ * PMQA_DEV_TIMEOUT) and per-call scratch. Two kernel launches.
  */
 int pmqa_mqa_logits(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_bytes,
                     pmqa_stream_t stream);

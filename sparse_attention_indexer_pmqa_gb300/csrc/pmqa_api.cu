@@ -297,36 +297,42 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     return launch_select(s, false, stream);
 }
 
-// Shared-memory layout of the prefill kernel: a ring of S key stages, QS query
+// Shared-memory layout of the prefill kernel: a ring of S key stages, two query
 // slots of 4 * G query rows (512 Q rows of 128 bytes) and their weights, the
-// mbarriers and the per-stage counters.
+// pair-exchange buffer, the mbarriers and the counters.
 bool pf_layout(int heads, PfArgs &a)
 {
     a.G = kPassCols / heads;
     a.SGR = kGroups * a.G;
     const uint32_t N = (uint32_t)(a.SGR * heads);
-    for (int S = kPfMaxStages; S >= 2; --S)
-        for (int QS = 2; QS >= 1; --QS) {
-            uint32_t off = 0;
-            a.off_k = off;  // 1024-byte aligned stages
-            off += (uint32_t)S * kStageBytes;
-            a.off_q = off;
-            off += (uint32_t)QS * N * kHeadDim;
-            a.off_w = off;
-            off += (uint32_t)QS * N * 4u;
-            off = (uint32_t)align_up(off, 16);
-            a.off_bar = off;
-            off += (uint32_t)(S + QS + kGroups) * 8u + (uint32_t)S * 4u;
-            const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
-            if (total > kMaxDynSmem)
-                continue;
-            a.S = S;
-            a.QS = QS;
-            a.smem_bytes = total;
-            return true;
-        }
+    const int QS = 2;  // the next super-group's MMAs start before the current one's slot is freed
+    for (int S = kPfMaxStages; S >= 2; --S) {
+        uint32_t off = 0;
+        a.off_k = off;  // 1024-byte aligned stages
+        off += (uint32_t)S * kStageBytes;
+        a.off_q = off;
+        off += (uint32_t)QS * N * kHeadDim;
+        a.off_w = off;
+        off += (uint32_t)QS * N * 4u;
+        off = (uint32_t)align_up(off, 16);
+        a.off_x = off;  // partial sums exchanged by warpgroup pairs (128 heads)
+        off += 2u * 2u * 128u * 4u;
+        a.off_bar = off;
+        off += (uint32_t)(S + QS + 4) * 8u;
+        const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
+        if (total > kMaxDynSmem)
+            continue;
+        a.S = S;
+        a.QS = QS;
+        a.smem_bytes = total;
+        return true;
+    }
     return false;
 }
+
+// Prefill workspace: the status word, then one (first tile, tile count) pair
+// per super-group; super-groups hold at least 4 query rows.
+size_t pf_ws_bytes(long long m) { return kWsAlign + align_up((size_t)((m + 3) / 4) * 8, kWsAlign); }
 
 int run_prefill(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_bytes,
                 cudaStream_t stream)
@@ -339,7 +345,7 @@ int run_prefill(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_by
         return PMQA_ERR_UNSUPPORTED;
     if (!ws || !aligned(ws, kWsAlign))
         return PMQA_ERR_INVALID_ARG;
-    if (ws_bytes < kWsAlign)
+    if (ws_bytes < pf_ws_bytes(p->m))
         return PMQA_ERR_WORKSPACE;
     if (p->m == 0 || p->n == 0)
         return PMQA_OK;
@@ -362,18 +368,22 @@ int run_prefill(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_by
     a.ke = p->ke;
     a.logits = logits;
     a.status = static_cast<uint32_t *>(ws);
+    a.ranges = reinterpret_cast<int2 *>(static_cast<uint8_t *>(ws) + kWsAlign);
     a.m = p->m;
     a.n = p->n;
     a.n_sg = (p->m + a.SGR - 1) / a.SGR;
     int sms = 0, rc;
     if ((rc = sm_count(&sms)) != PMQA_OK)
         return rc;
+    pmqa_prefill_prep_kernel<<<std::min(a.n_sg, 8 * sms), 256, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess)
+        return PMQA_ERR_CUDA;
     cudaError_t e;
     switch (p->heads) {
-    case 16: e = launch_prefill_h16(a, sms, kMaxThreads, stream); break;
-    case 32: e = launch_prefill_h32(a, sms, kMaxThreads, stream); break;
-    case 64: e = launch_prefill_h64(a, sms, kMaxThreads, stream); break;
-    default: e = launch_prefill_h128(a, sms, kMaxThreads, stream); break;
+    case 16: e = launch_prefill_h16(a, sms, kPfThreads, stream); break;
+    case 32: e = launch_prefill_h32(a, sms, kPfThreads, stream); break;
+    case 64: e = launch_prefill_h64(a, sms, kPfThreads, stream); break;
+    default: e = launch_prefill_h128(a, sms, kPfThreads, stream); break;
     }
     return e == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }
@@ -397,7 +407,7 @@ size_t pmqa_workspace_bytes(int32_t bs, int32_t next_n, int32_t max_model_len, i
 {
     (void)k;
     if (op == PMQA_OP_MQA_LOGITS)
-        return kWsAlign;
+        return bs < 0 ? 0 : pf_ws_bytes(bs);
     if (bs < 0 || next_n < 1 || max_model_len < 1)
         return 0;
     WsLayout L;

@@ -7,17 +7,18 @@
 // logit = sum_h w[r][h] * relu(s_n * q[r][h] . k_n) for ks[r] <= n < ke[r],
 // -inf elsewhere.
 //
-// A CTA works on super-groups of 4 * G query rows (G = 128 / heads, so one
-// warpgroup's G rows fill 128 accumulator columns) and walks a contiguous,
-// tile-balanced range of (super-group, 128-key tile) items. Each key tile is
-// loaded once by TMA, already in the 128B-swizzled K-major operand layout, into
-// a ring of S stages that all four warpgroups read: warpgroup g multiplies it
-// by the Q rows of its G query rows, D[key][(row, h)] in its own 128 TMEM
-// columns, and reduces its accumulators with the same epilogue as the paged
-// kernel (thread = key = TMEM lane). The last warpgroup whose MMA on a stage
-// completes refills that stage with the tile S items ahead. Query rows and
-// weights of the super-group QS ahead are loaded at super-group ends, as in the
-// paged kernel. Every wait is bounded.
+// A CTA works on super-groups of SGR = 4 G query rows (G = 128 / heads) and
+// walks a contiguous, tile-balanced range of (super-group, 128-key tile)
+// items. Warp 16 is the control warp: its lane 0 loads every key tile (TMA,
+// already in the 128B-swizzled K-major operand layout, a ring of S stages),
+// every query slot, and issues every MMA. Warps 0-15 are four warpgroups;
+// warpgroup g owns TMEM columns [128 g, 128 g + 128), the accumulators
+// D[key][(row, h)] = K_tile * Q^T of its G rows (one N = 128 MMA per item),
+// and reduces them (thread = key = TMEM lane): sum_h w[row][h] * relu(s_key *
+// x), masked to the row's key range. The warpgroups run independently of one
+// another, each handing its columns back to the control warp through an
+// mbarrier, so one warpgroup's reduction overlaps the others' MMAs and TMEM
+// reads. Every wait is bounded.
 #pragma once
 
 #include "pmqa_main.cuh"
@@ -34,57 +35,90 @@ struct PfArgs {
     const int32_t *ks, *ke;
     float *logits;  // [m, n]
     uint32_t *status;
+    int2 *ranges;   // per super-group: first key tile, tile count (written by the prep kernel)
     int m, n;
     int G;     // query rows per warpgroup (128 / heads)
     int SGR;   // query rows per super-group (4 * G)
     int n_sg;  // super-groups: ceil(m / SGR)
     int S, QS, q_box;
-    uint32_t off_k, off_q, off_w, off_bar, smem_bytes;
+    uint32_t off_k, off_q, off_w, off_x, off_bar, smem_bytes;
 };
 
-// Tile range [lo, lo + nt) of super-group sg: the union of its rows' key ranges.
-struct PfRange {
-    int lo, nt;
-};
+// ---------------------------------------------------------------- prep kernel
 
-__device__ __forceinline__ PfRange pf_range(const PfArgs &a, int sg)
+// One CTA per super-group (grid-strided): the tile range [lo, lo + nt) that
+// covers the union of its rows' key ranges, and -inf in every entry of its
+// rows outside those tiles (the main kernel writes the entries inside).
+static __global__ void __launch_bounds__(256) pmqa_prefill_prep_kernel(const __grid_constant__ PfArgs a)
 {
-    int lo = 0x7FFFFFFF, hi = 0;
-    const int r0 = sg * a.SGR, r1 = min(r0 + a.SGR, a.m);
-    for (int r = r0; r < r1; ++r) {
-        const int s = max(__ldg(a.ks + r), 0), e = min(__ldg(a.ke + r), a.n);
-        if (e > s) {
-            lo = min(lo, s);
-            hi = max(hi, e);
+    __shared__ int2 rng;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    for (int sg = blockIdx.x; sg < a.n_sg; sg += gridDim.x) {
+        if (tid < 32) {
+            const int r = sg * a.SGR + lane;
+            int lo = 0x7FFFFFFF, hi = 0;
+            if (lane < a.SGR && r < a.m) {
+                const int s = max(__ldg(a.ks + r), 0), e = min(__ldg(a.ke + r), a.n);
+                if (e > s) {
+                    lo = s;
+                    hi = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                lo = min(lo, __shfl_xor_sync(kFullMask, lo, o));
+                hi = max(hi, __shfl_xor_sync(kFullMask, hi, o));
+            }
+            if (lane == 0) {
+                int2 R = make_int2(0, 0);
+                if (hi > 0) {
+                    R.x = lo / kTileTokens;
+                    R.y = (hi + kTileTokens - 1) / kTileTokens - R.x;
+                }
+                a.ranges[sg] = R;
+                rng = R;
+            }
         }
+        __syncthreads();
+        const int2 R = rng;
+        const long long n = a.n;
+        const long long c0 = R.y > 0 ? (long long)R.x * kTileTokens : n;
+        const long long c1 = R.y > 0 ? min((long long)(R.x + R.y) * kTileTokens, n) : n;
+        const int r1 = min(a.SGR, a.m - sg * a.SGR);
+        for (int j = 0; j < r1; ++j) {
+            float *row = a.logits + (long long)(sg * a.SGR + j) * n;
+            for (long long x = tid; x < c0; x += blockDim.x)
+                row[x] = NEG_INF;
+            for (long long x = c1 + tid; x < n; x += blockDim.x)
+                row[x] = NEG_INF;
+        }
+        __syncthreads();  // rng is rewritten for the next super-group
     }
-    PfRange R;
-    if (hi == 0) {
-        R.lo = 0;
-        R.nt = 0;
-    } else {
-        R.lo = lo / kTileTokens;
-        R.nt = (hi + kTileTokens - 1) / kTileTokens - R.lo;
-    }
-    return R;
 }
+
+// ---------------------------------------------------------------- main kernel
 
 // Position (super-group sg, tile m of nt, first tile lo) in a CTA's walk over
 // (super-group, tile) items; empty super-groups are skipped.
 struct PfPos {
     int sg, m, nt, lo;
+    __device__ void load(const PfArgs &a)
+    {
+        if (sg < a.n_sg) {
+            const int2 R = a.ranges[sg];
+            lo = R.x;
+            nt = R.y;
+        } else {
+            lo = 0;
+            nt = 0;
+        }
+    }
     __device__ void at(const PfArgs &a, int g, int mm)
     {
         sg = g;
         m = mm;
-        if (sg < a.n_sg) {
-            const PfRange R = pf_range(a, sg);
-            nt = R.nt;
-            lo = R.lo;
-        } else {
-            nt = 0;
-            lo = 0;
-        }
+        load(a);
     }
     __device__ void next(const PfArgs &a)
     {
@@ -92,32 +126,26 @@ struct PfPos {
             return;
         m = 0;
         do {
-            if (++sg >= a.n_sg) {
-                nt = 0;
-                return;
-            }
-            const PfRange R = pf_range(a, sg);
-            nt = R.nt;
-            lo = R.lo;
-        } while (nt == 0);
+            ++sg;
+            load(a);
+        } while (nt == 0 && sg < a.n_sg);
     }
     __device__ int tile() const { return lo + m; }
 };
 
-// Shared-memory mbarriers of the prefill kernel, and the per-stage counters of
-// warpgroups done with a stage.
-//   kfull[S]   a key tile landed in stage s
-//   qfull[QS]  query rows + weights of a super-group landed
-//   mma[4]     a warpgroup's MMA finished
+// Shared-memory mbarriers of the prefill kernel.
+//   kfull[S]    a key tile landed in stage s
+//   qfull[QS]   query rows + weights of a super-group landed
+//   acc[2]      pair p's MMA finished (TMEM columns [256 p, 256 p + 256): warpgroups 2 p, 2 p + 1)
+//   bufree[2]   both warpgroups of pair p have read their columns (2 arrivals)
 struct PfBars {
-    uint64_t *kfull, *qfull, *mma;
-    int *done;
+    uint64_t *kfull, *qfull, *acc, *bufree;
     __device__ PfBars(const PfArgs &a, uint8_t *smem)
     {
         kfull = reinterpret_cast<uint64_t *>(smem + a.off_bar);
         qfull = kfull + a.S;
-        mma = qfull + a.QS;
-        done = reinterpret_cast<int *>(mma + kGroups);
+        acc = qfull + a.QS;
+        bufree = acc + 2;
     }
 };
 
@@ -146,37 +174,30 @@ __device__ __forceinline__ void pf_load_query(const PfArgs &a, uint8_t *smem, co
               a.w + (long long)sg * N, w_bytes, &B.qfull[slot]);
 }
 
-// Warpgroup g, warp quadrant qd: every item of the CTA's range, query rows
-// g * G .. g * G + G - 1 of each super-group.
+constexpr int kPfWarps = 4 * kGroups + 1;  // four reducing warpgroups and the control warp
+constexpr int kPfThreads = 32 * kPfWarps;
+// Register bound of the kernel: 5 of the 17 warps share one SM sub-partition
+// (16K registers), so at most 96 registers per thread.
+constexpr int kPfBoundThreads = 640;
+
+// Lane 0 of the control warp: every load and every MMA of the CTA's range.
+// For item k it issues pair p's MMA (N = 256: the 2 G query rows of
+// warpgroups 2 p and 2 p + 1 against the key tile) once both have read their
+// columns of item k - 1.
 template <int H>
-static __device__ void pf_group_role(const PfArgs &a, uint8_t *smem, CtaCtl &c, int g, int qd)
+static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int (&kissued)[kPfMaxStages],
+                                  int &qloads)
 {
-    constexpr int G = kPassCols / H;
     const PfBars B(a, smem);
-    const int lane = threadIdx.x & 31;
-    const uint32_t R = (uint32_t)(qd * 32 + lane);  // key of the tile = TMEM lane
-    const bool elected = qd == 0 && lane == 0;
-    const uint32_t wg_bar = 1u + (uint32_t)g;
     const int count = (int)c.count;
-    const int S = a.S, QS = a.QS, SGR = a.SGR, m = a.m, n = a.n;
+    const int S = a.S, QS = a.QS;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t kbase = sbase + a.off_k;
-    const uint32_t q_slot_bytes = (uint32_t)(SGR * H * kHeadDim);
-    const uint32_t w_slot_bytes = (uint32_t)(SGR * H * 4);
-    // this warpgroup's G query rows inside a query slot
-    const uint32_t q_off = (uint32_t)(g * G * H * kHeadDim);
-    const uint32_t w_off = (uint32_t)(g * G * H * 4);
-    const uint32_t dcol = c.tmem_base + (uint32_t)(g * kPassCols);
-    const uint32_t tacc = dcol + ((uint32_t)(qd * 32) << 16);
-    const uint32_t idesc = idesc_e4m3_f32(128, G * H);
-    float *const logits = a.logits;
-    const float NEG_INF = -__int_as_float(0x7f800000);
+    const uint32_t q_slot_bytes = (uint32_t)(a.SGR * H * kHeadDim);
+    const uint32_t idesc = idesc_e4m3_f32(128, 2 * kPassCols);
 
-    int q_slot = 0;
-    uint32_t q_phase = 0;
-    bool have_q = false;
-    int loads = 0;  // query loads issued (thread 0)
-    PfPos nxt;      // next super-group whose query is to be loaded (thread 0)
+    // query slots: super-group n of the range in slot n % QS
+    PfPos nxt;
     nxt.at(a, c.i0, c.m0);
     int nxt_first = 0;  // CTA item index of nxt's current tile
     auto nxt_valid = [&]() { return nxt.nt > 0 && nxt_first < count; };
@@ -185,179 +206,210 @@ static __device__ void pf_group_role(const PfArgs &a, uint8_t *smem, CtaCtl &c, 
         nxt.m = nxt.nt - 1;
         nxt.next(a);
     };
-    if (threadIdx.x == 0) {
-        for (int u = 0; u < QS; ++u) {
-            if (nxt_valid()) {
-                pf_load_query(a, smem, B, u, nxt.sg, H);
-                ++loads;
-            }
-            nxt_advance();
+    for (int u = 0; u < QS; ++u) {
+        if (nxt_valid()) {
+            pf_load_query(a, smem, B, u, nxt.sg, H);
+            ++qloads;
         }
+        nxt_advance();
     }
-    // key tiles: thread 0 fills the first S stages; afterwards the last
-    // warpgroup done with a stage refills it (pre = the tile S items ahead)
-    PfPos pre;
-    pre.at(a, c.i0, c.m0);
-    if (threadIdx.x == 0)
-        for (int s = 0; s < S && s < count; ++s) {
-            pf_load_k(a, kbase, B, s, pre.tile());
-            pre.next(a);
-        }
-    else if (elected)
-        for (int s = 0; s < S && s < count; ++s)
-            pre.next(a);
+    // key tiles: items 0 .. S - 1 now; item k - 1 + S once item k - 1 is done
+    PfPos kp;
+    kp.at(a, c.i0, c.m0);
+    for (int s = 0; s < S && s < count; ++s) {
+        pf_load_k(a, kbase, B, s, kp.tile());
+        ++kissued[s];
+        kp.next(a);
+    }
 
-    PfPos cur;
-    cur.at(a, c.i0, c.m0);
-    int rks[G], rke[G];  // key ranges of this warpgroup's rows in the current super-group
-    int r0 = 0, nr = 0;
-    uint32_t mma_phase = 0;
-    for (int kk = 0; kk < count; ++kk) {
-        const int s = kk % S;
-        const uint32_t kphase = (uint32_t)(kk / S) & 1u;
-        const int tile = cur.tile();
-        const int t = tile * kTileTokens + (int)R;
-        const float sc = t < n ? __ldg(a.k_scale + t) : 0.0f;
+    PfPos ip;
+    ip.at(a, c.i0, c.m0);
+    int islot = 0, prev_slot = 0;
+    uint32_t iqphase = 0;
+    bool prev_last = false, ok = true, have_q = false;
+    for (int k = 0; k < count; ++k) {
+        const int s = k % S;
+        const bool last = ip.m == ip.nt - 1 || k == count - 1;
+        ok = ok && mbar_wait(&B.kfull[s], (uint32_t)(k / S) & 1u, &c.abort);
         if (!have_q) {
-            r0 = cur.sg * SGR + g * G;
-            nr = max(0, min(G, m - r0));
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                rks[j] = j < nr ? __ldg(a.ks + r0 + j) : 0;
-                rke[j] = j < nr ? __ldg(a.ke + r0 + j) : 0;
-            }
-        }
-        // the previous epilogue's TMEM reads are done before the MMA overwrites
-        tc_fence_before_sync();
-        named_bar_sync(wg_bar, 128);
-        tc_fence_after_sync();
-        bool ok = true;
-        if (!have_q) {
-            ok = mbar_wait(&B.qfull[q_slot], q_phase, &c.abort);
+            ok = ok && mbar_wait(&B.qfull[islot], iqphase, &c.abort);
             have_q = true;
         }
-        bool mma_ok = true;
-        if (elected) {
-            mma_ok = mbar_wait(&B.kfull[s], kphase, &c.abort) && ok;
-            if (mma_ok) {
+        const uint64_t ad = sw128_kmajor_desc(kbase + (uint32_t)s * kStageBytes);
+        const uint64_t bd0 = sw128_kmajor_desc(sbase + a.off_q + (uint32_t)islot * q_slot_bytes);
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            // both warpgroups of pair p have read their columns of item k - 1
+            if (k > 0)
+                ok = ok && mbar_wait(&B.bufree[p], (uint32_t)(k - 1) & 1u, &c.abort);
+            if (ok) {
                 tc_fence_after_sync();
-                const uint64_t ad = sw128_kmajor_desc(kbase + (uint32_t)s * kStageBytes);
-                const uint64_t bd = sw128_kmajor_desc(sbase + a.off_q + (uint32_t)q_slot * q_slot_bytes +
-                                                      q_off);
+                const uint64_t bd = bd0 + (uint64_t)((uint32_t)(p * 2 * kPassCols * kHeadDim) >> 4);
 #pragma unroll
                 for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
-                    umma_e4m3(dcol, ad + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
-                umma_commit(&B.mma[g]);
-                mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
+                    umma_e4m3(c.tmem_base + (uint32_t)(p * 2 * kPassCols), ad + 2u * k4, bd + 2u * k4,
+                              idesc, k4 > 0 ? 1u : 0u);
+            } else if (!aborted(c)) {
+                c.abort = 1;
+                atomicOr(a.status, 0x4u);
             }
-            // the stage is free once all four warpgroups' MMAs on it completed;
-            // the fourth to get here refills it
-            const int done = atomicAdd(&B.done[s], 1) + 1;
-            if ((done & 3) == 0 && kk + S < count && !aborted(c))
-                pf_load_k(a, kbase, B, s, pre.tile());
-            if (kk + S < count)
-                pre.next(a);
+            // committed even when nothing was issued: the waiters' phases stay in step
+            umma_commit(&B.acc[p]);
         }
-        mma_phase ^= 1u;
-        ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
-        tc_fence_after_sync();
-        if (__all_sync(kFullMask, ok)) {
-            if (nr > 0) {
-                const uint32_t wsl =
-                    launder_u32(sbase + a.off_w + (uint32_t)q_slot * w_slot_bytes + w_off);
-                const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
-                const float mag = fabsf(sc);
-                const bool all_pos = __all_sync(kFullMask, flip == 0u);
-                float *const orow = logits + (long long)r0 * n + t;
-                auto out = [&](int j, float v) {
-                    if (t < n && j < nr)
-                        orow[(long long)j * n] = (t >= rks[j] && t < rke[j]) ? v : NEG_INF;
-                };
-                epi_dispatch<H, G>(nr, all_pos, tacc, wsl, flip, mag, 0, out);
+        if (k > 0 && ok) {
+            // every MMA of item k - 1 has completed (the warpgroups read their
+            // results): its key stage takes item k - 1 + S, and if it ended a
+            // super-group, that super-group's query slot takes the one QS ahead
+            if (k - 1 + S < count) {
+                pf_load_k(a, kbase, B, (k - 1) % S, kp.tile());
+                ++kissued[(k - 1) % S];
+                kp.next(a);
             }
-        } else {
-            c.abort = 1;
-            atomicOr(a.status, 0x4u);
-        }
-        // super-group end: all warpgroups meet, thread 0 loads the query of
-        // the super-group QS ahead into the freed slot
-        const bool last_of_sg = cur.m == cur.nt - 1 || kk == count - 1;
-        cur.next(a);
-        if (last_of_sg) {
-            named_bar_sync(kCtaBarrier, kMaxThreads);
-            if (threadIdx.x == 0) {
-                if (nxt_valid() && !aborted(c)) {
-                    pf_load_query(a, smem, B, q_slot, nxt.sg, H);
-                    ++loads;
+            if (prev_last) {
+                if (nxt_valid()) {
+                    pf_load_query(a, smem, B, prev_slot, nxt.sg, H);
+                    ++qloads;
                 }
                 nxt_advance();
             }
+        }
+        prev_last = last;
+        prev_slot = islot;
+        if (last) {
+            if (++islot == QS) {
+                islot = 0;
+                iqphase ^= 1u;
+            }
+            have_q = false;
+        }
+        ip.next(a);
+    }
+}
+
+// Warpgroup g, warp quadrant qd: the reductions of every item of the CTA's
+// range for query rows g * G .. g * G + G - 1 of each super-group (TMEM
+// columns 128 g .. 128 g + 127, thread = key = TMEM lane).
+template <int H>
+static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c, int g, int qd)
+{
+    constexpr int G = kPassCols / H;
+    const PfBars B(a, smem);
+    const int lane = threadIdx.x & 31;
+    const uint32_t R = (uint32_t)(qd * 32 + lane);
+    const bool elected = qd == 0 && lane == 0;
+    const uint32_t wg_bar = 1u + (uint32_t)g;
+    const int count = (int)c.count;
+    const int QS = a.QS, SGR = a.SGR, m = a.m, n = a.n;
+    const uint32_t w_slot_bytes = (uint32_t)(SGR * H * 4);
+    const uint32_t wbase = smem_u32(smem) + a.off_w + (uint32_t)(g * kPassCols * 4);
+    const uint32_t tacc = c.tmem_base + (uint32_t)(g * kPassCols) + ((uint32_t)(qd * 32) << 16);
+    float *const logits = a.logits;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+
+    PfPos cur;
+    cur.at(a, c.i0, c.m0);
+    int q_slot = 0;
+    uint32_t q_phase = 0;
+    bool have_q = false;
+    int r0 = 0, nr = 0;  // first row of this warpgroup in the super-group, rows that exist
+    for (int kk = 0; kk < count; ++kk) {
+        const int t = cur.tile() * kTileTokens + (int)R;
+        const float sc = t < n ? __ldg(a.k_scale + t) : 0.0f;
+        bool ok = true;
+        if (!have_q) {
+            r0 = cur.sg * SGR + g * G;
+            nr = max(0, min(G, m - r0));
+            ok = mbar_wait(&B.qfull[q_slot], q_phase, &c.abort);
+            have_q = true;
+        }
+        const uint32_t wsl = launder_u32(wbase + (uint32_t)q_slot * w_slot_bytes);
+        const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
+        const float mag = fabsf(sc);
+        bool acc_ok = true;
+        if (elected)
+            acc_ok = mbar_wait(&B.acc[g >> 1], (uint32_t)kk & 1u, &c.abort);
+        ok = named_bar_and(wg_bar, 128, acc_ok) && ok;
+        tc_fence_after_sync();
+        if (__all_sync(kFullMask, ok)) {
+            const bool all_pos = __all_sync(kFullMask, flip == 0u);
+            float *const orow = logits + (long long)r0 * n + t;
+            auto out = [&](int j, float v) {
+                if (t < n) {
+                    const bool in = t >= __ldg(a.ks + r0 + j) && t < __ldg(a.ke + r0 + j);
+                    orow[(long long)j * n] = in ? v : NEG_INF;
+                }
+            };
+            if (nr > 0)
+                epi_dispatch<H, G>(nr, all_pos, tacc, wsl, flip, mag, 0, out);
+        } else if (lane == 0 && !aborted(c)) {
+            c.abort = 1;
+            atomicOr(a.status, 0x4u);
+        }
+        // this warpgroup has read its columns: the control warp may reuse them
+        tc_fence_before_sync();
+        named_bar_sync(wg_bar, 128);
+        if (elected)
+            mbar_arrive(&B.bufree[g >> 1]);
+        if (cur.m == cur.nt - 1 || kk == count - 1) {
             if (++q_slot == QS) {
                 q_slot = 0;
                 q_phase ^= 1u;
             }
             have_q = false;
         }
+        cur.next(a);
     }
-    // after an abort, copies nobody consumed land before the CTA exits (bounded)
-    if (threadIdx.x == 0)
-        for (int u = loads > QS ? loads - QS : 0; u < loads; ++u)
-            mbar_wait(&B.qfull[u % QS], (uint32_t)(u / QS) & 1u, nullptr);
 }
 
 template <int H>
-__global__ void __launch_bounds__(kMaxThreads, 1) pmqa_prefill_kernel(const __grid_constant__ PfArgs a)
+__global__ void __launch_bounds__(kPfBoundThreads, 1) pmqa_prefill_kernel(const __grid_constant__ PfArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ CtaCtl ctl;
     uint8_t *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const PfBars B(a, smem);
 
     if (threadIdx.x == 0) {
         ctl.abort = 0;
-        const PfBars B(a, smem);
-        for (int s = 0; s < a.S; ++s) {
+        for (int s = 0; s < a.S; ++s)
             mbar_init(&B.kfull[s], 1);
-            B.done[s] = 0;
-        }
         for (int q = 0; q < a.QS; ++q)
             mbar_init(&B.qfull[q], 1);
-        for (int g = 0; g < kGroups; ++g)
-            mbar_init(&B.mma[g], 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(&B.acc[p], 1);
+            mbar_init(&B.bufree[p], 2);
+        }
         mbar_init_fence();
     }
     __syncwarp();
     if (warp == 0)
         tmem_alloc(&ctl.tmem_base, (uint32_t)(kGroups * kPassCols));
 
-    balance_schedule(a.n_sg, [&](int sg) { return (long long)pf_range(a, sg).nt; }, ctl);
+    balance_schedule(a.n_sg, [&](int sg) { return (long long)a.ranges[sg].y; }, ctl);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
 
-    // -inf outside the tiles each row's super-group covers: CTA b takes rows
-    // b, b + grid, ...; its 16 warps stride over each row's two segments.
-    {
-        const long long n = a.n;
-        for (int r = blockIdx.x; r < a.m; r += gridDim.x) {
-            const PfRange Rg = pf_range(a, r / a.SGR);
-            const long long c0 = Rg.nt > 0 ? (long long)Rg.lo * kTileTokens : n;
-            const long long c1 =
-                Rg.nt > 0 ? min((long long)(Rg.lo + Rg.nt) * kTileTokens, n) : n;
-            float *row = a.logits + (long long)r * n;
-            const float NEG_INF = -__int_as_float(0x7f800000);
-            for (long long x = threadIdx.x; x < c0; x += blockDim.x)
-                row[x] = NEG_INF;
-            for (long long x = c1 + threadIdx.x; x < n; x += blockDim.x)
-                row[x] = NEG_INF;
-        }
+    int kissued[kPfMaxStages] = {0, 0, 0, 0};
+    int qloads = 0;
+    if (warp < 4 * kGroups)
+        pf_reduce_role<H>(a, smem, ctl, warp >> 2, warp & 3);
+    else if (lane == 0)
+        pf_control<H>(a, smem, ctl, kissued, qloads);
+    __syncwarp();  // the control warp's lanes meet again before the CTA barrier
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 4 * kGroups && lane == 0) {
+        // loads still in flight after an abort land before the CTA exits (bounded)
+        for (int s = 0; s < a.S; ++s)
+            if (kissued[s] > 0)
+                mbar_wait(&B.kfull[s], (uint32_t)(kissued[s] - 1) & 1u, nullptr);
+        for (int u = qloads > a.QS ? qloads - a.QS : 0; u < qloads; ++u)
+            mbar_wait(&B.qfull[u % a.QS], (uint32_t)(u / a.QS) & 1u, nullptr);
     }
-
-    pf_group_role<H>(a, smem, ctl, warp >> 2, warp & 3);
-
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
     if (warp == 0)
         tmem_dealloc(ctl.tmem_base, (uint32_t)(kGroups * kPassCols));
 }

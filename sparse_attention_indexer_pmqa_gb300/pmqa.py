@@ -279,7 +279,7 @@ def pmqa_mqa_logits(q, k, k_scale, weights, ks, ke, *, out=None, ws=None, stream
     if out is None:
         out = torch.empty((p.m, p.n), dtype=torch.float32, device=q.device)
     if ws is None:
-        ws = workspace(0, 1, 1, 0, PMQA_OP_MQA_LOGITS, q.device, stream)
+        ws = workspace(p.m, 1, p.n, 0, PMQA_OP_MQA_LOGITS, q.device, stream)
     _check(load().pmqa_mqa_logits(ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(),
                                   _stream(stream)), "pmqa_mqa_logits")
     return out

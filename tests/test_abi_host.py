@@ -172,17 +172,21 @@ def _mqa(**kw):
 ])
 def test_mqa_problem_validation(lib, kw, code):
     p = _mqa(**kw)
-    assert lib.pmqa_mqa_logits(ctypes.byref(p), ctypes.c_void_p(0x60000), WS, 256, None) == code
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), ctypes.c_void_p(0x60000), WS, 1 << 20, None) == code
 
 
 def test_mqa_workspace_and_empty_shapes(lib):
     assert pmqa.pmqa_workspace_bytes(0, 0, 0, 0, pmqa.PMQA_OP_MQA_LOGITS) == 256
+    assert pmqa.pmqa_workspace_bytes(8, 1, 256, 0, pmqa.PMQA_OP_MQA_LOGITS) == 512
+    assert pmqa.pmqa_workspace_bytes(129, 1, 9, 0, pmqa.PMQA_OP_MQA_LOGITS) == 256 + 512
+    assert pmqa.pmqa_workspace_bytes(-1, 1, 9, 0, pmqa.PMQA_OP_MQA_LOGITS) == 0
     p = _mqa()
     out = ctypes.c_void_p(0x60000)
-    assert lib.pmqa_mqa_logits(None, out, WS, 256, None) == -1
-    assert lib.pmqa_mqa_logits(ctypes.byref(p), None, WS, 256, None) == -1
-    assert lib.pmqa_mqa_logits(ctypes.byref(p), out, WS, 255, None) == pmqa.PMQA_ERR_WORKSPACE
-    assert lib.pmqa_mqa_logits(ctypes.byref(p), out, ctypes.c_void_p(0x100010), 256, None) == -1
+    need = pmqa.pmqa_workspace_bytes(8, 1, 256, 0, pmqa.PMQA_OP_MQA_LOGITS)
+    assert lib.pmqa_mqa_logits(None, out, WS, need, None) == -1
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), None, WS, need, None) == -1
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), out, WS, need - 1, None) == pmqa.PMQA_ERR_WORKSPACE
+    assert lib.pmqa_mqa_logits(ctypes.byref(p), out, ctypes.c_void_p(0x100010), need, None) == -1
     # nothing to compute: no pointer is needed and nothing is launched
     assert lib.pmqa_mqa_logits(ctypes.byref(_mqa(m=0, q=None)), None, WS, 256, None) == 0
-    assert lib.pmqa_mqa_logits(ctypes.byref(_mqa(n=0, k=None)), None, WS, 256, None) == 0
+    assert lib.pmqa_mqa_logits(ctypes.byref(_mqa(n=0, k=None)), None, WS, need, None) == 0

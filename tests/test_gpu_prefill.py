@@ -58,7 +58,7 @@ def test_prefill_small(cuda_lib, case):
     m, n, H, ranges = case
     p = make_prefill(m, n, H, ranges=ranges, seed=m * 7 + n + H)
     ref, _, tol = oracle.mqa_logits(p, want_tol=True)
-    ws = cuda_lib.workspace(0, 1, 1, 0, cuda_lib.PMQA_OP_MQA_LOGITS)
+    ws = cuda_lib.workspace(p.m, 1, p.n, 0, cuda_lib.PMQA_OP_MQA_LOGITS)
     check_logits(gpu_mqa(cuda_lib, p, ws=ws), ref, tol)
     assert cuda_lib.pmqa_read_device_status(ws) == 0
 
@@ -117,7 +117,7 @@ def _rows_problem(p, rows):
 def test_prefill_full_size_sampled_rows(cuda_lib):
     p = prefill_config("PF1")
     d = dev(p)
-    ws = cuda_lib.workspace(0, 1, 1, 0, cuda_lib.PMQA_OP_MQA_LOGITS)
+    ws = cuda_lib.workspace(p.m, 1, p.n, 0, cuda_lib.PMQA_OP_MQA_LOGITS)
     got = gpu_mqa(cuda_lib, p, d=d, ws=ws)
     assert cuda_lib.pmqa_read_device_status(ws) == 0
     rng = np.random.default_rng(0)
