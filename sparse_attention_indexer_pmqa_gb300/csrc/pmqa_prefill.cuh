@@ -312,13 +312,24 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
     uint32_t q_phase = 0;
     bool have_q = false;
     int r0 = 0, nr = 0;  // first row of this warpgroup in the super-group, rows that exist
+    int rks[G], rke[G];  // their key ranges
+    // key scales are loaded one item ahead
+    int t = count > 0 ? cur.tile() * kTileTokens + (int)R : 0;
+    float sc = count > 0 && t < n ? __ldg(a.k_scale + t) : 0.0f;
     for (int kk = 0; kk < count; ++kk) {
-        const int t = cur.tile() * kTileTokens + (int)R;
-        const float sc = t < n ? __ldg(a.k_scale + t) : 0.0f;
+        PfPos nx = cur;
+        nx.next(a);
+        const int t_next = kk + 1 < count ? nx.tile() * kTileTokens + (int)R : 0;
+        const float sc_next = kk + 1 < count && t_next < n ? __ldg(a.k_scale + t_next) : 0.0f;
         bool ok = true;
         if (!have_q) {
             r0 = cur.sg * SGR + g * G;
             nr = max(0, min(G, m - r0));
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                rks[j] = j < nr ? __ldg(a.ks + r0 + j) : 0;
+                rke[j] = j < nr ? __ldg(a.ke + r0 + j) : 0;
+            }
             ok = mbar_wait(&B.qfull[q_slot], q_phase, &c.abort);
             have_q = true;
         }
@@ -334,10 +345,8 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
             const bool all_pos = __all_sync(kFullMask, flip == 0u);
             float *const orow = logits + (long long)r0 * n + t;
             auto out = [&](int j, float v) {
-                if (t < n) {
-                    const bool in = t >= __ldg(a.ks + r0 + j) && t < __ldg(a.ke + r0 + j);
-                    orow[(long long)j * n] = in ? v : NEG_INF;
-                }
+                if (t < n)
+                    orow[(long long)j * n] = (t >= rks[j] && t < rke[j]) ? v : NEG_INF;
             };
             if (nr > 0)
                 epi_dispatch<H, G>(nr, all_pos, tacc, wsl, flip, mag, 0, out);
@@ -345,7 +354,8 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
             c.abort = 1;
             atomicOr(a.status, 0x4u);
         }
-        // this warpgroup has read its columns: the control warp may reuse them
+        // this warpgroup has read its columns: once both warpgroups of the
+        // pair have, the control warp may reuse them
         tc_fence_before_sync();
         named_bar_sync(wg_bar, 128);
         if (elected)
@@ -357,7 +367,9 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
             }
             have_q = false;
         }
-        cur.next(a);
+        cur = nx;
+        t = t_next;
+        sc = sc_next;
     }
 }
 
