@@ -1,6 +1,7 @@
 /*
  * pmqa.h -- C ABI of libpmqa: the FP8 paged MQA-logits indexer and its per-row
- * top-k, as hand-written CUDA kernels for sm_103a (GB300).
+ * top-k, and the non-paged (prefill) MQA logits, as hand-written CUDA kernels
+ * for sm_103a (GB300).
  *
  * What is computed. Sources: the page "[Bug] aiter ops triton attention pa"
  * (stepcodex.com issue mirror), section "Minimal reproduction" (the reference
