@@ -429,8 +429,9 @@ def bench_prefill(name, args, device):
         "pairs": pairs, "pairs_per_s": pairs / (ms * 1e-3),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "peak_source": peak_kind,
+                     "traffic": measured_traffic(name),
                      "algorithmic_flops_per_launch": flops,
-                     "kernel": f"pmqa_prefill_kernel<{p.heads}>"},
+                     "kernel": f"pmqa_prefill_kernel<{p.heads}> (with its prep launch)"},
         "out_gbs": p.m * p.n * 4 / (ms * 1e-3) / 1e9,
         "launches": 1,
     }
