@@ -433,7 +433,7 @@ def bench_prefill(name, args, device):
                      "algorithmic_flops_per_launch": flops,
                      "kernel": f"pmqa_prefill_kernel<{p.heads}> (with its prep launch)"},
         "out_gbs": p.m * p.n * 4 / (ms * 1e-3) / 1e9,
-        "launches": 1,
+        "launches": 2,
     }
 
 
