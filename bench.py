@@ -19,6 +19,7 @@ replicas: every rank owns a full copy of the batch, no data-path collective.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import csv
 import hashlib
 import io
@@ -385,6 +386,25 @@ def bench_workload(name, args, device, dist, with_e2e: bool, with_paths: bool):
     return out
 
 
+def prefill_cpu_baseline(p, rows: int = 1024):
+    """The prefill oracle, as it stands, on a bounded sample: `rows` query rows
+    spread evenly over the workload (rows are independent)."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    sel = np.linspace(0, p.m - 1, rows).astype(np.int64)
+    sub = dataclasses.replace(p, q=p.q[sel], weights=p.weights[sel], ks=p.ks[sel], ke=p.ke[sel])
+    nthreads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.mqa_logits(sub, nthreads=nthreads)
+    sec = time.perf_counter() - t0
+    return {"value": sub.pairs / sec, "unit": "pairs/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{rows} of {p.m} query rows of {p.name}, evenly spaced ({sub.pairs} pairs), "
+                      f"{sec:.2f} s"}
+
+
 def bench_prefill(name, args, device):
     """Prefill logits (pmqa_mqa_logits) on one prefill workload: every step
     writes the whole [m, n] logits matrix; L2 flushed before each step."""
@@ -546,6 +566,10 @@ def run_ours(args):
         line["workloads"] = per
     if args.all or args.prefill:
         line["prefill"] = bench_prefill("PF1", args, device)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            from synth import prefill_config
+
+            line["prefill"]["cpu_baseline"] = prefill_cpu_baseline(prefill_config("PF1"))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob)
     if rank == 0:
