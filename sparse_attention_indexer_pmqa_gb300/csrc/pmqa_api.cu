@@ -21,6 +21,7 @@ cudaError_t launch_prefill_h16(const PfArgs &, int, int, cudaStream_t);
 cudaError_t launch_prefill_h32(const PfArgs &, int, int, cudaStream_t);
 cudaError_t launch_prefill_h64(const PfArgs &, int, int, cudaStream_t);
 cudaError_t launch_prefill_h128(const PfArgs &, int, int, cudaStream_t);
+cudaError_t launch_prefill_prep(const PfArgs &, int, cudaStream_t);
 size_t fused_ws_zero_bytes(int bs, int next_n);
 }  // namespace pmqa
 
@@ -299,11 +300,10 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
 
 // Shared-memory layout of the prefill kernel: a ring of S key stages, two query
 // slots of 4 * G query rows (512 Q rows of 128 bytes) and their weights, the
-// pair-exchange buffer, the mbarriers and the counters.
+// mbarriers.
 bool pf_layout(int heads, PfArgs &a)
 {
-    a.G = kPassCols / heads;
-    a.SGR = kGroups * a.G;
+    a.SGR = kGroups * (kPassCols / heads);
     const uint32_t N = (uint32_t)(a.SGR * heads);
     const int QS = 2;  // the next super-group's MMAs start before the current one's slot is freed
     for (int S = kPfMaxStages; S >= 2; --S) {
@@ -315,8 +315,6 @@ bool pf_layout(int heads, PfArgs &a)
         a.off_w = off;
         off += (uint32_t)QS * N * 4u;
         off = (uint32_t)align_up(off, 16);
-        a.off_x = off;  // partial sums exchanged by warpgroup pairs (128 heads)
-        off += 2u * 2u * 128u * 4u;
         a.off_bar = off;
         off += (uint32_t)(S + QS + 4) * 8u;
         const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
@@ -375,8 +373,7 @@ int run_prefill(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_by
     int sms = 0, rc;
     if ((rc = sm_count(&sms)) != PMQA_OK)
         return rc;
-    pmqa_prefill_prep_kernel<<<std::min(a.n_sg, 8 * sms), 256, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess)
+    if (launch_prefill_prep(a, std::min(a.n_sg, 8 * sms), stream) != cudaSuccess)
         return PMQA_ERR_CUDA;
     cudaError_t e;
     switch (p->heads) {

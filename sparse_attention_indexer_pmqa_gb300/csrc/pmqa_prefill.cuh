@@ -7,18 +7,20 @@
 // logit = sum_h w[r][h] * relu(s_n * q[r][h] . k_n) for ks[r] <= n < ke[r],
 // -inf elsewhere.
 //
-// A CTA works on super-groups of SGR = 4 G query rows (G = 128 / heads) and
-// walks a contiguous, tile-balanced range of (super-group, 128-key tile)
-// items. Warp 16 is the control warp: its lane 0 loads every key tile (TMA,
-// already in the 128B-swizzled K-major operand layout, a ring of S stages),
-// every query slot, and issues every MMA. Warps 0-15 are four warpgroups;
-// warpgroup g owns TMEM columns [128 g, 128 g + 128), the accumulators
-// D[key][(row, h)] = K_tile * Q^T of its G rows (one N = 128 MMA per item),
-// and reduces them (thread = key = TMEM lane): sum_h w[row][h] * relu(s_key *
-// x), masked to the row's key range. The warpgroups run independently of one
-// another, each handing its columns back to the control warp through an
-// mbarrier, so one warpgroup's reduction overlaps the others' MMAs and TMEM
-// reads. Every wait is bounded.
+// Two launches. The prep kernel reduces each super-group's rows (SGR = 4 G
+// query rows, G = 128 / heads) to the range of 128-key tiles their key ranges
+// touch, and writes -inf outside it. The main kernel, one CTA per SM, walks a
+// contiguous, tile-balanced range of (super-group, key tile) items. Warp 16 is
+// the control warp: its lane 0 loads every key tile (TMA, already in the
+// 128B-swizzled K-major operand layout, a ring of S stages) and every query
+// slot, and issues every MMA: per item, one N = 256 MMA per warpgroup pair p,
+// D[key][(row, h)] = K_tile * Q^T for the 2 G rows of warpgroups 2p and 2p + 1,
+// into TMEM columns [256 p, 256 p + 256). Warps 0-15 are four warpgroups;
+// warpgroup g reduces columns [128 g, 128 g + 128), its G rows (thread = key =
+// TMEM lane): sum_h w[row][h] * relu(s_key * x), masked to the row's key
+// range. The pairs run independently of each other, each handing its columns
+// back to the control warp through an mbarrier, so one pair's reduction
+// overlaps the other pair's MMA. Every wait is bounded.
 #pragma once
 
 #include "pmqa_main.cuh"
@@ -37,11 +39,10 @@ struct PfArgs {
     uint32_t *status;
     int2 *ranges;   // per super-group: first key tile, tile count (written by the prep kernel)
     int m, n;
-    int G;     // query rows per warpgroup (128 / heads)
-    int SGR;   // query rows per super-group (4 * G)
+    int SGR;   // query rows per super-group: 4 warpgroups x 128 / heads
     int n_sg;  // super-groups: ceil(m / SGR)
     int S, QS, q_box;
-    uint32_t off_k, off_q, off_w, off_x, off_bar, smem_bytes;
+    uint32_t off_k, off_q, off_w, off_bar, smem_bytes;
 };
 
 // ---------------------------------------------------------------- prep kernel
@@ -49,7 +50,8 @@ struct PfArgs {
 // One CTA per super-group (grid-strided): the tile range [lo, lo + nt) that
 // covers the union of its rows' key ranges, and -inf in every entry of its
 // rows outside those tiles (the main kernel writes the entries inside).
-static __global__ void __launch_bounds__(256) pmqa_prefill_prep_kernel(const __grid_constant__ PfArgs a)
+#ifdef PMQA_PREFILL_PREP
+__global__ void __launch_bounds__(256) pmqa_prefill_prep_kernel(const __grid_constant__ PfArgs a)
 {
     __shared__ int2 rng;
     const int tid = threadIdx.x, lane = tid & 31;
@@ -96,6 +98,7 @@ static __global__ void __launch_bounds__(256) pmqa_prefill_prep_kernel(const __g
         __syncthreads();  // rng is rewritten for the next super-group
     }
 }
+#endif  // PMQA_PREFILL_PREP
 
 // ---------------------------------------------------------------- main kernel
 

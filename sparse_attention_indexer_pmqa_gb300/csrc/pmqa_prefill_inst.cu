@@ -1,7 +1,11 @@
 // pmqa_prefill_inst.cu -- the prefill kernel for one head count per
-// translation unit (-DPMQA_HEADS=16, 32, 64 or 128), compiled in parallel.
+// translation unit (-DPMQA_HEADS=16, 32, 64 or 128), compiled in parallel;
+// the head-count-independent prep kernel lives in the 16-head unit.
 #include <cuda_runtime.h>
 
+#if PMQA_HEADS == 16
+#define PMQA_PREFILL_PREP
+#endif
 #include "pmqa_prefill.cuh"
 
 #ifndef PMQA_HEADS
@@ -24,5 +28,13 @@ cudaError_t PMQA_CAT(launch_prefill_h, PMQA_HEADS)(const PfArgs &a, int grid, in
     pmqa_prefill_kernel<PMQA_HEADS><<<grid, threads, a.smem_bytes, stream>>>(a);
     return cudaGetLastError();
 }
+
+#ifdef PMQA_PREFILL_PREP
+cudaError_t launch_prefill_prep(const PfArgs &a, int grid, cudaStream_t stream)
+{
+    pmqa_prefill_prep_kernel<<<grid, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+#endif
 
 }  // namespace pmqa
