@@ -291,8 +291,9 @@ __device__ __forceinline__ void load_query(const MainArgs &a, uint8_t *smem, con
 // acc += sum over NC consecutive columns of w[h] * relu(x[h]) (SIGNED: of
 // relu(-x[h]) when the thread's scale is negative, flip = its sign bit).
 // Packed fp32x2 multiply-adds into four accumulator pairs; the weights come as
-// float4 broadcasts from shared memory.
-template <int NC, bool SIGNED>
+// float4 broadcasts from shared memory. FIRST: the chunk starts a row, and its
+// first products initialise the accumulators instead of adding to them.
+template <int NC, bool SIGNED, bool FIRST = false>
 __device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[NC], uint32_t w, uint32_t flip,
                                                float (&acc)[8])
 {
@@ -304,18 +305,24 @@ __device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[NC], uint32_t
         for (int u = 0; u < 4; ++u)
             v[u] = fmaxf(__uint_as_float(SIGNED ? (x[h + u] ^ flip) : x[h + u]), 0.f);
         float *p = acc + ((h / 4) & 1) * 4;
-        ffma2(p[0], p[1], wv.x, wv.y, v[0], v[1]);
-        ffma2(p[2], p[3], wv.z, wv.w, v[2], v[3]);
+        if (FIRST && h < 8) {
+            fmul2(p[0], p[1], wv.x, wv.y, v[0], v[1]);
+            fmul2(p[2], p[3], wv.z, wv.w, v[2], v[3]);
+        } else {
+            ffma2(p[0], p[1], wv.x, wv.y, v[0], v[1]);
+            ffma2(p[2], p[3], wv.z, wv.w, v[2], v[3]);
+        }
     }
 }
 
+// The row's sum of the eight accumulators (packed adds); the next row's first
+// chunk re-initialises them.
 __device__ __forceinline__ float acc_sum(float (&acc)[8])
 {
-    const float s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-        acc[u] = 0.f;
-    return s;
+    fadd2(acc[0], acc[1], acc[2], acc[3]);
+    fadd2(acc[4], acc[5], acc[6], acc[7]);
+    fadd2(acc[0], acc[1], acc[4], acc[5]);
+    return acc[0] + acc[1];
 }
 
 // Draft rows j0 .. j0 + NR - 1 for this thread's token (TMEM lane): row j's
@@ -333,7 +340,7 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t 
     constexpr int CPR = H / NC;  // chunks per draft row
     constexpr int TOTAL = NR * CPR;
     uint32_t b[2][NC];
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc[8];
     float res[NR];
     tmem_ld_cols<NC>(taddr, b[0]);
     tmem_ld_wait();
@@ -342,7 +349,10 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t 
     for (int ch = 0; ch < TOTAL; ++ch) {
         if (ch + 1 < TOTAL)
             tmem_ld_cols<NC>(taddr + (uint32_t)((ch + 1) * NC), b[(ch + 1) & 1]);
-        epi_accumulate<NC, SIGNED>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), flip, acc);
+        if (ch % CPR == 0)
+            epi_accumulate<NC, SIGNED, true>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), flip, acc);
+        else
+            epi_accumulate<NC, SIGNED>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), flip, acc);
         if ((ch + 1) % CPR == 0)
             res[ch / CPR] = acc_sum(acc) * mag;
         if (ch + 1 < TOTAL) {

@@ -188,8 +188,7 @@ constexpr int kPfBoundThreads = 640;
 // warpgroups 2 p and 2 p + 1 against the key tile) once both have read their
 // columns of item k - 1.
 template <int H>
-static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int (&kissued)[kPfMaxStages],
-                                  int &qloads)
+static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int &kloads, int &qloads)
 {
     const PfBars B(a, smem);
     const int count = (int)c.count;
@@ -221,7 +220,7 @@ static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int
     kp.at(a, c.i0, c.m0);
     for (int s = 0; s < S && s < count; ++s) {
         pf_load_k(a, kbase, B, s, kp.tile());
-        ++kissued[s];
+        ++kloads;
         kp.next(a);
     }
 
@@ -265,7 +264,7 @@ static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int
             // super-group, that super-group's query slot takes the one QS ahead
             if (k - 1 + S < count) {
                 pf_load_k(a, kbase, B, (k - 1) % S, kp.tile());
-                ++kissued[(k - 1) % S];
+                ++kloads;
                 kp.next(a);
             }
             if (prev_last) {
@@ -406,12 +405,11 @@ __global__ void __launch_bounds__(kPfBoundThreads, 1) pmqa_prefill_kernel(const 
     __syncthreads();
     tc_fence_after_sync();
 
-    int kissued[kPfMaxStages] = {0, 0, 0, 0};
-    int qloads = 0;
+    int kloads = 0, qloads = 0;  // loads issued by the control warp (item i into stage i % S)
     if (warp < 4 * kGroups)
         pf_reduce_role<H>(a, smem, ctl, warp >> 2, warp & 3);
     else if (lane == 0)
-        pf_control<H>(a, smem, ctl, kissued, qloads);
+        pf_control<H>(a, smem, ctl, kloads, qloads);
     __syncwarp();  // the control warp's lanes meet again before the CTA barrier
 
     tc_fence_before_sync();
@@ -419,9 +417,10 @@ __global__ void __launch_bounds__(kPfBoundThreads, 1) pmqa_prefill_kernel(const 
     tc_fence_after_sync();
     if (warp == 4 * kGroups && lane == 0) {
         // loads still in flight after an abort land before the CTA exits (bounded)
-        for (int s = 0; s < a.S; ++s)
-            if (kissued[s] > 0)
-                mbar_wait(&B.kfull[s], (uint32_t)(kissued[s] - 1) & 1u, nullptr);
+        for (int s = 0; s < a.S && s < kloads; ++s) {
+            const int uses = (kloads - s + a.S - 1) / a.S;  // loads into stage s
+            mbar_wait(&B.kfull[s], (uint32_t)(uses - 1) & 1u, nullptr);
+        }
         for (int u = qloads > a.QS ? qloads - a.QS : 0; u < qloads; ++u)
             mbar_wait(&B.qfull[u % a.QS], (uint32_t)(u / a.QS) & 1u, nullptr);
     }

@@ -216,6 +216,30 @@ __device__ __forceinline__ void ffma2(float &a0, float &a1, float w0, float w1, 
         : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
 }
 
+// (a0, a1) = (w0, w1) * (x0, x1): one packed fp32x2 multiply.
+__device__ __forceinline__ void fmul2(float &a0, float &a1, float w0, float w1, float x0, float x1)
+{
+    asm("{\n\t.reg .b64 ra, rw, rx;\n\t"
+        "mov.b64 rw, {%2, %3};\n\t"
+        "mov.b64 rx, {%4, %5};\n\t"
+        "mul.rn.f32x2 ra, rw, rx;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(a0), "=f"(a1)
+        : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
+// (a0, a1) += (b0, b1): one packed fp32x2 add.
+__device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rb, {%2, %3};\n\t"
+        "add.rn.f32x2 ra, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 // ---------------------------------------------------------------- TMA
 
 // Expect `bytes` more transaction bytes on the barrier and arrive once.
