@@ -205,7 +205,20 @@ int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
     const dim3 grid((unsigned)s.splits, (unsigned)rows);
     if (with_hist_pass)
         pmqa_hist_kernel<<<grid, kSelThreads, 0, stream>>>(s);
-    pmqa_select_kernel<<<grid, kSelThreads, 0, stream>>>(s);
+    // a programmatic dependent of the preceding kernel (the KV pass on the
+    // fused path): its launch overlaps that kernel's end
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, pmqa_select_kernel, s) != cudaSuccess)
+        return PMQA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }
 

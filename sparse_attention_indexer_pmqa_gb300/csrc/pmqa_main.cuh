@@ -742,6 +742,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     uint8_t *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // the selection launched after this kernel may start launching now; it
+    // waits for this grid's completion before it reads anything
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         ctl.abort = 0;
         const Bars B(a, smem);

@@ -240,6 +240,20 @@ __device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1)
         : "f"(b0), "f"(b1));
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start
+// launching (its CTAs still wait in griddep_wait until this grid is done).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until every grid this one depends on has completed and its memory
+// operations are visible; returns at once when launched without a dependency.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 // Expect `bytes` more transaction bytes on the barrier and arrive once.

@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
 {
     __shared__ SelShared s;
     const int row = blockIdx.y, tid = threadIdx.x;
+    // launched as a dependent of the KV pass: its logits and histograms are
+    // complete and visible after this
+    griddep_wait();
     const int n = sel_valid_len(a, row);
     const uint32_t keff = (uint32_t)min(a.k, n);
     const float NEG_INF = -__int_as_float(0x7f800000);
