@@ -190,7 +190,8 @@ int pmqa_logits_topk_noalloc(const pmqa_problem *p, int32_t k, int32_t *idx, flo
  *   weights  fp32 [m, heads], contiguous, 16-byte aligned
  *   ks, ke   int32 [m]: row r's key range [ks[r], ke[r]); values outside [0, n]
  *            are clamped, ks >= ke gives an all -inf row
- * head_dim must be 128 and heads one of 16, 32, 64, 128; m * heads < 2^31.
+ * head_dim must be 128 and heads one of 16, 32, 64, 128; m * heads < 2^31 and
+ * n <= 2^31 - 129 (PMQA_ERR_UNSUPPORTED otherwise).
  */
 typedef struct pmqa_mqa_problem {
     const void *q;

@@ -352,7 +352,8 @@ int run_prefill(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_by
         return PMQA_ERR_INVALID_ARG;
     if (p->head_dim != kHeadDim || !supported_heads(p->heads))
         return PMQA_ERR_UNSUPPORTED;
-    if ((long long)p->m * p->heads >= (1ll << 31))
+    // query rows address the q tensor map as int; key positions (tile * 128 + lane) as int
+    if ((long long)p->m * p->heads >= (1ll << 31) || (long long)p->n > (1ll << 31) - 1 - kTileTokens)
         return PMQA_ERR_UNSUPPORTED;
     if (!ws || !aligned(ws, kWsAlign))
         return PMQA_ERR_INVALID_ARG;

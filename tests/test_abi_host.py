@@ -160,6 +160,7 @@ def _mqa(**kw):
     (dict(head_dim=64), pmqa.PMQA_ERR_UNSUPPORTED),
     (dict(heads=48), pmqa.PMQA_ERR_UNSUPPORTED),
     (dict(m=1 << 27, heads=16), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(n=(1 << 31) - 100), pmqa.PMQA_ERR_UNSUPPORTED),
     (dict(m=-1), pmqa.PMQA_ERR_INVALID_ARG),
     (dict(n=-1), pmqa.PMQA_ERR_INVALID_ARG),
     (dict(heads=0), pmqa.PMQA_ERR_INVALID_ARG),
