@@ -208,17 +208,30 @@ int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
     // a programmatic dependent of the preceding kernel (the KV pass on the
     // fused path): its launch overlaps that kernel's end
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kSelThreads);
-    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, pmqa_select_kernel, s) != cudaSuccess)
-        return PMQA_ERR_CUDA;
+    if (s.mml <= kRowMaxLen) {
+        // rows short enough for one CTA each, the logits held in shared memory
+        const int smem = s.mml * (int)sizeof(float);
+        if (cudaFuncSetAttribute(pmqa_select_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kRowMaxLen * (int)sizeof(float)) != cudaSuccess)
+            return PMQA_ERR_CUDA;
+        cfg.gridDim = dim3((unsigned)rows);
+        cfg.blockDim = dim3(kRowThreads);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        if (cudaLaunchKernelEx(&cfg, pmqa_select_row_kernel, s) != cudaSuccess)
+            return PMQA_ERR_CUDA;
+    } else {
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kSelThreads);
+        cfg.dynamicSmemBytes = 0;
+        if (cudaLaunchKernelEx(&cfg, pmqa_select_kernel, s) != cudaSuccess)
+            return PMQA_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }
 

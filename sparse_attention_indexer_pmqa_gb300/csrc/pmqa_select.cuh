@@ -389,4 +389,276 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     }
 }
 
+// ---------------------------------------------------------------- one CTA per row
+
+// Rows of at most kRowMaxLen positions are selected by one CTA of kRowThreads
+// threads that holds the row's logits in shared memory: the same radix select
+// (first digit from the row's histogram, one classifying pass, the boundary
+// bin resolved with two more digits), with every count, offset and candidate
+// list in shared memory, so no global atomics, arrival counters or second
+// CTA are involved.
+constexpr int kRowThreads = 1024;
+constexpr int kRowMaxLen = 32768;  // 128 KB of logits in dynamic shared memory
+static_assert(kRowMaxLen <= 32 * kRowThreads, "one 32-bit mask per thread covers its positions");
+
+struct RowShared {
+    uint32_t h[kHistBins];
+    uint32_t wsum[kRowThreads / 32];
+    uint32_t digit, above2, bstar, above, eq_taken, cursor;
+    uint64_t loaded;  // mbarrier of the row's bulk copy
+    int32_t tpos[kTieCap];
+    uint32_t tkey[kTieCap];
+};
+
+// find_bin for kRowThreads threads (1 or 2 bins each).
+__device__ void row_find_bin(RowShared &s, const uint32_t *h, int nbins, uint32_t need)
+{
+    const int per = nbins / kRowThreads;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int hi = nbins - 1 - tid * per;
+    if (tid == 0) {
+        s.digit = 0;
+        s.above2 = 0;
+    }
+    uint32_t loc = 0;
+    for (int q = 0; q < per; ++q)
+        loc += h[hi - q];
+    uint32_t incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        s.wsum[wid] = incl;
+    __syncthreads();
+    uint32_t woff = 0;
+    for (int w = 0; w < wid; ++w)
+        woff += s.wsum[w];
+    incl += woff;
+    const uint32_t excl = incl - loc;
+    if (excl < need && need <= incl) {
+        uint32_t acc = excl;
+        for (int q = 0; q < per; ++q) {
+            const uint32_t v = h[hi - q];
+            if (acc + v >= need) {
+                s.digit = (uint32_t)(hi - q);
+                s.above2 = acc;
+                break;
+            }
+            acc += v;
+        }
+    }
+    __syncthreads();
+}
+
+// Exclusive prefix of a per-thread count over the CTA; the total in *total.
+__device__ uint32_t row_exclusive_scan(RowShared &s, uint32_t x, uint32_t *total)
+{
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    __syncthreads();
+    if (lane == 31)
+        s.wsum[wid] = incl;
+    __syncthreads();
+    // warp 0 turns the 32 warp sums into exclusive offsets (and the total)
+    if (wid == 0) {
+        const uint32_t w = s.wsum[lane];
+        uint32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(kFullMask, wi, o);
+            if (lane >= o)
+                wi += v;
+        }
+        s.wsum[lane] = wi - w;
+        if (lane == 31)
+            s.cursor = wi;
+    }
+    __syncthreads();
+    *total = s.cursor;
+    return s.wsum[wid] + incl - x;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const __grid_constant__ SelectArgs a)
+{
+    extern __shared__ __align__(16) float sv[];  // the row's logits, positions 0 .. n - 1
+    __shared__ RowShared s;
+    const int row = blockIdx.x, tid = threadIdx.x;
+    // launched as a dependent of the KV pass: its logits and histograms are
+    // complete and visible after this
+    griddep_wait();
+    const int n = min(sel_valid_len(a, row), kRowMaxLen);
+    const uint32_t keff = (uint32_t)min(a.k, n);
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const long long rbase = (long long)row * a.mml;
+    int32_t *orow = a.idx + (long long)row * a.k;
+    float *vrow = a.vals ? a.vals + (long long)row * a.k : nullptr;
+    uint32_t *const status = a.status;
+
+    // the row by bulk copy when it is 16-byte aligned (every row is when the
+    // logits are and max_model_len is a multiple of 4), else by plain loads
+    const float *src = a.logits + rbase;
+    const bool bulk = keff > 0 && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && (a.mml % 4 == 0);
+    if (bulk && tid == 0) {
+        mbar_init(&s.loaded, 1);
+        mbar_init_fence();
+        const uint32_t bytes = (uint32_t)((n + 3) & ~3) * 4u;  // inside the row: mml % 4 == 0
+        mbar_arrive_expect_tx(&s.loaded, bytes);
+        for (uint32_t off = 0; off < bytes; off += 32768u)
+            bulk_load(smem_u32(sv) + off, reinterpret_cast<const uint8_t *>(src) + off,
+                      min(32768u, bytes - off), &s.loaded);
+    }
+    if (keff > 0) {
+        for (int e = tid; e < kHistBins; e += kRowThreads)
+            s.h[e] = __ldcg(a.hist + (long long)row * kHistBins + e);
+        __syncthreads();  // the mbarrier is initialised
+        if (bulk && !mbar_wait(&s.loaded, 0, nullptr))
+            atomicOr(status, 0x4u);
+        // the row into shared memory, 16 independent loads in flight per thread
+        constexpr int kBatch = 16;
+        for (int base = 0; !bulk && base < n; base += kRowThreads * kBatch) {
+            float v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int t = base + u * kRowThreads + tid;
+                v[u] = t < n ? __ldcg(a.logits + rbase + t) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int t = base + u * kRowThreads + tid;
+                if (t < n)
+                    sv[t] = v[u];
+            }
+        }
+        __syncthreads();
+        row_find_bin(s, s.h, kHistBins, keff);
+        const uint32_t bstar = s.digit, above = s.above2;
+        // winners (key bin above b*) and candidates (bin b*) of this thread:
+        // bit u stands for position tid + u * kRowThreads (n <= 32 * kRowThreads)
+        uint32_t msel = 0, mtie = 0;
+#pragma unroll 8
+        for (int u = 0; u < kRowMaxLen / kRowThreads; ++u) {
+            const int t = tid + u * kRowThreads;
+            if (t < n) {
+                const uint32_t bin = f32_order_key(sv[t]) >> kHistShift;
+                msel |= (bin > bstar ? 1u : 0u) << u;
+                mtie |= (bin == bstar ? 1u : 0u) << u;
+            }
+        }
+        const uint32_t cs = (uint32_t)__popc(msel), ct = (uint32_t)__popc(mtie);
+        uint32_t tot_s, tot_t;
+        uint32_t o_s = row_exclusive_scan(s, cs, &tot_s);
+        uint32_t o_t = row_exclusive_scan(s, ct, &tot_t);
+        if (tid == 0 && tot_s != above)
+            atomicOr(status, 0x8u);
+        // candidates stay in shared memory when they fit, else go to the
+        // row's list in the workspace
+        const bool cached = tot_t <= (uint32_t)kTieCap;
+        uint2 *const tl = a.ties + rbase;
+        for (uint32_t m = msel; m; m &= m - 1) {
+            const int t = tid + (__ffs(m) - 1) * kRowThreads;
+            if (o_s < keff) {
+                orow[o_s] = t;
+                if (vrow)
+                    vrow[o_s] = sv[t];
+            } else {
+                atomicOr(status, 0x8u);
+            }
+            ++o_s;
+        }
+        for (uint32_t m = mtie; m; m &= m - 1) {
+            const int t = tid + (__ffs(m) - 1) * kRowThreads;
+            const uint32_t key = f32_order_key(sv[t]);
+            if (cached) {
+                s.tpos[o_t] = t;
+                s.tkey[o_t] = key;
+            } else {
+                tl[o_t] = make_uint2((uint32_t)t, key);
+            }
+            ++o_t;
+        }
+        if (!cached)
+            __threadfence_block();
+        __syncthreads();
+        const uint32_t need = keff > above ? keff - above : 0u;
+        const uint32_t ntie = tot_t;
+        auto key_of = [&](uint32_t e) -> uint32_t { return cached ? s.tkey[e] : __ldcg(tl + e).y; };
+        auto pos_of = [&](uint32_t e) -> int32_t { return cached ? s.tpos[e] : (int32_t)__ldcg(tl + e).x; };
+        if (need >= ntie) {
+            // every candidate is selected
+            for (uint32_t e = tid; e < ntie && above + e < keff; e += kRowThreads) {
+                orow[above + e] = pos_of(e);
+                if (vrow)
+                    vrow[above + e] = f32_from_order_key(key_of(e));
+            }
+            if (need > ntie && tid == 0)
+                atomicOr(status, 0x8u);
+        } else if (need > 0) {
+            // second digit: key bits 20..10 of the candidates
+            for (int e = tid; e < kHistBins; e += kRowThreads)
+                s.h[e] = 0;
+            __syncthreads();
+            for (uint32_t e = tid; e < ntie; e += kRowThreads)
+                atomicAdd(&s.h[(key_of(e) >> 10) & 2047u], 1u);
+            __syncthreads();
+            row_find_bin(s, s.h, kHistBins, need);
+            const uint32_t d2 = s.digit, above2 = s.above2;
+            const uint32_t need2 = need - above2;
+            __syncthreads();
+            // third digit: key bits 9..0 of the candidates in sub-bin d2
+            for (int e = tid; e < 1024; e += kRowThreads)
+                s.h[e] = 0;
+            __syncthreads();
+            for (uint32_t e = tid; e < ntie; e += kRowThreads) {
+                const uint32_t key = key_of(e);
+                if (((key >> 10) & 2047u) == d2)
+                    atomicAdd(&s.h[key & 1023u], 1u);
+            }
+            __syncthreads();
+            row_find_bin(s, s.h, 1024, need2);
+            const uint32_t d3 = s.digit, above3 = s.above2;
+            const uint32_t T = (bstar << kHistShift) | (d2 << 10) | d3;  // the k-th largest key
+            const uint32_t eq_need = need2 - above3;
+            if (tid == 0) {
+                s.eq_taken = 0;
+                s.cursor = 0;
+            }
+            __syncthreads();
+            for (uint32_t e = tid; e < ntie; e += kRowThreads) {
+                const uint32_t key = key_of(e);
+                bool take = key > T;
+                if (key == T)
+                    take = atomicAdd(&s.eq_taken, 1u) < eq_need;
+                if (take) {
+                    const uint32_t o = above + atomicAdd(&s.cursor, 1u);
+                    if (o < keff) {
+                        orow[o] = pos_of(e);
+                        if (vrow)
+                            vrow[o] = f32_from_order_key(key);
+                    } else {
+                        atomicOr(status, 0x8u);
+                    }
+                }
+            }
+        }
+    }
+    for (int e = (int)keff + tid; e < a.k; e += kRowThreads) {
+        orow[e] = -1;
+        if (vrow)
+            vrow[e] = NEG_INF;
+    }
+    // the row's histogram returns to zero for the next call (every read of it
+    // happened before the first row_find_bin's barriers)
+    for (int e = tid; e < kHistBins; e += kRowThreads)
+        a.hist[(long long)row * kHistBins + e] = 0;
+}
+
 }  // namespace pmqa
