@@ -217,13 +217,21 @@ int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
     if (s.mml <= kRowMaxLen) {
         // rows short enough for one CTA each, the logits held in shared memory
         const int smem = s.mml * (int)sizeof(float);
-        if (cudaFuncSetAttribute(pmqa_select_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(pmqa_select_row_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kRowMaxLen * (int)sizeof(float)) != cudaSuccess)
             return PMQA_ERR_CUDA;
         cfg.gridDim = dim3((unsigned)rows);
         cfg.blockDim = dim3(kRowThreads);
         cfg.dynamicSmemBytes = (size_t)smem;
-        if (cudaLaunchKernelEx(&cfg, pmqa_select_row_kernel, s) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, pmqa_select_row_kernel<true>, s) != cudaSuccess)
+            return PMQA_ERR_CUDA;
+    } else if (s.mml <= kRowMaxLenStream) {
+        // one CTA per row, the logits read in place
+        cfg.gridDim = dim3((unsigned)rows);
+        cfg.blockDim = dim3(kRowThreads);
+        cfg.dynamicSmemBytes = 0;
+        if (cudaLaunchKernelEx(&cfg, pmqa_select_row_kernel<false>, s) != cudaSuccess)
             return PMQA_ERR_CUDA;
     } else {
         cfg.gridDim = grid;

@@ -398,8 +398,9 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
 // list in shared memory, so no global atomics, arrival counters or second
 // CTA are involved.
 constexpr int kRowThreads = 1024;
-constexpr int kRowMaxLen = 32768;  // 128 KB of logits in dynamic shared memory
-static_assert(kRowMaxLen <= 32 * kRowThreads, "one 32-bit mask per thread covers its positions");
+constexpr int kRowMaxLen = 32768;        // 128 KB of logits in dynamic shared memory
+constexpr int kRowMaxLenStream = 65536;  // rows read from L2 in place
+static_assert(kRowMaxLenStream <= 64 * kRowThreads, "one 64-bit mask per thread covers its positions");
 
 struct RowShared {
     uint32_t h[kHistBins];
@@ -487,15 +488,20 @@ __device__ uint32_t row_exclusive_scan(RowShared &s, uint32_t x, uint32_t *total
     return s.wsum[wid] + incl - x;
 }
 
+// IN_SMEM: the row (at most kRowMaxLen positions) is copied into shared
+// memory first; else (at most kRowMaxLenStream) it is read in place, once in
+// full and again at the winners and candidates.
+template <bool IN_SMEM>
 __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const __grid_constant__ SelectArgs a)
 {
     extern __shared__ __align__(16) float sv[];  // the row's logits, positions 0 .. n - 1
     __shared__ RowShared s;
+    constexpr int PER = (IN_SMEM ? kRowMaxLen : kRowMaxLenStream) / kRowThreads;  // positions per thread
     const int row = blockIdx.x, tid = threadIdx.x;
     // launched as a dependent of the KV pass: its logits and histograms are
     // complete and visible after this
     griddep_wait();
-    const int n = min(sel_valid_len(a, row), kRowMaxLen);
+    const int n = min(sel_valid_len(a, row), PER * kRowThreads);
     const uint32_t keff = (uint32_t)min(a.k, n);
     const float NEG_INF = -__int_as_float(0x7f800000);
     const long long rbase = (long long)row * a.mml;
@@ -506,7 +512,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
     // the row by bulk copy when it is 16-byte aligned (every row is when the
     // logits are and max_model_len is a multiple of 4), else by plain loads
     const float *src = a.logits + rbase;
-    const bool bulk = keff > 0 && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && (a.mml % 4 == 0);
+    const bool bulk = IN_SMEM && keff > 0 && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) &&
+                      (a.mml % 4 == 0);
     if (bulk && tid == 0) {
         mbar_init(&s.loaded, 1);
         mbar_init_fence();
@@ -524,7 +531,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
             atomicOr(status, 0x4u);
         // the row into shared memory, 16 independent loads in flight per thread
         constexpr int kBatch = 16;
-        for (int base = 0; !bulk && base < n; base += kRowThreads * kBatch) {
+        for (int base = 0; IN_SMEM && !bulk && base < n; base += kRowThreads * kBatch) {
             float v[kBatch];
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
@@ -541,19 +548,20 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
         __syncthreads();
         row_find_bin(s, s.h, kHistBins, keff);
         const uint32_t bstar = s.digit, above = s.above2;
+        auto val = [&](int t) -> float { return IN_SMEM ? sv[t] : __ldcg(src + t); };
         // winners (key bin above b*) and candidates (bin b*) of this thread:
-        // bit u stands for position tid + u * kRowThreads (n <= 32 * kRowThreads)
-        uint32_t msel = 0, mtie = 0;
-#pragma unroll 8
-        for (int u = 0; u < kRowMaxLen / kRowThreads; ++u) {
+        // bit u stands for position tid + u * kRowThreads
+        uint64_t msel = 0, mtie = 0;
+#pragma unroll 16
+        for (int u = 0; u < PER; ++u) {
             const int t = tid + u * kRowThreads;
             if (t < n) {
-                const uint32_t bin = f32_order_key(sv[t]) >> kHistShift;
-                msel |= (bin > bstar ? 1u : 0u) << u;
-                mtie |= (bin == bstar ? 1u : 0u) << u;
+                const uint32_t bin = f32_order_key(val(t)) >> kHistShift;
+                msel |= (uint64_t)(bin > bstar ? 1u : 0u) << u;
+                mtie |= (uint64_t)(bin == bstar ? 1u : 0u) << u;
             }
         }
-        const uint32_t cs = (uint32_t)__popc(msel), ct = (uint32_t)__popc(mtie);
+        const uint32_t cs = (uint32_t)__popcll(msel), ct = (uint32_t)__popcll(mtie);
         uint32_t tot_s, tot_t;
         uint32_t o_s = row_exclusive_scan(s, cs, &tot_s);
         uint32_t o_t = row_exclusive_scan(s, ct, &tot_t);
@@ -563,20 +571,20 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
         // row's list in the workspace
         const bool cached = tot_t <= (uint32_t)kTieCap;
         uint2 *const tl = a.ties + rbase;
-        for (uint32_t m = msel; m; m &= m - 1) {
-            const int t = tid + (__ffs(m) - 1) * kRowThreads;
+        for (uint64_t m = msel; m; m &= m - 1) {
+            const int t = tid + (__ffsll((long long)m) - 1) * kRowThreads;
             if (o_s < keff) {
                 orow[o_s] = t;
                 if (vrow)
-                    vrow[o_s] = sv[t];
+                    vrow[o_s] = val(t);
             } else {
                 atomicOr(status, 0x8u);
             }
             ++o_s;
         }
-        for (uint32_t m = mtie; m; m &= m - 1) {
-            const int t = tid + (__ffs(m) - 1) * kRowThreads;
-            const uint32_t key = f32_order_key(sv[t]);
+        for (uint64_t m = mtie; m; m &= m - 1) {
+            const int t = tid + (__ffsll((long long)m) - 1) * kRowThreads;
+            const uint32_t key = f32_order_key(val(t));
             if (cached) {
                 s.tpos[o_t] = t;
                 s.tkey[o_t] = key;

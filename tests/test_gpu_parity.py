@@ -279,3 +279,33 @@ def test_many_short_requests(cuda_lib, nn, H):
     idx, vals = gpu_fused(cuda_lib, prob, 64, d=d, ws=ws)
     check_topk_rows(idx, r64, tol, prob.context_lens, nn, 64, vals=vals)
     assert cuda_lib.pmqa_read_device_status(ws) == 0
+
+
+# Row lengths that pick each selection kernel: up to 32768 positions (one CTA
+# per row, logits in shared memory), up to 65536 (one CTA per row, logits read
+# in place), above (several CTAs per row).
+@pytest.mark.parametrize("mml", [32768, 40000, 65536, 70000])
+@pytest.mark.parametrize("ties", [False, True])
+def test_standalone_topk_each_selection_kernel(cuda_lib, mml, ties):
+    ctx, nn, k = [mml, mml - 1, 33000, 2049, 1], 1, 2048
+    vals = random_logits(len(ctx) * nn, mml, seed=mml + ties, ties=ties)
+    t = torch.from_numpy(vals).cuda()
+    c = torch.tensor(ctx, dtype=torch.int32, device="cuda")
+    idx, got = cuda_lib.pmqa_topk(t, c, nn, k, want_vals=True)
+    idx, got = idx.cpu().numpy(), got.cpu().numpy()
+    check_topk_exact(idx, vals, ctx, nn, k)
+    for r, cx in enumerate(ctx):
+        ke = min(k, cx)
+        assert np.array_equal(got[r, :ke], vals[r, idx[r, :ke]])
+
+
+def test_fused_topk_with_rows_read_in_place(cuda_lib):
+    """max_model_len between 32768 and 65536: the fused call's selection reads
+    each row in place."""
+    prob = make_problem(3, 2, 64, 16, [33000, 40000, 100], 40000, seed=21, table="perm",
+                        extra_blocks=2)
+    ref, r64, tol = oracle_all(prob)
+    logits = torch.empty((prob.rows, prob.max_model_len), dtype=torch.float32, device="cuda")
+    idx, vals = gpu_fused(cuda_lib, prob, 2048, logits=logits)
+    check_logits(logits.cpu().numpy(), ref, tol)
+    check_topk_rows(idx, r64, tol, prob.context_lens, prob.next_n, 2048, vals=vals)
