@@ -550,15 +550,38 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
         const uint32_t bstar = s.digit, above = s.above2;
         auto val = [&](int t) -> float { return IN_SMEM ? sv[t] : __ldcg(src + t); };
         // winners (key bin above b*) and candidates (bin b*) of this thread:
-        // bit u stands for position tid + u * kRowThreads
+        // bit u stands for position tid + u * kRowThreads. The order key is
+        // monotone in the value (-0 folded onto +0, which v >= +0 also does),
+        // so the bin tests are two float compares against the values whose
+        // keys bound bin b*; for finite logits those are finite or +inf, and
+        // the key compare stays for the case where one is NaN.
+        const bool top = bstar + 1 >= (uint32_t)kHistBins;  // nothing lies above b*
+        const float f0 = f32_from_order_key(bstar << kHistShift);
+        const float f1 = top ? 0.0f : f32_from_order_key((bstar + 1) << kHistShift);
+        const bool by_value = !isnan(f0) && !isnan(f1);
         uint64_t msel = 0, mtie = 0;
+        if (by_value) {
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int t = tid + u * kRowThreads;
+                if (t < n) {
+                    const float v = val(t);
+                    const bool sel = !top && v >= f1;
+                    if (sel)
+                        msel |= 1ull << u;
+                    else if (v >= f0)
+                        mtie |= 1ull << u;
+                }
+            }
+        } else {
 #pragma unroll 16
-        for (int u = 0; u < PER; ++u) {
-            const int t = tid + u * kRowThreads;
-            if (t < n) {
-                const uint32_t bin = f32_order_key(val(t)) >> kHistShift;
-                msel |= (uint64_t)(bin > bstar ? 1u : 0u) << u;
-                mtie |= (uint64_t)(bin == bstar ? 1u : 0u) << u;
+            for (int u = 0; u < PER; ++u) {
+                const int t = tid + u * kRowThreads;
+                if (t < n) {
+                    const uint32_t bin = f32_order_key(val(t)) >> kHistShift;
+                    msel |= (uint64_t)(bin > bstar ? 1u : 0u) << u;
+                    mtie |= (uint64_t)(bin == bstar ? 1u : 0u) << u;
+                }
             }
         }
         const uint32_t cs = (uint32_t)__popcll(msel), ct = (uint32_t)__popcll(mtie);
