@@ -227,10 +227,14 @@ int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
         if (cudaLaunchKernelEx(&cfg, pmqa_select_row_kernel<true>, s) != cudaSuccess)
             return PMQA_ERR_CUDA;
     } else if (s.mml <= kRowMaxLenStream) {
-        // one CTA per row, the logits read in place
+        // one CTA per row, the logits through shared memory in halves
+        if (cudaFuncSetAttribute(pmqa_select_row_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kRowMaxLen * (int)sizeof(float)) != cudaSuccess)
+            return PMQA_ERR_CUDA;
         cfg.gridDim = dim3((unsigned)rows);
         cfg.blockDim = dim3(kRowThreads);
-        cfg.dynamicSmemBytes = 0;
+        cfg.dynamicSmemBytes = (size_t)kRowMaxLen * sizeof(float);
         if (cudaLaunchKernelEx(&cfg, pmqa_select_row_kernel<false>, s) != cudaSuccess)
             return PMQA_ERR_CUDA;
     } else {

@@ -489,8 +489,10 @@ __device__ uint32_t row_exclusive_scan(RowShared &s, uint32_t x, uint32_t *total
 }
 
 // IN_SMEM: the row (at most kRowMaxLen positions) is copied into shared
-// memory first; else (at most kRowMaxLenStream) it is read in place, once in
-// full and again at the winners and candidates.
+// memory first; else (at most kRowMaxLenStream) it passes through shared
+// memory in halves of kRowMaxLen positions for the counting pass (or is read
+// in place when it cannot be bulk-copied), and the writing pass re-reads the
+// winners and candidates in place.
 template <bool IN_SMEM>
 __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const __grid_constant__ SelectArgs a)
 {
@@ -512,22 +514,26 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
     // the row by bulk copy when it is 16-byte aligned (every row is when the
     // logits are and max_model_len is a multiple of 4), else by plain loads
     const float *src = a.logits + rbase;
-    const bool bulk = IN_SMEM && keff > 0 && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) &&
-                      (a.mml % 4 == 0);
+    const bool bulk = keff > 0 && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && (a.mml % 4 == 0);
+    // copy positions [c * kRowMaxLen, ...) of the row into sv (thread 0)
+    auto copy_chunk = [&](int c) {
+        const int p0 = c * kRowMaxLen, len = min(n - p0, kRowMaxLen);
+        const uint32_t bytes = (uint32_t)((len + 3) & ~3) * 4u;  // inside the row: mml % 4 == 0
+        mbar_arrive_expect_tx(&s.loaded, bytes);
+        for (uint32_t off = 0; off < bytes; off += 32768u)
+            bulk_load(smem_u32(sv) + off, reinterpret_cast<const uint8_t *>(src + p0) + off,
+                      min(32768u, bytes - off), &s.loaded);
+    };
     if (bulk && tid == 0) {
         mbar_init(&s.loaded, 1);
         mbar_init_fence();
-        const uint32_t bytes = (uint32_t)((n + 3) & ~3) * 4u;  // inside the row: mml % 4 == 0
-        mbar_arrive_expect_tx(&s.loaded, bytes);
-        for (uint32_t off = 0; off < bytes; off += 32768u)
-            bulk_load(smem_u32(sv) + off, reinterpret_cast<const uint8_t *>(src) + off,
-                      min(32768u, bytes - off), &s.loaded);
+        copy_chunk(0);
     }
     if (keff > 0) {
         for (int e = tid; e < kHistBins; e += kRowThreads)
             s.h[e] = __ldcg(a.hist + (long long)row * kHistBins + e);
         __syncthreads();  // the mbarrier is initialised
-        if (bulk && !mbar_wait(&s.loaded, 0, nullptr))
+        if (IN_SMEM && bulk && !mbar_wait(&s.loaded, 0, nullptr))
             atomicOr(status, 0x4u);
         // the row into shared memory, 16 independent loads in flight per thread
         constexpr int kBatch = 16;
@@ -560,7 +566,34 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
         const float f1 = top ? 0.0f : f32_from_order_key((bstar + 1) << kHistShift);
         const bool by_value = !isnan(f0) && !isnan(f1);
         uint64_t msel = 0, mtie = 0;
-        if (by_value) {
+        if (!IN_SMEM && bulk && by_value) {
+            // half by half through shared memory: half c is bits 32 c .. 32 c + 31
+            for (int c = 0; c * kRowMaxLen < n; ++c) {
+                if (c > 0 && tid == 0)
+                    copy_chunk(c);
+                if (!mbar_wait(&s.loaded, (uint32_t)c & 1u, nullptr))
+                    atomicOr(status, 0x4u);
+                uint32_t ms = 0, mt = 0;
+#pragma unroll
+                for (int u = 0; u < kRowMaxLen / kRowThreads; ++u) {
+                    const int tl0 = tid + u * kRowThreads;  // position within the half
+                    if (c * kRowMaxLen + tl0 < n) {
+                        const float v = sv[tl0];
+                        const bool sel = !top && v >= f1;
+                        if (sel)
+                            ms |= 1u << u;
+                        else if (v >= f0)
+                            mt |= 1u << u;
+                    }
+                }
+                msel |= (uint64_t)ms << (32 * c);
+                mtie |= (uint64_t)mt << (32 * c);
+                __syncthreads();  // every thread is done with the half before the next copy
+            }
+        } else if (by_value) {
+            // (read in place; a first half already on its way lands first)
+            if (!IN_SMEM && bulk && !mbar_wait(&s.loaded, 0, nullptr))
+                atomicOr(status, 0x4u);
 #pragma unroll
             for (int u = 0; u < PER; ++u) {
                 const int t = tid + u * kRowThreads;
@@ -574,6 +607,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
                 }
             }
         } else {
+            if (!IN_SMEM && bulk && !mbar_wait(&s.loaded, 0, nullptr))
+                atomicOr(status, 0x4u);
 #pragma unroll 16
             for (int u = 0; u < PER; ++u) {
                 const int t = tid + u * kRowThreads;
