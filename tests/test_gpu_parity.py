@@ -309,3 +309,40 @@ def test_fused_topk_with_rows_read_in_place(cuda_lib):
     idx, vals = gpu_fused(cuda_lib, prob, 2048, logits=logits)
     check_logits(logits.cpu().numpy(), ref, tol)
     check_topk_rows(idx, r64, tol, prob.context_lens, prob.next_n, 2048, vals=vals)
+
+
+@pytest.mark.parametrize("mml", [4096, 40000, 70000])
+def test_fused_call_replays_from_a_cuda_graph(cuda_lib, mml):
+    """The fused call (KV pass + programmatic-dependent selection) captured in a
+    CUDA graph and replayed gives what the direct call gives, with the same
+    workspace state afterwards (every call leaves it zeroed)."""
+    ctx = [mml - 5, mml // 2, 3000]
+    prob = make_problem(3, 2, 64, 16, ctx, mml, seed=mml, table="perm", extra_blocks=2)
+    d = dev(prob)
+    k = 2048
+    ws = cuda_lib.workspace(prob.bs, prob.next_n, mml, k, cuda_lib.PMQA_OP_LOGITS_TOPK)
+    idx_direct, vals_direct = cuda_lib.pmqa_logits_topk(d["q"], d["kv"], d["w"], d["ctx"], d["bt"],
+                                                        mml, k, want_vals=True, ws=ws)
+    torch.cuda.synchronize()
+    idx = torch.empty_like(idx_direct)
+    vals = torch.empty_like(vals_direct)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        # one call on the capture stream first, so that any lazy setup is done
+        cuda_lib.pmqa_logits_topk(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], mml, k, idx=idx,
+                                  vals=vals, ws=ws, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            cuda_lib.pmqa_logits_topk(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], mml, k,
+                                      idx=idx, vals=vals, ws=ws, stream=stream)
+    for _ in range(2):
+        idx.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize()
+        a, b = idx.cpu().numpy(), idx_direct.cpu().numpy()
+        # same selected sets per row (order within a row is unspecified)
+        assert np.array_equal(np.sort(a, axis=1), np.sort(b, axis=1))
+        assert np.array_equal(np.sort(vals.cpu().numpy(), axis=1),
+                              np.sort(vals_direct.cpu().numpy(), axis=1))
+    assert cuda_lib.pmqa_read_device_status(ws) == 0
