@@ -88,12 +88,27 @@ __global__ void __launch_bounds__(256) pmqa_prefill_prep_kernel(const __grid_con
         const long long c0 = R.y > 0 ? (long long)R.x * kTileTokens : n;
         const long long c1 = R.y > 0 ? min((long long)(R.x + R.y) * kTileTokens, n) : n;
         const int r1 = min(a.SGR, a.m - sg * a.SGR);
+        // [x0, x1) of a row to -inf: scalar stores up to a 16-byte boundary,
+        // then 16-byte stores, then the scalar tail
+        auto fill = [&](float *row, long long x0, long long x1) {
+            const long long mis = (long long)((reinterpret_cast<uintptr_t>(row + x0) >> 2) & 3u);
+            const long long head = min(x1 - x0, mis ? 4 - mis : 0);
+            if (tid < head)
+                row[x0 + tid] = NEG_INF;
+            const long long v0 = x0 + head, nv = (x1 - v0) >> 2;
+            float4 *rv = reinterpret_cast<float4 *>(row + v0);
+            const float4 ninf = make_float4(NEG_INF, NEG_INF, NEG_INF, NEG_INF);
+            for (long long x = tid; x < nv; x += blockDim.x)
+                rv[x] = ninf;
+            for (long long x = v0 + 4 * nv + tid; x < x1; x += blockDim.x)
+                row[x] = NEG_INF;
+        };
         for (int j = 0; j < r1; ++j) {
             float *row = a.logits + (long long)(sg * a.SGR + j) * n;
-            for (long long x = tid; x < c0; x += blockDim.x)
-                row[x] = NEG_INF;
-            for (long long x = c1 + tid; x < n; x += blockDim.x)
-                row[x] = NEG_INF;
+            if (c0 > 0)
+                fill(row, 0, c0);
+            if (c1 < n)
+                fill(row, c1, n);
         }
         __syncthreads();  // rng is rewritten for the next super-group
     }
