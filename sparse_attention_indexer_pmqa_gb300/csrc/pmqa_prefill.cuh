@@ -55,6 +55,9 @@ __global__ void __launch_bounds__(256) pmqa_prefill_prep_kernel(const __grid_con
 {
     __shared__ int2 rng;
     const int tid = threadIdx.x, lane = tid & 31;
+    // the main kernel may start launching; it waits for this grid before it
+    // reads the ranges
+    griddep_launch_dependents();
     const float NEG_INF = -__int_as_float(0x7f800000);
     for (int sg = blockIdx.x; sg < a.n_sg; sg += gridDim.x) {
         if (tid < 32) {
@@ -415,6 +418,9 @@ __global__ void __launch_bounds__(kPfBoundThreads, 1) pmqa_prefill_kernel(const 
     if (warp == 0)
         tmem_alloc(&ctl.tmem_base, (uint32_t)(kGroups * kPassCols));
 
+    // launched as a dependent of the prep kernel: the ranges are complete
+    // and visible after this
+    griddep_wait();
     balance_schedule(a.n_sg, [&](int sg) { return (long long)a.ranges[sg].y; }, ctl);
     tc_fence_before_sync();
     __syncthreads();

@@ -25,7 +25,21 @@ cudaError_t PMQA_CAT(launch_prefill_h, PMQA_HEADS)(const PfArgs &a, int grid, in
                                          (int)a.smem_bytes);
     if (e != cudaSuccess)
         return e;
-    pmqa_prefill_kernel<PMQA_HEADS><<<grid, threads, a.smem_bytes, stream>>>(a);
+    // a programmatic dependent of the prep kernel: its launch and prologue
+    // overlap the prep kernel's end
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = a.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, pmqa_prefill_kernel<PMQA_HEADS>, a);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
