@@ -129,3 +129,24 @@ def test_prefill_full_size_sampled_rows(cuda_lib):
     fin = np.isfinite(got)
     assert np.array_equal(fin.sum(axis=1), p.ke.astype(np.int64))
     assert all(fin[r, : p.ke[r]].all() for r in (0, p.m // 2, p.m - 1))
+
+
+@pytest.mark.parametrize("m,n,H,ranges", [
+    (2048, 8192, 64, "causal"),
+    (1024, 4096, 128, "causal"),
+    (6144, 6144, 32, "packed"),
+])
+def test_prefill_larger_shapes_sampled_rows(cuda_lib, m, n, H, ranges):
+    p = make_prefill(m, n, H, ranges=ranges, seed=m + H)
+    d = dev(p)
+    ws = cuda_lib.workspace(p.m, 1, p.n, 0, cuda_lib.PMQA_OP_MQA_LOGITS)
+    got = gpu_mqa(cuda_lib, p, d=d, ws=ws)
+    assert cuda_lib.pmqa_read_device_status(ws) == 0
+    rng = np.random.default_rng(m)
+    rows = np.unique(np.concatenate([[0, 1, m // 2, m - 1], rng.choice(m, size=20, replace=False)]))
+    ref, _, tol = oracle.mqa_logits(_rows_problem(p, rows), want_tol=True)
+    check_logits(got[rows], ref, tol)
+    # every row's finite entries are exactly its clamped key range
+    lo = np.clip(p.ks.astype(np.int64), 0, n)
+    hi = np.clip(p.ke.astype(np.int64), 0, n)
+    assert np.array_equal(np.isfinite(got).sum(axis=1), np.maximum(hi - lo, 0))
