@@ -288,41 +288,54 @@ __device__ __forceinline__ void load_query(const MainArgs &a, uint8_t *smem, con
 
 // ---------------------------------------------------------------- epilogue math
 
-// acc += sum over NC consecutive columns of w[h] * relu(x[h]) (SIGNED: of
-// relu(-x[h]) when the thread's scale is negative, flip = its sign bit).
-// Packed fp32x2 multiply-adds into four accumulator pairs; the weights come as
-// float4 broadcasts from shared memory. FIRST: the chunk starts a row, and its
-// first products initialise the accumulators instead of adding to them.
-template <int NC, bool SIGNED, bool FIRST = false>
-__device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[NC], uint32_t w, uint32_t flip,
-                                               float (&acc)[8])
+// Over NC consecutive columns: acc[0..3] += w[h] * x[h] and acc[4..7] +=
+// w[h] * |x[h]|, packed fp32x2 multiply-adds (two accumulator pairs each).
+// relu(x) = (x + |x|) / 2 and relu(-x) = (|x| - x) / 2, so the row's
+// sum_h w[h] * relu(+-x[h]) is formed from the two sums in acc_sum without a
+// max per column; the thread's scale sign enters there once. The weights come
+// as float4 broadcasts from shared memory. FIRST: the chunk starts a row, and
+// its products initialise the accumulators instead of adding to them.
+template <int NC, bool FIRST = false>
+__device__ __forceinline__ void epi_accumulate(const uint32_t (&x)[NC], uint32_t w, float (&acc)[8])
 {
 #pragma unroll
     for (int h = 0; h < NC; h += 4) {
         const float4 wv = lds128f_nv(w + (uint32_t)(h * 4));
-        float v[4];
+        float v[4], av[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            v[u] = fmaxf(__uint_as_float(SIGNED ? (x[h + u] ^ flip) : x[h + u]), 0.f);
-        float *p = acc + ((h / 4) & 1) * 4;
-        if (FIRST && h < 8) {
-            fmul2(p[0], p[1], wv.x, wv.y, v[0], v[1]);
-            fmul2(p[2], p[3], wv.z, wv.w, v[2], v[3]);
+        for (int u = 0; u < 4; ++u) {
+            v[u] = __uint_as_float(x[h + u]);
+            av[u] = fabsf(v[u]);
+        }
+        if (FIRST && h == 0) {
+            fmul2(acc[0], acc[1], wv.x, wv.y, v[0], v[1]);
+            fmul2(acc[2], acc[3], wv.z, wv.w, v[2], v[3]);
+            fmul2(acc[4], acc[5], wv.x, wv.y, av[0], av[1]);
+            fmul2(acc[6], acc[7], wv.z, wv.w, av[2], av[3]);
         } else {
-            ffma2(p[0], p[1], wv.x, wv.y, v[0], v[1]);
-            ffma2(p[2], p[3], wv.z, wv.w, v[2], v[3]);
+            ffma2(acc[0], acc[1], wv.x, wv.y, v[0], v[1]);
+            ffma2(acc[2], acc[3], wv.z, wv.w, v[2], v[3]);
+            ffma2(acc[4], acc[5], wv.x, wv.y, av[0], av[1]);
+            ffma2(acc[6], acc[7], wv.z, wv.w, av[2], av[3]);
         }
     }
 }
 
-// The row's sum of the eight accumulators (packed adds); the next row's first
-// chunk re-initialises them.
-__device__ __forceinline__ float acc_sum(float (&acc)[8])
+// The row's sum_h w[h] * relu(x[h]) (SIGNED: relu(-x[h]) when the thread's
+// scale is negative, flip = its sign bit) from the signed sum (acc[0..3]) and
+// the absolute sum (acc[4..7]): (|sum| part +- signed part) / 2. Where every
+// term is clipped the two parts cancel exactly (the same operations on
+// negated operands), so the score is exactly 0. The next row's first chunk
+// re-initialises the accumulators.
+template <bool SIGNED>
+__device__ __forceinline__ float acc_sum(float (&acc)[8], uint32_t flip)
 {
     fadd2(acc[0], acc[1], acc[2], acc[3]);
     fadd2(acc[4], acc[5], acc[6], acc[7]);
-    fadd2(acc[0], acc[1], acc[4], acc[5]);
-    return acc[0] + acc[1];
+    float s = acc[0] + acc[1];
+    if (SIGNED)
+        s = __uint_as_float(__float_as_uint(s) ^ flip);
+    return 0.5f * (s + (acc[4] + acc[5]));
 }
 
 // Draft rows j0 .. j0 + NR - 1 for this thread's token (TMEM lane): row j's
@@ -350,11 +363,11 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t 
         if (ch + 1 < TOTAL)
             tmem_ld_cols<NC>(taddr + (uint32_t)((ch + 1) * NC), b[(ch + 1) & 1]);
         if (ch % CPR == 0)
-            epi_accumulate<NC, SIGNED, true>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), flip, acc);
+            epi_accumulate<NC, true>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), acc);
         else
-            epi_accumulate<NC, SIGNED>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), flip, acc);
+            epi_accumulate<NC>(b[ch & 1], wsl + (uint32_t)(ch * NC * 4), acc);
         if ((ch + 1) % CPR == 0)
-            res[ch / CPR] = acc_sum(acc) * mag;
+            res[ch / CPR] = acc_sum<SIGNED>(acc, flip) * mag;
         if (ch + 1 < TOTAL) {
             tmem_ld_wait();
             reg_fence_cols<NC>(b[(ch + 1) & 1]);
