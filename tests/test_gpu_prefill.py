@@ -150,3 +150,33 @@ def test_prefill_larger_shapes_sampled_rows(cuda_lib, m, n, H, ranges):
     lo = np.clip(p.ks.astype(np.int64), 0, n)
     hi = np.clip(p.ke.astype(np.int64), 0, n)
     assert np.array_equal(np.isfinite(got).sum(axis=1), np.maximum(hi - lo, 0))
+
+
+@pytest.mark.parametrize("H", [32, 128])
+def test_prefill_replays_from_a_cuda_graph(cuda_lib, H):
+    """Both prefill launches (the prep kernel and the main kernel, its
+    programmatic dependent) captured in a CUDA graph on a side stream: every
+    replay rewrites the whole output bit-identically to the direct call."""
+    p = make_prefill(200, 1500, H, ranges="causal", seed=H)
+    ref, _, tol = oracle.mqa_logits(p, want_tol=True)
+    d = dev(p)
+    ws = cuda_lib.workspace(p.m, 1, p.n, 0, cuda_lib.PMQA_OP_MQA_LOGITS)
+    direct = gpu_mqa(cuda_lib, p, d=d, ws=ws)
+    args = (d["q"], d["k"], d["s"], d["w"], d["ks"], d["ke"])
+    out = torch.empty((p.m, p.n), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        # one call on the capture stream first, so that any lazy setup is done
+        cuda_lib.pmqa_mqa_logits(*args, out=out, ws=ws, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            cuda_lib.pmqa_mqa_logits(*args, out=out, ws=ws, stream=stream)
+    for _ in range(2):
+        out.fill_(7.0)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), direct.view(np.uint32))
+    check_logits(got, ref, tol)
+    assert cuda_lib.pmqa_read_device_status(ws) == 0
