@@ -47,13 +47,19 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--all", action="store_true", help="also time every workload")
+    ap.add_argument("--all", action="store_true", default=True,
+                    help="also time every other workload and the prefill (the default)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the headline workload alone (no other workloads, no prefill)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--prefill", action="store_true",
                     help="also time the prefill (non-paged) logits on PF1 (on with --all)")
-    return ap.parse_args(argv)
+    args = ap.parse_args(argv)
+    if args.headline_only:
+        args.all = False
+    return args
 
 
 # ---------------------------------------------------------------- helpers
@@ -557,7 +563,7 @@ def run_ours(args):
             p = r["prob"]
             b = algorithmic_bytes(p, p.k)
             sbw = score_kernel_bytes(p)
-            per[wl] = {"ms": r["ms"], "tokens_per_s": p.total_ctx / (r["ms"] * 1e-3),
+            per[wl] = {"workload": f"{wl}: {CONFIGS[wl]['desc']}", "ms": r["ms"], "tokens_per_s": p.total_ctx / (r["ms"] * 1e-3),
                        "gbs": b["total"] / (r["ms"] * 1e-3) / 1e9,
                        "score_ms": r["ms_score"],
                        "score_gbs": sbw["total"] / (r["ms_score"] * 1e-3) / 1e9,
