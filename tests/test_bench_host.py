@@ -84,3 +84,16 @@ def test_reference_arm_json_line():
         assert key in line, key
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_default_run_times_every_config_and_the_prefill():
+    """With no flags the line carries every config and the prefill beside the
+    headline; --headline-only (used by the profiling commands) times the
+    headline alone unless --prefill asks for the prefill too."""
+    a = bench.parse_args([])
+    assert a.all and a.workload == bench.DEFAULT_WORKLOAD and a.steps >= 1 and a.warmup >= 3
+    a = bench.parse_args(["--headline-only"])
+    assert not a.all and not a.prefill
+    a = bench.parse_args(["--headline-only", "--prefill"])
+    assert not a.all and a.prefill
+    assert set(bench.CONFIGS) >= {"C0", "C1", "C2", "C3", "C4"}
