@@ -563,7 +563,8 @@ def run_ours(args):
             p = r["prob"]
             b = algorithmic_bytes(p, p.k)
             sbw = score_kernel_bytes(p)
-            per[wl] = {"workload": f"{wl}: {CONFIGS[wl]['desc']}", "ms": r["ms"], "tokens_per_s": p.total_ctx / (r["ms"] * 1e-3),
+            per[wl] = {"workload": f"{wl}: {CONFIGS[wl]['desc']}", "ms": r["ms"],
+                       "tokens_per_s": p.total_ctx / (r["ms"] * 1e-3),
                        "gbs": b["total"] / (r["ms"] * 1e-3) / 1e9,
                        "score_ms": r["ms_score"],
                        "score_gbs": sbw["total"] / (r["ms_score"] * 1e-3) / 1e9,
