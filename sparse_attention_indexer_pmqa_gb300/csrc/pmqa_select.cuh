@@ -119,9 +119,12 @@ __device__ void find_bin(SelShared &s, const uint32_t *h, int nbins, uint32_t ne
     if (lane == 31)
         s.wsum[wid] = incl;
     __syncthreads();
-    uint32_t woff = 0;
-    for (int w = 0; w < wid; ++w)
-        woff += s.wsum[w];
+    // the sums of the warps before this one: lane l holds warp l's, then a
+    // warp reduction (exact: integer adds)
+    uint32_t woff = lane < wid ? s.wsum[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        woff += __shfl_xor_sync(kFullMask, woff, o);
     incl += woff;
     const uint32_t excl = incl - loc;
     if (excl < need && need <= incl) {
@@ -434,9 +437,12 @@ __device__ void row_find_bin(RowShared &s, const uint32_t *h, int nbins, uint32_
     if (lane == 31)
         s.wsum[wid] = incl;
     __syncthreads();
-    uint32_t woff = 0;
-    for (int w = 0; w < wid; ++w)
-        woff += s.wsum[w];
+    // the sums of the warps before this one: lane l holds warp l's, then a
+    // warp reduction (exact: integer adds)
+    uint32_t woff = lane < wid ? s.wsum[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        woff += __shfl_xor_sync(kFullMask, woff, o);
     incl += woff;
     const uint32_t excl = incl - loc;
     if (excl < need && need <= incl) {
