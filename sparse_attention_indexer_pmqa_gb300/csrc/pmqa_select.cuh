@@ -539,8 +539,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
         for (int e = tid; e < kHistBins; e += kRowThreads)
             s.h[e] = __ldcg(a.hist + (long long)row * kHistBins + e);
         __syncthreads();  // the mbarrier is initialised
-        if (IN_SMEM && bulk && !mbar_wait(&s.loaded, 0, nullptr))
-            atomicOr(status, 0x4u);
         // the row into shared memory, 16 independent loads in flight per thread
         constexpr int kBatch = 16;
         for (int base = 0; IN_SMEM && !bulk && base < n; base += kRowThreads * kBatch) {
@@ -560,6 +558,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
         __syncthreads();
         row_find_bin(s, s.h, kHistBins, keff);
         const uint32_t bstar = s.digit, above = s.above2;
+        // the bulk copy of the row ran during the bin search
+        if (IN_SMEM && bulk && !mbar_wait(&s.loaded, 0, nullptr))
+            atomicOr(status, 0x4u);
         auto val = [&](int t) -> float { return IN_SMEM ? sv[t] : __ldcg(src + t); };
         // winners (key bin above b*) and candidates (bin b*) of this thread:
         // bit u stands for position tid + u * kRowThreads. The order key is
