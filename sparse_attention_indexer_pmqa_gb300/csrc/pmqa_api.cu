@@ -22,7 +22,8 @@ cudaError_t launch_prefill_h32(const PfArgs &, int, int, cudaStream_t);
 cudaError_t launch_prefill_h64(const PfArgs &, int, int, cudaStream_t);
 cudaError_t launch_prefill_h128(const PfArgs &, int, int, cudaStream_t);
 cudaError_t launch_prefill_prep(const PfArgs &, int, cudaStream_t);
-size_t fused_ws_zero_bytes(int bs, int next_n);
+int fused_call_clearing_state(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
+                              float *logits, void *ws, size_t ws_bytes, cudaStream_t stream);
 }  // namespace pmqa
 
 using namespace pmqa;
@@ -171,8 +172,9 @@ bool encode_rows_map(CUtensorMap *m, const void *q, long long rows, int box_rows
            CUDA_SUCCESS;
 }
 
-SelectArgs select_args(const float *logits, const int32_t *ctx, int bs, int nn, int mml, int k,
-                       int32_t *idx, float *vals, void *ws, const WsLayout &L)
+SelectArgs select_args(const float *logits, const int32_t *ctx, int bs, int nn, int mml,
+                       long long ctx_lim, int k, int32_t *idx, float *vals, void *ws,
+                       const WsLayout &L)
 {
     uint8_t *b = static_cast<uint8_t *>(ws);
     SelectArgs s{};
@@ -181,6 +183,7 @@ SelectArgs select_args(const float *logits, const int32_t *ctx, int bs, int nn, 
     s.bs = bs;
     s.nn = nn;
     s.mml = mml;
+    s.ctx_lim = (int)std::min<long long>(ctx_lim, (long long)mml);
     s.k = k;
     s.idx = idx;
     s.vals = vals;
@@ -247,9 +250,12 @@ int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }
 
+// clear_state: zero the workspace's counters and histograms on the stream
+// first (after every argument check, so an error still enqueues nothing), for
+// a workspace whose previous contents are unknown.
 int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals, float *logits,
              void *ws, size_t ws_bytes, cudaStream_t stream,
-             int stages = PMQA_STAGE_SCORE | PMQA_STAGE_SELECT)
+             int stages = PMQA_STAGE_SCORE | PMQA_STAGE_SELECT, bool clear_state = false)
 {
     if (stages < 1 || stages > (PMQA_STAGE_SCORE | PMQA_STAGE_SELECT))
         return PMQA_ERR_INVALID_ARG;
@@ -314,10 +320,12 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
             sel_src = a.clogits;
         }
     }
+    int sms = 0;
+    if ((rc = sm_count(&sms)) != PMQA_OK)
+        return rc;
+    if (clear_state && fused && cudaMemsetAsync(ws, 0, L.ties, stream) != cudaSuccess)
+        return PMQA_ERR_CUDA;
     if (stages & PMQA_STAGE_SCORE) {
-        int sms = 0;
-        if ((rc = sm_count(&sms)) != PMQA_OK)
-            return rc;
         const int threads = kMaxThreads;
         cudaError_t e;
         switch (p->heads) {
@@ -331,8 +339,10 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     }
     if (!fused || !(stages & PMQA_STAGE_SELECT))
         return PMQA_OK;
-    const SelectArgs s = select_args(sel_src, p->context_lens, p->bs, p->next_n, p->max_model_len,
-                                     k, idx, vals, ws, L);
+    // the same context clamp as the KV pass, so both use one valid length
+    const SelectArgs s =
+        select_args(sel_src, p->context_lens, p->bs, p->next_n, p->max_model_len,
+                    (long long)p->max_blocks_per_seq * p->block_size, k, idx, vals, ws, L);
     return launch_select(s, false, stream);
 }
 
@@ -427,13 +437,14 @@ int run_prefill(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_by
 }  // namespace
 
 namespace pmqa {
-// Bytes at the start of a fused-call workspace that must be zero when a call starts.
-size_t fused_ws_zero_bytes(int bs, int next_n)
+// The fused call on a workspace whose previous contents are unknown: its
+// counters and histograms are zeroed on the stream once every argument check
+// has passed.
+int fused_call_clearing_state(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
+                              float *logits, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
-    WsLayout L;
-    if (!ws_layout((long long)bs * next_n, 1, PMQA_OP_LOGITS_TOPK, &L))
-        return 0;
-    return L.ties;
+    return run_main(p, true, k, idx, vals, logits, ws, ws_bytes, stream,
+                    PMQA_STAGE_SCORE | PMQA_STAGE_SELECT, true);
 }
 }  // namespace pmqa
 
@@ -499,8 +510,8 @@ int pmqa_topk(const float *logits, const int32_t *context_lens, int32_t bs, int3
     if (!logits || !context_lens || !idx || !aligned(logits, 4) || !aligned(context_lens, 4) ||
         !aligned(idx, 4) || (vals && !aligned(vals, 4)))
         return PMQA_ERR_INVALID_ARG;
-    const SelectArgs s =
-        select_args(logits, context_lens, bs, next_n, max_model_len, k, idx, vals, ws, L);
+    const SelectArgs s = select_args(logits, context_lens, bs, next_n, max_model_len,
+                                     max_model_len, k, idx, vals, ws, L);
     return launch_select(s, true, stream);
 }
 

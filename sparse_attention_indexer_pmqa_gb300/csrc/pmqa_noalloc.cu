@@ -20,7 +20,8 @@
 #include "../../include/pmqa.h"
 
 namespace pmqa {
-size_t fused_ws_zero_bytes(int bs, int next_n);
+int fused_call_clearing_state(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
+                              float *logits, void *ws, size_t ws_bytes, cudaStream_t stream);
 }
 
 namespace {
@@ -70,10 +71,8 @@ extern "C" int pmqa_logits_topk_noalloc(const pmqa_problem *p, int32_t k, int32_
     if (rc != PMQA_OK)
         return rc;
     // The array keeps whatever the previous call left. The fused call needs its
-    // status word, per-row counters and per-row histograms at zero; the rest is
-    // always written before it is read.
-    const size_t zero = pmqa::fused_ws_zero_bytes(p->bs, p->next_n);
-    if (zero == 0 || cudaMemsetAsync(ws, 0, zero, stream) != cudaSuccess)
-        return PMQA_ERR_CUDA;
-    return pmqa_logits_topk(p, k, idx, vals, logits, ws, kScratchBytes, stream);
+    // status word, per-row counters and per-row histograms at zero (the rest is
+    // always written before it is read); it clears them on the stream once
+    // every argument has been checked, so a rejected call enqueues nothing.
+    return pmqa::fused_call_clearing_state(p, k, idx, vals, logits, ws, kScratchBytes, stream);
 }

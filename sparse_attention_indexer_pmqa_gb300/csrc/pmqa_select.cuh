@@ -27,6 +27,8 @@ struct SelectArgs {
     const float *logits;  // [rows, mml]; positions t < valid_len are read
     const int32_t *ctx_lens;
     int bs, nn, mml, k;
+    int ctx_lim;        // contexts are clamped to [0, ctx_lim]: the KV pass's limit
+                        // min(mml, P * max_blocks_per_seq) on the fused path, mml alone
     int32_t *idx;       // [rows, k]
     float *vals;        // [rows, k] or null
     uint32_t *hist;     // [rows, 2048]
@@ -44,7 +46,7 @@ constexpr int kSelPer = 16;  // positions per thread: one CTA covers 256 * 16 = 
 
 __device__ __forceinline__ int sel_valid_len(const SelectArgs &a, int row)
 {
-    const int c = clamp_ctx(__ldg(a.ctx_lens + row / a.nn), (long long)a.mml);
+    const int c = clamp_ctx(__ldg(a.ctx_lens + row / a.nn), (long long)a.ctx_lim);
     return valid_len(c, a.nn, row % a.nn);
 }
 

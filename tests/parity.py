@@ -4,9 +4,9 @@ Logits: the -inf pattern must match exactly; every finite entry must satisfy
 |gpu - oracle| <= 1e-3 * (1 + sum_h |w_h| |x_h|) (the oracle's tolerance array).
 Top-k: per row the selected set has exactly min(k, valid_len) distinct positions
 inside the window and -1 after; it equals the oracle's set except for positions
-whose oracle logit lies within the tolerance of the oracle's k-th value (for a
-swapped pair both entries' errors count, so the bound is twice the larger of
-their tolerances).
+whose oracle logit lies within that position's own tolerance of the oracle's
+k-th value: a position chosen in place of an oracle pick sits at most tol below
+the k-th value, and an oracle pick left out sits at most tol above it.
 """
 
 from __future__ import annotations
@@ -56,15 +56,12 @@ def check_topk_rows(idx: np.ndarray, ref64: np.ndarray, tol: np.ndarray, ctx, nn
         kth = row[ref_set[-1]]
         g, o = set(sel.tolist()), set(ref_set.tolist())
         extra, missing = g - o, o - g
-        # A swap needs the two entries' GPU errors to bridge their gap, so each
-        # swapped position lies within the sum of two entry tolerances of the
-        # k-th value.
-        if extra:
-            tmax = max(float(tol[r, p]) for p in extra | missing | {int(ref_set[-1])})
-            for p in extra:
-                assert row[p] >= kth - 2 * tmax, f"row {r}: chose {p} ({row[p]}) below k-th {kth}"
-            for p in missing:
-                assert row[p] <= kth + 2 * tmax, f"row {r}: missed {p} ({row[p]}) above k-th {kth}"
+        for p in extra:
+            assert row[p] >= kth - float(tol[r, p]), \
+                f"row {r}: chose {p} ({row[p]}) more than its tolerance below the k-th {kth}"
+        for p in missing:
+            assert row[p] <= kth + float(tol[r, p]), \
+                f"row {r}: missed {p} ({row[p]}) more than its tolerance above the k-th {kth}"
         swaps += len(extra)
         if vals is not None:
             assert np.all(np.isneginf(vals[r, ke:])), f"row {r}: padding values not -inf"

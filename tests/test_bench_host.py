@@ -99,3 +99,22 @@ def test_default_run_times_every_config_and_the_prefill():
     from synth import CONFIGS
 
     assert set(CONFIGS) >= {"C0", "C1", "C2", "C3", "C4"}
+
+
+def test_kv_roofline_counts_the_kv_stream_only():
+    prob = make_problem(2, 2, 16, 4, [10, 3], 16, seed=1)
+    kr = bench.kv_roofline(prob, score_ms=1e-3, step_ms=2e-3, peak=1000.0)
+    assert kr["kv_bytes"] == 132 * 13
+    assert kr["achieved"] == pytest.approx(132 * 13 / 1e-6 / 1e9)
+    assert kr["frac"] == pytest.approx(kr["achieved"] / 1000.0)
+    assert kr["fused_frac"] == pytest.approx(kr["frac"] / 2)
+    other = kr["other_bytes"]
+    assert "kv" not in other and other["compact_logits"] == 4 * 24
+    assert other["total"] == sum(v for k, v in other.items() if k != "total")
+
+
+def test_cpu_description_and_cpu_ranges():
+    d = bench.cpu_description()
+    assert d["cpu_model"] and d["logical_cpus"] >= 1 and d["affinity"]
+    assert bench._ranges([0, 1, 2, 5, 7, 8]) == "0-2,5,7-8"
+    assert bench._ranges([3]) == "3"

@@ -112,6 +112,39 @@ def test_block_sizes_and_draft_rows(cuda_lib, case):
         check_logits(logits.cpu().numpy(), ref, tol)
 
 
+# The scale's sign: relu(s * x) = |s| * relu(-x) for s < 0, which the kernel
+# applies per token by flipping the sign of the row's signed sum. Mixed signs
+# put both kinds of token in every warp; an all-negative range makes every
+# token of every tile flip. Block sizes 1 (row windows) and 64 (page runs),
+# one and four draft rows.
+SIGNED = [
+    # bs, next_n, heads, block_size, context lengths, max_model_len, scale range
+    (3, 1, 64, 1, [300, 129, 1000], 1024, (-0.1, 0.1)),
+    (2, 4, 64, 1, [700, 260], 768, (-0.1, 0.1)),
+    (2, 1, 32, 64, [1000, 130], 1024, (-0.1, 0.1)),
+    (2, 4, 64, 64, [513, 1000], 1024, (-0.1, 0.1)),
+    (2, 1, 64, 1, [640, 300], 640, (-0.1, -0.01)),
+    (2, 4, 64, 64, [513, 1000], 1024, (-0.1, -0.01)),
+    (2, 2, 128, 1, [400, 129], 512, (-0.1, -0.01)),
+]
+
+
+@pytest.mark.parametrize("case", SIGNED, ids=lambda c: f"nn{c[1]}H{c[2]}P{c[3]}s{c[6][1]:+g}")
+def test_negative_and_mixed_scales(cuda_lib, case):
+    bs, nn, H, P, ctx, mml, sr = case
+    prob = make_problem(bs, nn, H, P, ctx, mml, seed=sum(ctx) + nn + P, table="perm",
+                        extra_blocks=2, scale_range=sr)
+    ref, r64, tol = oracle_all(prob)
+    if sr[1] < 0:  # every scale negative: the scores come from the q.k < 0 terms alone
+        assert np.any(ref[np.isfinite(ref)] != 0)
+    check_logits(gpu_logits(cuda_lib, prob), ref, tol)
+    for k in (7, 2048):
+        logits = torch.empty((bs * nn, mml), dtype=torch.float32, device="cuda")
+        idx, vals = gpu_fused(cuda_lib, prob, k, logits=logits)
+        check_topk_rows(idx, r64, tol, prob.context_lens, nn, k, vals=vals)
+        check_logits(logits.cpu().numpy(), ref, tol)
+
+
 @pytest.mark.parametrize("ties", [False, True])
 @pytest.mark.parametrize("k", [1, 5, 300, 2048])
 def test_standalone_topk_exact(cuda_lib, k, ties):
@@ -234,6 +267,26 @@ def test_context_longer_than_max_model_len_is_flagged(cuda_lib):
     ws = cuda_lib.workspace(1, 1, 128, 0, cuda_lib.PMQA_OP_LOGITS)
     cuda_lib.pmqa_logits(d["q"], d["kv"], d["w"], d["ctx"], d["bt"], 128, ws=ws)
     assert cuda_lib.pmqa_read_device_status(ws) & cuda_lib.PMQA_DEV_BAD_CONTEXT
+
+
+def test_context_beyond_the_block_table_is_clamped_in_the_fused_call(cuda_lib):
+    """A context longer than block_size * max_blocks_per_seq (but within
+    max_model_len): the KV pass and the selection clamp it to the table's reach
+    alike, so no selected position lies past it, and the status says so."""
+    P, W, mml = 16, 20, 512
+    prob = make_problem(2, 2, 64, P, [P * W, 300], mml, seed=31, table="perm", extra_blocks=2,
+                        width=W)
+    ref, r64, tol = oracle_all(prob)
+    d = dev(prob)
+    d["ctx"][0] = 400  # the table reaches 320 tokens
+    for k in (7, 2048):
+        ws = cuda_lib.workspace(prob.bs, prob.next_n, mml, k, cuda_lib.PMQA_OP_LOGITS_TOPK)
+        logits = torch.empty((prob.rows, mml), dtype=torch.float32, device="cuda")
+        idx, vals = gpu_fused(cuda_lib, prob, k, d=d, ws=ws, logits=logits)
+        assert cuda_lib.pmqa_read_device_status(ws) == cuda_lib.PMQA_DEV_BAD_CONTEXT
+        assert idx.max() < P * W
+        check_topk_rows(idx, r64, tol, prob.context_lens, prob.next_n, k, vals=vals)
+        check_logits(logits.cpu().numpy(), ref, tol)
 
 
 # ------------------------------------------------------------- full workloads

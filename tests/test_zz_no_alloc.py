@@ -68,3 +68,33 @@ def test_noalloc_matches_the_workspace_entry_point(cuda_lib):
             assert np.all(np.abs(va[fin].astype(np.float64) - vb[fin]) <= tol[r, pos])
         lg = logits.cpu().numpy()
         assert np.array_equal(np.isneginf(lg), np.isneginf(r64))
+
+
+@pytest.mark.gpu
+def test_noalloc_clamps_a_context_beyond_the_table_over_stale_scratch(cuda_lib):
+    """The scratch keeps the previous call's compact logits. A following call
+    whose context runs past block_size * max_blocks_per_seq must select only
+    from positions its KV pass scored, never from what an earlier call left."""
+    P, W, mml, k = 16, 20, 512, 2048
+    big = make_problem(2, 2, 64, P, [mml, mml], mml, seed=41, table="perm", extra_blocks=2)
+    big.weights *= 100.0  # large leftovers past position P * W
+    db = {n: torch.from_numpy(a).cuda() for n, a in
+          (("kv", big.kv), ("w", big.weights), ("ctx", big.context_lens), ("bt", big.block_tables))}
+    qb = torch.from_numpy(big.q).cuda().view(torch.float8_e4m3fn)
+    idx = torch.empty((big.rows, k), dtype=torch.int32, device="cuda")
+    cuda_lib.pmqa_logits_topk_noalloc(qb, db["kv"], db["w"], db["ctx"], db["bt"], mml, k, idx=idx)
+    prob = make_problem(2, 2, 64, P, [P * W, 300], mml, seed=42, table="perm", extra_blocks=2,
+                        width=W)
+    _, r64, tol = oracle.logits(prob, want64=True, want_tol=True)
+    d = {n: torch.from_numpy(a).cuda() for n, a in
+         (("kv", prob.kv), ("w", prob.weights), ("ctx", prob.context_lens),
+          ("bt", prob.block_tables))}
+    q = torch.from_numpy(prob.q).cuda().view(torch.float8_e4m3fn)
+    d["ctx"][0] = 400  # the table reaches 320 tokens
+    vals = torch.empty((prob.rows, k), dtype=torch.float32, device="cuda")
+    cuda_lib.pmqa_logits_topk_noalloc(q, d["kv"], d["w"], d["ctx"], d["bt"], mml, k, idx=idx,
+                                      vals=vals)
+    torch.cuda.synchronize()
+    got_i, got_v = idx.cpu().numpy(), vals.cpu().numpy()
+    assert got_i.max() < P * W
+    check_topk_rows(got_i, r64, tol, prob.context_lens, prob.next_n, k, vals=got_v)
