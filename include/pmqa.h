@@ -162,7 +162,11 @@ int pmqa_logits_topk_stages(const pmqa_problem *p, int32_t k, int32_t *idx, floa
  * The workspace is a 32 MiB array that the library keeps in device memory on
  * every GPU where it is loaded, until the process exits. Problems whose
  * pmqa_workspace_bytes(bs, next_n, max_model_len, k, PMQA_OP_LOGITS_TOPK)
- * exceeds 32 MiB return PMQA_ERR_WORKSPACE with nothing enqueued.
+ * exceeds 32 MiB return PMQA_ERR_WORKSPACE with nothing enqueued: that size is
+ * 12 bytes per (row, position) -- an 8-byte candidate entry and a 4-byte
+ * compact logit -- plus 8 KB of histogram and 12 bytes of counters per row and
+ * 256 bytes of status, so for example 16 rows of 131072 positions fit and 16
+ * rows of 202752 do not.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before capturing
  * any stream. Every call shares the one array and clears its counters at the
@@ -173,6 +177,46 @@ int pmqa_logits_topk_stages(const pmqa_problem *p, int32_t k, int32_t *idx, floa
  */
 int pmqa_logits_topk_noalloc(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
                              float *logits, pmqa_stream_t stream);
+
+/*
+ * The fused call restricted to a slice of every request's tokens: request i
+ * scores only tokens token_begin[i] <= t < token_end[i] (device int32 [bs]
+ * each, clamped to [0, ctx_i]; an empty slice scores nothing), with the
+ * request's full context for the causal window, and selects per row the
+ * positions (global t) of the min(k, admitted tokens of the slice) largest
+ * logits; idx and vals as for pmqa_logits_topk. The block table is read only
+ * for pages that hold tokens of the slice, so a GPU that keeps only its
+ * slice's pages may leave the other entries unset. This is the per-GPU step
+ * of a context-parallel split, whose lists pmqa_topk_merge combines; a call on
+ * the whole range [0, ctx_i) equals pmqa_logits_topk. Workspace as for
+ * PMQA_OP_LOGITS_TOPK; two kernel launches, as pmqa_logits_topk.
+ */
+int pmqa_logits_topk_range(const pmqa_problem *p, const int32_t *token_begin,
+                           const int32_t *token_end, int32_t k, int32_t *idx, float *vals,
+                           void *ws, size_t ws_bytes, pmqa_stream_t stream);
+
+/*
+ * Top-k of the union of candidate lists, per row: the merge step of a
+ * context-parallel split of the indexer, in which each GPU holds a slice of
+ * every request's tokens, scores it (pmqa_logits_topk_range) and keeps the
+ * slice's top-k positions and logits; the lists are gathered from the GPUs
+ * (an all-gather) and merged here. Every one of a row's k largest logits lies
+ * in its own slice's top-k, so the union's top-k is the row's top-k. The pages
+ * name decode context parallelism (DCP) among the configurations of the
+ * sparse-MLA decode path (page "[Bug][ROCm]: ROCM_AITER_MLA can select an aiter
+ * MLA decode kernel that silently returns uncorrelated output", chat-gpts.plus
+ * summary, closing notes); the split and this merge are the library's design.
+ *   idx       int32 [lists, rows, k_in]: positions, -1 for an empty slot (skipped)
+ *   vals      fp32 [lists, rows, k_in]: their logits
+ *   out_idx   int32 [rows, k]: the positions of the min(k, valid candidates)
+ *             largest logits (order unspecified, ties either way), then -1
+ *   out_vals  fp32 [rows, k] or NULL: their logits, then -inf
+ * A position may appear in at most one of a row's lists. lists * k_in < 2^31
+ * (PMQA_ERR_UNSUPPORTED otherwise). No workspace; one kernel launch.
+ */
+int pmqa_topk_merge(const int32_t *idx, const float *vals, int32_t lists, int32_t rows,
+                    int32_t k_in, int32_t k, int32_t *out_idx, float *out_vals,
+                    pmqa_stream_t stream);
 
 /*
  * Prefill (non-paged) logits. Source: the page "[Bug] aiter ops triton

@@ -125,7 +125,7 @@ bool main_layout(int heads, int nn, MainArgs &a)
         off += (uint32_t)(QS * N * 4);
         off = (uint32_t)align_up(off, 16);
         a.off_bar = off;
-        off += (uint32_t)(QS + kGroups + kNumWarps) * 8u;
+        off += (uint32_t)(QS + kNumBars) * 8u;
         const uint32_t total = std::max<uint32_t>(off + 1024, kMinMainSmem);
         if (total > kMaxDynSmem)
             continue;
@@ -253,9 +253,12 @@ int launch_select(const SelectArgs &s, bool with_hist_pass, cudaStream_t stream)
 // clear_state: zero the workspace's counters and histograms on the stream
 // first (after every argument check, so an error still enqueues nothing), for
 // a workspace whose previous contents are unknown.
+// tok_begin / tok_end: score and select only that slice of each request's
+// tokens (the fused call without a logits output).
 int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals, float *logits,
              void *ws, size_t ws_bytes, cudaStream_t stream,
-             int stages = PMQA_STAGE_SCORE | PMQA_STAGE_SELECT, bool clear_state = false)
+             int stages = PMQA_STAGE_SCORE | PMQA_STAGE_SELECT, bool clear_state = false,
+             const int32_t *tok_begin = nullptr, const int32_t *tok_end = nullptr)
 {
     if (stages < 1 || stages > (PMQA_STAGE_SCORE | PMQA_STAGE_SELECT))
         return PMQA_ERR_INVALID_ARG;
@@ -271,6 +274,10 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
         return PMQA_ERR_INVALID_ARG;
     }
     if (logits && !aligned(logits, 4))
+        return PMQA_ERR_INVALID_ARG;
+    if ((tok_begin != nullptr) != (tok_end != nullptr))
+        return PMQA_ERR_INVALID_ARG;
+    if (tok_begin && (!fused || logits || !aligned(tok_begin, 4) || !aligned(tok_end, 4)))
         return PMQA_ERR_INVALID_ARG;
     const long long rows = (long long)p->bs * p->next_n;
     WsLayout L;
@@ -312,6 +319,8 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     a.status = reinterpret_cast<uint32_t *>(wsb);
     a.l2_policy = PMQA_L2_POLICY;
     a.page_mode = (p->block_size % 4 == 0) ? 1 : 0;
+    a.tok_begin = tok_begin;
+    a.tok_end = tok_end;
     float *sel_src = logits;
     if (fused) {
         a.hist = reinterpret_cast<uint32_t *>(wsb + L.hist);
@@ -340,9 +349,11 @@ int run_main(const pmqa_problem *p, bool fused, int k, int32_t *idx, float *vals
     if (!fused || !(stages & PMQA_STAGE_SELECT))
         return PMQA_OK;
     // the same context clamp as the KV pass, so both use one valid length
-    const SelectArgs s =
+    SelectArgs s =
         select_args(sel_src, p->context_lens, p->bs, p->next_n, p->max_model_len,
                     (long long)p->max_blocks_per_seq * p->block_size, k, idx, vals, ws, L);
+    s.tok_begin = tok_begin;
+    s.tok_end = tok_end;
     return launch_select(s, false, stream);
 }
 
@@ -482,6 +493,16 @@ int pmqa_logits_topk(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals
     return run_main(p, true, k, idx, vals, logits, ws, ws_bytes, stream);
 }
 
+int pmqa_logits_topk_range(const pmqa_problem *p, const int32_t *token_begin,
+                           const int32_t *token_end, int32_t k, int32_t *idx, float *vals,
+                           void *ws, size_t ws_bytes, pmqa_stream_t stream)
+{
+    if (!token_begin || !token_end)
+        return PMQA_ERR_INVALID_ARG;
+    return run_main(p, true, k, idx, vals, nullptr, ws, ws_bytes, stream,
+                    PMQA_STAGE_SCORE | PMQA_STAGE_SELECT, false, token_begin, token_end);
+}
+
 int pmqa_logits_topk_stages(const pmqa_problem *p, int32_t k, int32_t *idx, float *vals,
                             float *logits, void *ws, size_t ws_bytes, pmqa_stream_t stream,
                             int32_t stages)
@@ -513,6 +534,32 @@ int pmqa_topk(const float *logits, const int32_t *context_lens, int32_t bs, int3
     const SelectArgs s = select_args(logits, context_lens, bs, next_n, max_model_len,
                                      max_model_len, k, idx, vals, ws, L);
     return launch_select(s, true, stream);
+}
+
+int pmqa_topk_merge(const int32_t *idx, const float *vals, int32_t lists, int32_t rows,
+                    int32_t k_in, int32_t k, int32_t *out_idx, float *out_vals,
+                    pmqa_stream_t stream)
+{
+    if (lists < 1 || rows < 0 || k_in < 1 || k < 1)
+        return PMQA_ERR_INVALID_ARG;
+    if ((long long)lists * k_in >= (1ll << 31))
+        return PMQA_ERR_UNSUPPORTED;
+    if (rows == 0)
+        return PMQA_OK;
+    if (!idx || !vals || !out_idx || !aligned(idx, 4) || !aligned(vals, 4) || !aligned(out_idx, 4) ||
+        (out_vals && !aligned(out_vals, 4)))
+        return PMQA_ERR_INVALID_ARG;
+    MergeArgs m{};
+    m.idx = idx;
+    m.vals = vals;
+    m.lists = lists;
+    m.rows = rows;
+    m.k_in = k_in;
+    m.k = k;
+    m.out_idx = out_idx;
+    m.out_vals = out_vals;
+    pmqa_merge_kernel<<<(unsigned)rows, kSelThreads, 0, stream>>>(m);
+    return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }
 
 int pmqa_mqa_logits(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_bytes,

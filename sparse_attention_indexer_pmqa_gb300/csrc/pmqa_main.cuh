@@ -73,6 +73,9 @@ struct MainArgs {
     uint32_t *status;
     int l2_policy;     // KV stream: 0 evict_first, 1 evict_normal, 2 evict_last
     int page_mode;     // block_size % 4 == 0: rows move as page runs by bulk copy
+    // a slice [tok_begin[i], tok_end[i]) of every request's tokens, or null
+    // for all of them (clamped to [0, ctx_i])
+    const int32_t *tok_begin, *tok_end;
     // shared-memory / TMEM layout, computed on the host
     int N, QS, cols, tmem_cols;
     int q_box;  // rows per q TMA box: N / ceil(N / 256)
@@ -171,11 +174,13 @@ __device__ void balance_schedule(int n_items, LenFn len_of, CtaCtl &c)
 }
 
 // Context lengths of the CTA's requests: from the shared-memory cache while it
-// covers them, else from global memory (clamped).
+// covers them, else from global memory (clamped); and the slice of each
+// request's tokens to score.
 struct ReqCtx {
     int bs, i0, lim;
     const int *cache;  // clamped contexts of requests i0 .. i0 + kCtxCache - 1
     const int32_t *ctx_lens;
+    const int32_t *tok_begin, *tok_end;
     __device__ void init(const MainArgs &a, const CtaCtl &cc)
     {
         bs = a.bs;
@@ -183,39 +188,90 @@ struct ReqCtx {
         lim = (int)min((long long)a.mml, (long long)a.W * a.P);
         cache = cc.ctx;
         ctx_lens = a.ctx_lens;
+        tok_begin = a.tok_begin;
+        tok_end = a.tok_end;
     }
     __device__ int ctx_at(int r) const
     {
         const int n = r - i0;
         return (n >= 0 && n < kCtxCache) ? cache[n] : clamp_ctx(__ldg(ctx_lens + r), (long long)lim);
     }
+    // tokens [tb, te) of request r (context ctx) are scored
+    __device__ void bounds(int r, int ctx, int &tb, int &te) const
+    {
+        if (tok_begin) {
+            tb = clamp_ctx(__ldg(tok_begin + r), (long long)ctx);
+            te = max(tb, clamp_ctx(__ldg(tok_end + r), (long long)ctx));
+        } else {
+            tb = 0;
+            te = ctx;
+        }
+    }
 };
 
-// Position (request i, tile m of nt, context ctx) in the CTA's walk over
-// (request, tile) pairs; empty requests are skipped.
+// 128-token tiles [mb, nt) that cover tokens [tb, te) (none when te <= tb).
+__device__ __forceinline__ void tile_span(int tb, int te, int &mb, int &nt)
+{
+    if (te > tb) {
+        mb = tb / kTileTokens;
+        nt = (te + kTileTokens - 1) / kTileTokens;
+    } else {
+        mb = nt = 0;
+    }
+}
+
+// Tiles of request i to score (the length of its work item in the schedule).
+__device__ __forceinline__ int tiles_of(const MainArgs &a, int i)
+{
+    const int ctx = ctx_of(a, i);
+    int tb = 0, te = ctx, mb, nt;
+    if (a.tok_begin) {
+        tb = clamp_ctx(__ldg(a.tok_begin + i), (long long)ctx);
+        te = max(tb, clamp_ctx(__ldg(a.tok_end + i), (long long)ctx));
+    }
+    tile_span(tb, te, mb, nt);
+    return nt - mb;
+}
+
+// Position (request i, tile m of the tiles [mb, nt) covering its tokens
+// [tb, te), context ctx) in the CTA's walk over (request, tile) pairs;
+// requests without tiles are skipped.
 struct TilePos {
-    int i, m, nt, ctx;
+    int i, m, mb, nt, ctx, tb, te;
+    __device__ void set_request(const ReqCtx &rc, int r)
+    {
+        i = r;
+        ctx = rc.ctx_at(r);
+        rc.bounds(r, ctx, tb, te);
+        tile_span(tb, te, mb, nt);
+    }
+    __device__ void clear()
+    {
+        m = mb = nt = ctx = tb = te = 0;
+    }
     __device__ void init(const ReqCtx &rc, const CtaCtl &cc)
     {
-        i = cc.i0;
-        m = cc.m0;
-        ctx = i < rc.bs ? rc.ctx_at(i) : 0;
-        nt = (ctx + kTileTokens - 1) / kTileTokens;
+        if (cc.i0 < rc.bs) {
+            set_request(rc, cc.i0);
+            m = mb + cc.m0;
+        } else {
+            i = cc.i0;
+            clear();
+        }
     }
     __device__ void next(const ReqCtx &rc)
     {
         if (++m < nt)
             return;
-        m = 0;
         do {
-            if (++i >= rc.bs) {
-                nt = 0;
-                ctx = 0;
+            if (i + 1 >= rc.bs) {
+                ++i;
+                clear();
                 return;
             }
-            ctx = rc.ctx_at(i);
-            nt = (ctx + kTileTokens - 1) / kTileTokens;
+            set_request(rc, i + 1);
         } while (nt == 0);
+        m = mb;
     }
     __device__ void skip(const ReqCtx &rc, int n)
     {
@@ -257,6 +313,7 @@ struct Bars {
         run = mma + kGroups;
     }
 };
+constexpr int kNumBars = kGroups + kNumWarps;  // plus QS
 
 __device__ __forceinline__ void raise_abort(const MainArgs &a, CtaCtl &c)
 {
@@ -423,83 +480,76 @@ struct Walk {
     }
 };
 
-// Warpgroup g, warp quadrant qd (warp % 4): CTA tiles g, g + 4, g + 8, ...
-// Shared memory is addressed through 32-bit shared addresses throughout.
-template <int H>
-static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int g, int qd)
-{
-    const Bars B(a, smem);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t R = (uint32_t)(qd * 32 + lane);  // tile row = TMEM lane
-    const bool elected = qd == 0 && lane == 0;
-    const uint32_t wg_bar = 1u + (uint32_t)g;
-    const int count = (int)c.count;
-    const uint32_t tmem_base = c.tmem_base;
-    const int N = a.N, nn = a.nn, QS = a.QS;
-    // gather
-    const uint64_t pol = a.l2_policy == 0   ? l2_evict_first_policy()
-                         : a.l2_policy == 2 ? l2_evict_last_policy()
-                                            : l2_evict_normal_policy();
-    const uint8_t *const kv = a.kv;
-    const int32_t *const bt = a.bt;
-    const long long num_blocks = a.num_blocks, pool_bytes = a.pool_bytes;
-    const bool pool32 = pool_bytes < (1ll << 31) - 1024;  // every byte offset fits in 31 bits
-    const int P = a.P, W = a.W;
-    const bool p_pow2 = (P & (P - 1)) == 0;
-    const int p_shift = __ffs(P) - 1;
-    uint32_t *const status = a.status;
-    const bool page_mode = a.page_mode != 0;
-    auto page_of = [&](int tok) { return p_pow2 ? tok >> p_shift : tok / P; };
-    // shared memory: the group's staging slot, then its operand tile
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t stage = sbase + a.off_grp + (uint32_t)g * kGroupBytes;
-    // window mode: row R's 16-byte aligned window; page runs: the row itself
-    const uint32_t win = stage + (page_mode ? R * (uint32_t)kKvRowBytes : R * kWinBytes);
-    // operand row R is 128-byte aligned: chunk ch sits at opx ^ (ch << 4)
-    const uint32_t opx = (stage + kSlotBytes + R * 128u) ^ ((R & 7u) << 4);
-    const uint32_t wstage = stage + (uint32_t)(qd * 32) * kWinBytes;  // this warp's 32 windows
-    uint64_t *const run_bar = &B.run[warp];
-    const uint32_t w_base = sbase + a.off_w;
-    const uint32_t w_slot_bytes = (uint32_t)N * 4u;
-    // TMEM: this warp's lane quadrant, the group's columns
-    const uint32_t dcol = tmem_base + (uint32_t)(g * a.cols);
-    const uint32_t tacc = dcol + ((uint32_t)(qd * 32) << 16);
-    // MMA operands; passes of at most 128 accumulator columns (whole draft rows)
-    const uint64_t adesc = sw128_kmajor_desc(stage + kSlotBytes);
-    const uint64_t bdesc0 = sw128_kmajor_desc(sbase + a.off_q);
-    const uint32_t q_units = (uint32_t)N * kHeadDim >> 4;
-    constexpr int kRpp = kPassCols / H < kMaxRows ? kPassCols / H : kMaxRows;  // rows per pass
-    const int npass = (nn + kRpp - 1) / kRpp;
-    // copy e = qq * 32 + lane of a warp's 288 window chunks: window e / 9,
-    // chunk e % 9; bit qq of last9 marks chunk 8 (the window's last)
-    uint32_t last9 = 0;
-#pragma unroll
-    for (int qq = 0; qq < 9; ++qq)
-        last9 |= (((uint32_t)(qq * 32 + lane) % 9u) == 8u ? 1u : 0u) << qq;
-    // outputs
-    const long long mml = a.mml;
-    float *const logits = a.logits;
-    float *const clogits = a.clogits;
-    uint32_t *const hist = a.hist;
-    const uint64_t keep_pol = l2_evict_last_policy();
-    const float NEG_INF = -__int_as_float(0x7f800000);
+// One warpgroup's gather of its own tiles: the block-table entries, the copies
+// of a tile's rows into the warpgroup's staging slot, and the repack of this
+// thread's row R into the 128B-swizzled K-major operand tile behind the slot.
+struct TileGather {
+    const uint8_t *kv;
+    const int32_t *bt;
+    long long num_blocks, pool_bytes;
+    uint32_t *status;
+    uint64_t pol;
+    int P, W, p_shift;
+    bool p_pow2, page_mode, pool32;
+    uint32_t R, lane, last9;
+    uint32_t stage, win, opx, wstage;
+    uint64_t *run_bar;
+    uint32_t run_phase;
 
-    ReqCtx rc;
-    rc.init(a, c);
+    __device__ void init(const MainArgs &a, uint32_t stage_addr, uint32_t qd, uint32_t lane_,
+                         uint64_t *run_bar_)
+    {
+        pol = a.l2_policy == 0   ? l2_evict_first_policy()
+              : a.l2_policy == 2 ? l2_evict_last_policy()
+                                 : l2_evict_normal_policy();
+        kv = a.kv;
+        bt = a.bt;
+        num_blocks = a.num_blocks;
+        pool_bytes = a.pool_bytes;
+        pool32 = pool_bytes < (1ll << 31) - 1024;  // every byte offset fits in 31 bits
+        P = a.P;
+        W = a.W;
+        p_pow2 = (P & (P - 1)) == 0;
+        p_shift = __ffs(P) - 1;
+        status = a.status;
+        page_mode = a.page_mode != 0;
+        lane = lane_;
+        R = qd * 32u + lane;
+        stage = stage_addr;
+        // window mode: row R's 16-byte aligned window; page runs: the row itself
+        win = stage + (page_mode ? R * (uint32_t)kKvRowBytes : R * kWinBytes);
+        // operand row R is 128-byte aligned: chunk ch sits at opx ^ (ch << 4)
+        opx = (stage + kSlotBytes + R * 128u) ^ ((R & 7u) << 4);
+        wstage = stage + qd * 32u * kWinBytes;  // this warp's 32 windows
+        run_bar = run_bar_;
+        run_phase = 0;
+        // copy e = qq * 32 + lane of a warp's 288 window chunks: window e / 9,
+        // chunk e % 9; bit qq of last9 marks chunk 8 (the window's last)
+        last9 = 0;
+#pragma unroll
+        for (int qq = 0; qq < 9; ++qq)
+            last9 |= (((uint32_t)(qq * 32) + lane) % 9u == 8u ? 1u : 0u) << qq;
+    }
+
+    __device__ int page_of(int tok) const { return p_pow2 ? tok >> p_shift : tok / P; }
 
     // Block-table entry of this thread's row in tile p (-1 past the context).
-    auto table_entry = [&](const TilePos &p) -> int32_t {
+    __device__ int32_t table_entry(const TilePos &p) const
+    {
         const int tok = p.m * kTileTokens + (int)R;
-        return (p.nt > 0 && tok < p.ctx) ? __ldg(bt + (long long)p.i * W + page_of(tok)) : -1;
-    };
+        return (p.nt > 0 && tok >= p.tb && tok < p.te) ? __ldg(bt + (long long)p.i * W + page_of(tok))
+                                                        : -1;
+    }
+
     // Copies of this warp's 32 rows of tile p (this row's table entry b) into
     // the staging slot; returns the row's repack metadata: 4 | misalignment / 4
     // when the row is valid, else 0.
-    auto issue = [&](const TilePos &p, int32_t b) -> uint32_t {
+    __device__ uint32_t issue(const TilePos &p, int32_t b)
+    {
         const int t = p.m * kTileTokens + (int)R;
         bool v = false;
         long long o = 0;  // byte offset of the row in the pool
-        if (t < p.ctx) {
+        if (t >= p.tb && t < p.te) {
             if (b >= 0 && (long long)b < num_blocks) {
                 const int in_page = p_pow2 ? (t & (P - 1)) : t - page_of(t) * P;
                 o = ((long long)b * P + in_page) * kKvRowBytes;
@@ -509,29 +559,37 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             }
         }
         if (page_mode) {
-            // A run starts at a row whose position in its page is a multiple
-            // of 4 (the warp's first row, a page start, or the first row after
-            // a bad page), so it is 16-byte aligned in the pool and in the
-            // slot; its length is rounded up to whole 4-row groups of the same
-            // page, which lie in the pool, and stays inside the warp's 32 rows.
-            // Extra rows are masked.
+            // A run of consecutive valid rows moves as one bulk copy of whole
+            // 4-row groups: its start is rounded down, and its length up, to
+            // group boundaries. A group's 4 tokens are t = 4u .. 4u + 3 (the
+            // warp's rows start at a multiple of 32), so they sit in one page
+            // (P % 4 == 0) at in-page positions 4v .. 4v + 3: the copy is
+            // 16-byte aligned (4 rows = 528 bytes) in the pool and in the slot,
+            // reads only rows of the run's pages and stays inside the warp's
+            // 32 rows. Rows copied outside the run are masked. Runs start at
+            // the warp's first row, a page start, the first row after a bad
+            // page, or the first row of the request's scored slice; valid rows
+            // never resume inside a group once they stop, so runs do not share
+            // a group.
             const uint32_t tok = (uint32_t)(o / kKvRowBytes);
             const uint32_t vmask = __ballot_sync(kFullMask, v);
             const uint32_t tprev = __shfl_up_sync(kFullMask, tok, 1);
             const bool start = v && (lane == 0 || !((vmask >> (lane - 1)) & 1u) || tok != tprev + 1u);
             const uint32_t smask = __ballot_sync(kFullMask, start);
+            const uint32_t back = lane & 3u;  // rows from the group's first row
             uint32_t bytes = 0;
             if (start) {
                 const uint32_t later = lane == 31 ? 0u : (smask | ~vmask) & (~0u << (lane + 1));
                 const int end = later ? __ffs(later) - 1 : 32;
-                bytes = (uint32_t)(((end - lane) + 3) & ~3) * (uint32_t)kKvRowBytes;
+                bytes = (uint32_t)(((end - (int)(lane - back)) + 3) & ~3) * (uint32_t)kKvRowBytes;
             }
             const uint32_t total = __reduce_add_sync(kFullMask, bytes);
             if (lane == 0)
                 mbar_arrive_expect_tx(run_bar, total);
             __syncwarp();
             if (start)
-                bulk_load(stage + R * (uint32_t)kKvRowBytes, kv + o, bytes, run_bar);
+                bulk_load(stage + (R - back) * (uint32_t)kKvRowBytes, kv + (o - (long long)back * kKvRowBytes),
+                          bytes, run_bar);
             return v ? 4u : 0u;
         }
         // Window j of the warp starts at wstage + 144 j = wstage + 16 (9 j),
@@ -544,10 +602,10 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
         const uint32_t last = v ? (uint32_t)min(16ll, pool_bytes - (w0 + 128)) : 0u;
         const uint32_t ml = (v ? 0x100u : 0u) | last;
         if (pool32) {
-            const int wrel = (int)w0 - (int)kWinBytes * lane;
+            const int wrel = (int)w0 - (int)kWinBytes * (int)lane;
 #pragma unroll
             for (int qq = 0; qq < 9; ++qq) {
-                const uint32_t e = (uint32_t)(qq * 32 + lane);
+                const uint32_t e = (uint32_t)(qq * 32) + lane;
                 const int j = (int)((e * 7282u) >> 16);  // e / 9 for e < 288
                 const int wj = __shfl_sync(kFullMask, wrel, j);
                 const uint32_t mj = __shfl_sync(kFullMask, ml, j);
@@ -559,7 +617,7 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             const long long wrel = w0 - (long long)kWinBytes * lane;
 #pragma unroll
             for (int qq = 0; qq < 9; ++qq) {
-                const uint32_t e = (uint32_t)(qq * 32 + lane);
+                const uint32_t e = (uint32_t)(qq * 32) + lane;
                 const int j = (int)((e * 7282u) >> 16);
                 const long long wj = __shfl_sync(kFullMask, wrel, j);
                 const uint32_t mj = __shfl_sync(kFullMask, ml, j);
@@ -569,68 +627,28 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             }
         }
         return v ? 4u | ((uint32_t)(o >> 2) & 3u) : 0u;
-    };
+    }
 
-    // query slots: request n of the range sits in slot n % QS
-    int q_slot = 0;
-    uint32_t q_phase = 0;
-    bool have_q = false;  // the group has waited for the current request's query slot
-    int loads = 0;        // query loads issued (thread 0)
-    ReqWalk nxt;          // next request whose query is to be loaded (thread 0)
-    nxt.init(rc, c);
-    if (threadIdx.x == 0)
-        for (int n = 0; n < QS; ++n) {
-            if (nxt.valid(count)) {
-                load_query(a, smem, B, n, nxt.p.i);
-                ++loads;
-            }
-            nxt.advance(rc);
-        }
-    // Request ends passed: every group meets the others there in order, then
-    // thread 0 loads the query of the request QS ahead into the freed slot.
-    auto pass_ends = [&](int ends) {
-        for (int u = 0; u < ends; ++u) {
-            named_bar_sync(kCtaBarrier, kMaxThreads);
-            if (threadIdx.x == 0) {
-                if (nxt.valid(count) && !aborted(c)) {
-                    load_query(a, smem, B, q_slot, nxt.p.i);
-                    ++loads;
-                }
-                nxt.advance(rc);
-            }
-            if (++q_slot == QS) {
-                q_slot = 0;
-                q_phase ^= 1u;
-            }
-            have_q = false;
-        }
-    };
-
-    Walk w;  // the group's current tile
-    w.cur.init(rc, c);
-    w.kk = 0;
-    pass_ends(w.step(rc, g, count));
-    Walk nx = w;  // the group's next tile to gather
-    uint32_t meta = 0;
-    if (w.kk < count)
-        meta = issue(w.cur, table_entry(w.cur));
-    cp_async_commit();
-    nx.step(rc, kGroups, count);
-    int32_t b_nx = nx.kk < count ? table_entry(nx.cur) : -1;
-    uint32_t run_phase = 0, mma_phase = 0;
-
-    while (w.kk < count) {
-        // 1. the tile's rows have landed
+    // Wait until the rows of the tile in the staging slot have landed: window
+    // copies per thread, page runs on the warp's mbarrier.
+    __device__ bool wait_rows(const int *abort_flag)
+    {
         bool ok = true;
         if (page_mode) {
-            ok = mbar_wait(run_bar, run_phase, &c.abort);
+            ok = mbar_wait(run_bar, run_phase, abort_flag);
             run_phase ^= 1u;
         } else {
             cp_async_wait_group<0>();
         }
         __syncwarp();
-        // 2. repack row R into the operand; scale -> register. Rows past the
-        // context keep whatever the slot holds: their scores are masked.
+        return ok;
+    }
+
+    // Repack row R into the operand; returns its scale (0 for an invalid row).
+    // Rows past the context keep whatever the slot holds: their scores are
+    // masked.
+    __device__ float repack(uint32_t meta) const
+    {
         float sc;
         if (page_mode) {
             // rows 132 bytes apart: word k of the 32 lanes' rows sits in bank
@@ -664,40 +682,175 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             sc = (meta & 4u) ? __uint_as_float(wv[32]) : 0.0f;
         }
         __syncwarp();  // every lane has read its row before the slot is refilled
+        return sc;
+    }
+};
+
+// Query slots. Request n of the CTA's range (counting only requests with
+// tokens) sits in slot n % QS; at each request end every warpgroup meets the
+// others (a CTA barrier), then thread 0 loads the query of the request QS
+// ahead into the slot just freed.
+struct QuerySlots {
+    int ord;     // request ends this warpgroup has passed = ordinal of its current request
+    bool have;   // the warpgroup has waited for its current request's slot
+    int loads;   // query loads issued (thread 0)
+    ReqWalk nxt; // next request whose query is to be loaded (thread 0)
+
+    __device__ void init(const MainArgs &a, uint8_t *smem, const Bars &B, const ReqCtx &rc,
+                         const CtaCtl &c, int count)
+    {
+        ord = 0;
+        have = false;
+        loads = 0;
+        nxt.init(rc, c);
+        if (threadIdx.x == 0)
+            for (int n = 0; n < a.QS; ++n) {
+                if (nxt.valid(count)) {
+                    load_query(a, smem, B, n, nxt.p.i);
+                    ++loads;
+                }
+                nxt.advance(rc);
+            }
+    }
+    __device__ void pass_ends(const MainArgs &a, uint8_t *smem, const Bars &B, const ReqCtx &rc,
+                              const CtaCtl &c, int count, int ends)
+    {
+        for (int u = 0; u < ends; ++u) {
+            named_bar_sync(kCtaBarrier, kMaxThreads);
+            if (threadIdx.x == 0) {
+                if (nxt.valid(count) && !aborted(c)) {
+                    load_query(a, smem, B, ord % a.QS, nxt.p.i);
+                    ++loads;
+                }
+                nxt.advance(rc);
+            }
+            ++ord;
+            have = false;
+        }
+    }
+    __device__ int slot(int n, int QS) const { return n % QS; }
+    __device__ uint32_t phase(int n, int QS) const { return (uint32_t)(n / QS) & 1u; }
+    // after an abort, query loads nobody consumed land before the CTA exits (bounded)
+    __device__ void drain(const Bars &B, int QS) const
+    {
+        if (threadIdx.x == 0)
+            for (int u = loads > QS ? loads - QS : 0; u < loads; ++u)
+                mbar_wait(&B.qfull[u % QS], (uint32_t)(u / QS) & 1u, nullptr);
+    }
+};
+
+// The epilogue's output of one token for draft row j: the full logits row
+// and/or the compact logits plus the row's key histogram.
+struct TokenOut {
+    float *logits, *clogits;
+    uint32_t *hrow;
+    long long obase, mml;
+    int t, lim0;
+    bool in_slice;  // t inside the request's scored tokens [tb, te)
+    uint64_t keep_pol;
+    __device__ void operator()(int j, float lj) const
+    {
+        const bool vj = in_slice && t < lim0 + j;
+        const long long o = obase + (long long)j * mml;
+        if (logits && t < mml)
+            logits[o] = vj ? lj : -__int_as_float(0x7f800000);
+        if (clogits && vj)
+            st_global_hint(clogits + o, lj, keep_pol);
+        if (hrow && vj)
+            atomicAdd(hrow + j * kHistBins + (f32_order_key(lj) >> kHistShift), 1u);
+    }
+};
+
+__device__ __forceinline__ TokenOut token_out(const MainArgs &a, const TilePos &it, uint32_t R,
+                                              uint64_t keep_pol)
+{
+    TokenOut o;
+    o.logits = a.logits;
+    o.clogits = a.clogits;
+    o.mml = a.mml;
+    o.t = it.m * kTileTokens + (int)R;
+    o.lim0 = it.ctx - a.nn + 1;  // draft row j admits t < lim0 + j
+    o.in_slice = o.t >= it.tb && o.t < it.te;
+    o.obase = (long long)it.i * a.nn * o.mml + o.t;
+    o.hrow = a.hist ? a.hist + (long long)it.i * a.nn * kHistBins : nullptr;
+    o.keep_pol = keep_pol;
+    return o;
+}
+
+// Warpgroup g, warp quadrant qd (warp % 4): CTA tiles g, g + 4, g + 8, ...,
+// each carried through every step by this warpgroup alone. Shared memory is
+// addressed through 32-bit shared addresses throughout.
+template <int H>
+static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int g, int qd)
+{
+    const Bars B(a, smem);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t R = (uint32_t)(qd * 32 + lane);  // tile row = TMEM lane
+    const bool elected = qd == 0 && lane == 0;
+    const uint32_t wg_bar = 1u + (uint32_t)g;
+    const int count = (int)c.count;
+    const uint32_t tmem_base = c.tmem_base;
+    const int N = a.N, nn = a.nn, QS = a.QS;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t stage = sbase + a.off_grp + (uint32_t)g * kGroupBytes;
+    TileGather G;
+    G.init(a, stage, (uint32_t)qd, (uint32_t)lane, &B.run[warp]);
+    const uint32_t w_base = sbase + a.off_w;
+    const uint32_t w_slot_bytes = (uint32_t)N * 4u;
+    // TMEM: this warp's lane quadrant, the group's columns
+    const uint32_t dcol = tmem_base + (uint32_t)(g * a.cols);
+    const uint32_t tacc = dcol + ((uint32_t)(qd * 32) << 16);
+    // MMA operands; passes of at most 128 accumulator columns (whole draft rows)
+    const uint64_t adesc = sw128_kmajor_desc(stage + kSlotBytes);
+    const uint64_t bdesc0 = sw128_kmajor_desc(sbase + a.off_q);
+    const uint32_t q_units = (uint32_t)N * kHeadDim >> 4;
+    constexpr int kRpp = kPassCols / H < kMaxRows ? kPassCols / H : kMaxRows;  // rows per pass
+    const int npass = (nn + kRpp - 1) / kRpp;
+    const uint64_t keep_pol = l2_evict_last_policy();
+
+    ReqCtx rc;
+    rc.init(a, c);
+    QuerySlots qs;
+    qs.init(a, smem, B, rc, c, count);
+
+    Walk w;  // the group's current tile
+    w.cur.init(rc, c);
+    w.kk = 0;
+    qs.pass_ends(a, smem, B, rc, c, count, w.step(rc, g, count));
+    Walk nx = w;  // the group's next tile to gather
+    uint32_t meta = 0;
+    if (w.kk < count)
+        meta = G.issue(w.cur, G.table_entry(w.cur));
+    cp_async_commit();
+    nx.step(rc, kGroups, count);
+    int32_t b_nx = nx.kk < count ? G.table_entry(nx.cur) : -1;
+    uint32_t mma_phase = 0;
+
+    while (w.kk < count) {
+        // 1. the tile's rows have landed; 2. repack row R, scale -> register
+        bool ok = G.wait_rows(&c.abort);
+        const float sc = G.repack(meta);
         // 3. the group's next tile: copies now, table entries of the one after
         if (nx.kk < count)
-            meta = issue(nx.cur, b_nx);
+            meta = G.issue(nx.cur, b_nx);
         cp_async_commit();
         nx.step(rc, kGroups, count);
-        b_nx = nx.kk < count ? table_entry(nx.cur) : -1;
+        b_nx = nx.kk < count ? G.table_entry(nx.cur) : -1;
         // operand visible to the tensor core; the previous tile's TMEM reads done
         fence_proxy_async_smem();
         tc_fence_before_sync();
         named_bar_sync(wg_bar, 128);
         tc_fence_after_sync();
-        if (!have_q) {
-            ok = mbar_wait(&B.qfull[q_slot], q_phase, &c.abort) && ok;
-            have_q = true;
+        const int q_slot = qs.slot(qs.ord, QS);
+        if (!qs.have) {
+            ok = mbar_wait(&B.qfull[q_slot], qs.phase(qs.ord, QS), &c.abort) && ok;
+            qs.have = true;
         }
         // weights of the request: valid after the query-slot wait above
         const uint32_t wsl = launder_u32(w_base + (uint32_t)q_slot * w_slot_bytes);
-        const TilePos &it = w.cur;
-        const int t = it.m * kTileTokens + (int)R;
-        const int lim0 = it.ctx - nn + 1;  // draft row j admits t < lim0 + j
-        const long long obase = (long long)it.i * nn * mml + t;
-        uint32_t *const hrow = hist ? hist + (long long)it.i * nn * kHistBins : nullptr;
+        const TokenOut out = token_out(a, w.cur, R, keep_pol);
         const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
         const float mag = fabsf(sc);
-        auto out = [&](int j, float lj) {
-            const bool vj = t < lim0 + j;
-            const long long o = obase + (long long)j * mml;
-            if (logits && t < mml)
-                logits[o] = vj ? lj : NEG_INF;
-            if (clogits && vj)
-                st_global_hint(clogits + o, lj, keep_pol);
-            if (hrow && vj)
-                atomicAdd(hrow + j * kHistBins + (f32_order_key(lj) >> kHistShift), 1u);
-        };
         const bool all_pos = __all_sync(kFullMask, flip == 0u);
         for (int p = 0; p < npass; ++p) {
             const int j0 = p * kRpp, nr = min(kRpp, nn - j0);
@@ -731,98 +884,10 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
                 tc_fence_after_sync();
             }
         }
-        pass_ends(w.step(rc, kGroups, count));
+        qs.pass_ends(a, smem, B, rc, c, count, w.step(rc, kGroups, count));
     }
     cp_async_wait_all();
-    // after an abort, query loads nobody consumed land before the CTA exits (bounded)
-    if (threadIdx.x == 0)
-        for (int u = loads > QS ? loads - QS : 0; u < loads; ++u)
-            mbar_wait(&B.qfull[u % QS], (uint32_t)(u / QS) & 1u, nullptr);
-}
-
-// ---------------------------------------------------------------- kernel
-
-static_assert(kMaxThreads <= 32 * 32, "CtaCtl holds per-warp sums for at most 32 warps");
-
-template <int H>
-__global__ void __launch_bounds__(kMaxThreads, 1)
-    pmqa_main_kernel(const __grid_constant__ MainArgs a)
-{
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ CtaCtl ctl;
-    // 1024-byte aligned (128B-swizzled operands); pointer arithmetic on the
-    // shared array keeps the pointer in the shared address space
-    uint8_t *const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // the selection launched after this kernel may start launching now; it
-    // waits for this grid's completion before it reads anything
-    griddep_launch_dependents();
-    if (threadIdx.x == 0) {
-        ctl.abort = 0;
-        const Bars B(a, smem);
-        for (int q = 0; q < a.QS; ++q)
-            mbar_init(&B.qfull[q], 1);
-        for (int g = 0; g < kGroups; ++g)
-            mbar_init(&B.mma[g], 1);
-        for (int w = 0; w < kNumWarps; ++w)
-            mbar_init(&B.run[w], 1);
-        mbar_init_fence();
-    }
-    __syncwarp();
-    if (warp == 0)
-        tmem_alloc(&ctl.tmem_base, (uint32_t)a.tmem_cols);
-
-    balance_schedule(
-        a.bs, [&](int i) { return (long long)((ctx_of(a, i) + kTileTokens - 1) / kTileTokens); },
-        ctl);
-    for (int n = threadIdx.x; n < kCtxCache; n += blockDim.x)
-        ctl.ctx[n] = ctl.i0 + n < a.bs ? ctx_of(a, ctl.i0 + n) : 0;
-    if (blockIdx.x == 0) {
-        const long long lim = min((long long)a.mml, (long long)a.W * a.P);
-        for (int i = threadIdx.x; i < a.bs; i += blockDim.x) {
-            const int cx = __ldg(a.ctx_lens + i);
-            if (cx < 0 || cx > lim)
-                atomicOr(a.status, 0x2u);
-        }
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-
-    // -inf beyond the last tile of each row: this CTA's share of every row.
-    // Each warp takes 32 rows at a time (one coalesced load of their context
-    // lengths), then writes the rows' shares one after another.
-    if (a.logits) {
-        const int rows = a.bs * a.nn;
-        const long long mml = a.mml;
-        const float NEG_INF = -__int_as_float(0x7f800000);
-        for (int base = warp * 32; base < rows; base += kMaxThreads) {
-            const int my_row = base + lane;
-            const int my_cx = my_row < rows ? ctx_of(a, my_row / a.nn) : 0;
-            const int nr = min(32, rows - base);
-            for (int u = 0; u < nr; ++u) {
-                const int cx = __shfl_sync(kFullMask, my_cx, u);
-                const long long lo =
-                    min((long long)(cx + kTileTokens - 1) / kTileTokens * kTileTokens, mml);
-                const long long L = mml - lo;
-                const long long s0 = lo + L * blockIdx.x / gridDim.x;
-                const long long s1 = lo + L * (blockIdx.x + 1) / gridDim.x;
-                float *row = a.logits + (long long)(base + u) * mml;
-                for (long long t = s0 + lane; t < s1; t += 32)
-                    row[t] = NEG_INF;
-            }
-        }
-    }
-
-    group_role<H>(a, smem, ctl, warp >> 2, warp & 3);
-
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    __syncwarp();
-    if (warp == 0)
-        tmem_dealloc(ctl.tmem_base, (uint32_t)a.tmem_cols);
+    qs.drain(B, QS);
 }
 
 }  // namespace pmqa

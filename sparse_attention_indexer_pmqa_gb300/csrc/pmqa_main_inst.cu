@@ -3,7 +3,7 @@
 // -DPMQA_HEADS=16, 32, 64 or 128.
 #include <cuda_runtime.h>
 
-#include "pmqa_main.cuh"
+#include "pmqa_kernel.cuh"
 
 #ifndef PMQA_HEADS
 #error "PMQA_HEADS must be defined"

@@ -114,15 +114,6 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ float4 lds128f(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
 // Non-volatile: for data that stays fixed while it is read (the weights of a
 // request). The compiler may schedule these loads freely between the
 // statements that order them: derive the address from launder_u32 after the
@@ -169,28 +160,6 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy()
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
-}
-
-// 4-byte asynchronous copy global -> shared; src_bytes 0 zero-fills without reading.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes,
-                                           uint64_t policy)
-{
-    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2, %3;" ::"r"(dst),
-                 "l"(src), "r"(src_bytes), "l"(policy)
-                 : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned).
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, uint64_t policy)
-{
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
-                 "l"(src), "l"(policy)
-                 : "memory");
 }
 
 // 16-byte asynchronous copy that reads only the first src_bytes (1..16) bytes of
@@ -292,14 +261,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 __device__ __forceinline__ void st_global_hint(float *p, float v, uint64_t policy)
 {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy)
-                 : "memory");
-}
-
-// Arrive on the mbarrier once all of this thread's prior cp.async copies have
-// landed (the barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
 
@@ -411,18 +372,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r)
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-}
-
-// Wait for this thread's outstanding TMEM loads. The registers are passed
-// through the statement so that no use of them is scheduled before it.
-__device__ __forceinline__ void tmem_ld_wait16(uint32_t *r)
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
 }
 
 // No memory clobber: the wait orders TMEM loads only (their destination

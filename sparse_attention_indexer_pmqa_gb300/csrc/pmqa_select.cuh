@@ -29,6 +29,7 @@ struct SelectArgs {
     int bs, nn, mml, k;
     int ctx_lim;        // contexts are clamped to [0, ctx_lim]: the KV pass's limit
                         // min(mml, P * max_blocks_per_seq) on the fused path, mml alone
+    const int32_t *tok_begin, *tok_end;  // a slice of each request's tokens, or null
     int32_t *idx;       // [rows, k]
     float *vals;        // [rows, k] or null
     uint32_t *hist;     // [rows, 2048]
@@ -44,10 +45,21 @@ struct SelectArgs {
 constexpr int kSelThreads = 256;
 constexpr int kSelPer = 16;  // positions per thread: one CTA covers 256 * 16 = 4096
 
-__device__ __forceinline__ int sel_valid_len(const SelectArgs &a, int row)
+// Positions [lo, hi) that row `row` selects from: the admitted positions
+// t < valid_len, inside its request's slice [tok_begin, tok_end) when one is
+// given (the clamps of the KV pass).
+__device__ __forceinline__ void sel_window(const SelectArgs &a, int row, int &lo, int &hi)
 {
-    const int c = clamp_ctx(__ldg(a.ctx_lens + row / a.nn), (long long)a.ctx_lim);
-    return valid_len(c, a.nn, row % a.nn);
+    const int i = row / a.nn;
+    const int c = clamp_ctx(__ldg(a.ctx_lens + i), (long long)a.ctx_lim);
+    hi = valid_len(c, a.nn, row % a.nn);
+    lo = 0;
+    if (a.tok_begin) {
+        const int tb = clamp_ctx(__ldg(a.tok_begin + i), (long long)c);
+        const int te = max(tb, clamp_ctx(__ldg(a.tok_end + i), (long long)c));
+        lo = tb;
+        hi = max(tb, min(hi, te));
+    }
 }
 
 // Per-row histogram of the top 11 bits of the order keys (stand-alone top-k).
@@ -55,7 +67,9 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_hist_kernel(const __grid_con
 {
     __shared__ uint32_t h[kHistBins];
     const int row = blockIdx.y;
-    const int n = sel_valid_len(a, row);
+    int lo, hi;
+    sel_window(a, row, lo, hi);
+    const int n = hi - lo;
     const long long t0 = (long long)blockIdx.x * a.chunk;
     const long long t1 = min(t0 + a.chunk, (long long)n);
     if (t0 >= t1)
@@ -63,7 +77,7 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_hist_kernel(const __grid_con
     for (int e = threadIdx.x; e < kHistBins; e += kSelThreads)
         h[e] = 0;
     __syncthreads();
-    const float *src = a.logits + (long long)row * a.mml;
+    const float *src = a.logits + (long long)row * a.mml + lo;
     // all of this CTA's loads in flight first, then plain shared atomics
     float v[kSelPer];
 #pragma unroll
@@ -186,10 +200,12 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     // launched as a dependent of the KV pass: its logits and histograms are
     // complete and visible after this
     griddep_wait();
-    const int n = sel_valid_len(a, row);
+    int lo, hi;
+    sel_window(a, row, lo, hi);
+    const int n = hi - lo;  // positions lo + t, 0 <= t < n
     const uint32_t keff = (uint32_t)min(a.k, n);
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const long long rbase = (long long)row * a.mml;
+    const long long rbase = (long long)row * a.mml + lo;
     int32_t *orow = a.idx + (long long)row * a.k;
     float *vrow = a.vals ? a.vals + (long long)row * a.k : nullptr;
     uint32_t *const status = a.status;
@@ -265,12 +281,12 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
         // its winners (and candidates) of each u as one contiguous run
         uint32_t o_sel = s.base_sel + s.wsel[wid], o_tie = s.base_tie + s.wtie[wid];
         const uint32_t lt = (1u << lane) - 1u;
-        uint2 *const trow = a.ties + rbase;
+        uint2 *const trow = a.ties + (long long)row * a.mml;
 #pragma unroll
         for (int u = 0; u < kSelPer; ++u) {
             const bool is_sel = (msel >> u) & 1u, is_tie = (mtie >> u) & 1u;
             const uint32_t bs = __ballot_sync(kFullMask, is_sel), bt = __ballot_sync(kFullMask, is_tie);
-            const int32_t t = (int32_t)(t0 + u * kSelThreads + tid);
+            const int32_t t = (int32_t)(lo + t0 + u * kSelThreads + tid);
             if (is_sel) {
                 const uint32_t o = o_sel + __popc(bs & lt);
                 if (o < keff) {
@@ -304,7 +320,7 @@ __global__ void __launch_bounds__(kSelThreads) pmqa_select_kernel(const __grid_c
     const uint32_t above = s.above;
     const uint32_t need = keff > above ? keff - above : 0u;
     const uint32_t ntie_row = keff > 0 ? min(__ldcg(a.tie_cnt + row), (uint32_t)a.mml) : 0u;
-    const uint2 *tl = a.ties + rbase;
+    const uint2 *tl = a.ties + (long long)row * a.mml;
     if (keff > 0 && __ldcg(a.sel_cnt + row) != above)
         atomicOr(status, 0x8u);
     if (need >= ntie_row) {
@@ -511,16 +527,19 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
     // launched as a dependent of the KV pass: its logits and histograms are
     // complete and visible after this
     griddep_wait();
-    const int n = min(sel_valid_len(a, row), PER * kRowThreads);
+    int lo, hi;
+    sel_window(a, row, lo, hi);
+    const int n = min(hi - lo, PER * kRowThreads);  // positions lo + t, 0 <= t < n
     const uint32_t keff = (uint32_t)min(a.k, n);
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const long long rbase = (long long)row * a.mml;
+    const long long rbase = (long long)row * a.mml + lo;
     int32_t *orow = a.idx + (long long)row * a.k;
     float *vrow = a.vals ? a.vals + (long long)row * a.k : nullptr;
     uint32_t *const status = a.status;
 
     // the row by bulk copy when it is 16-byte aligned (every row is when the
-    // logits are and max_model_len is a multiple of 4), else by plain loads
+    // logits are, max_model_len is a multiple of 4 and so is lo), else by
+    // plain loads; a copy rounded up to 16 bytes stays inside the row
     const float *src = a.logits + rbase;
     const bool bulk = keff > 0 && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && (a.mml % 4 == 0);
     // copy positions [c * kRowMaxLen, ...) of the row into sv (thread 0)
@@ -637,11 +656,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
         // candidates stay in shared memory when they fit, else go to the
         // row's list in the workspace
         const bool cached = tot_t <= (uint32_t)kTieCap;
-        uint2 *const tl = a.ties + rbase;
+        uint2 *const tl = a.ties + (long long)row * a.mml;
         for (uint64_t m = msel; m; m &= m - 1) {
             const int t = tid + (__ffsll((long long)m) - 1) * kRowThreads;
             if (o_s < keff) {
-                orow[o_s] = t;
+                orow[o_s] = lo + t;
                 if (vrow)
                     vrow[o_s] = val(t);
             } else {
@@ -653,10 +672,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
             const int t = tid + (__ffsll((long long)m) - 1) * kRowThreads;
             const uint32_t key = f32_order_key(val(t));
             if (cached) {
-                s.tpos[o_t] = t;
+                s.tpos[o_t] = lo + t;
                 s.tkey[o_t] = key;
             } else {
-                tl[o_t] = make_uint2((uint32_t)t, key);
+                tl[o_t] = make_uint2((uint32_t)(lo + t), key);
             }
             ++o_t;
         }
@@ -734,6 +753,156 @@ __global__ void __launch_bounds__(kRowThreads, 1) pmqa_select_row_kernel(const _
     // happened before the first row_find_bin's barriers)
     for (int e = tid; e < kHistBins; e += kRowThreads)
         a.hist[(long long)row * kHistBins + e] = 0;
+}
+
+}  // namespace pmqa
+
+namespace pmqa {
+
+// ---------------------------------------------------------------- merge of shard lists
+
+// Candidate lists of a context-parallel split (section 8 of the scope: each
+// GPU holds a slice of every request's tokens, keeps its slice's top-k as
+// (position, logit) pairs, and the lists are gathered and merged): the top-k
+// of the union of `lists` lists per row. Each global top-k position is in its
+// slice's top-k, so the union's top-k is the row's top-k.
+struct MergeArgs {
+    const int32_t *idx;  // [lists, rows, k_in], -1 for an empty slot
+    const float *vals;   // [lists, rows, k_in]
+    int lists, rows, k_in, k;
+    int32_t *out_idx;    // [rows, k]
+    float *out_vals;     // [rows, k] or null
+};
+
+// One CTA per row: a histogram of the valid candidates' top 11 key bits, the
+// boundary bin, one pass that writes the winners and sets the boundary bin's
+// candidates aside, and those resolved with two more digits.
+__global__ void __launch_bounds__(kSelThreads) pmqa_merge_kernel(const __grid_constant__ MergeArgs a)
+{
+    __shared__ SelShared s;
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const long long n = (long long)a.lists * a.k_in;
+    int32_t *orow = a.out_idx + (long long)row * a.k;
+    float *vrow = a.out_vals ? a.out_vals + (long long)row * a.k : nullptr;
+    // candidate e of the row: slot e % k_in of list e / k_in
+    auto load = [&](long long e, int32_t &pos, uint32_t &key) -> bool {
+        const long long l = e / a.k_in, c = e - l * a.k_in;
+        const long long o = (l * a.rows + row) * a.k_in + c;
+        pos = __ldg(a.idx + o);
+        key = pos >= 0 ? f32_order_key(__ldg(a.vals + o)) : 0u;
+        return pos >= 0;
+    };
+    for (int e = tid; e < kHistBins; e += kSelThreads)
+        s.h[e] = 0;
+    __syncthreads();
+    uint32_t cnt = 0;
+    for (long long e = tid; e < n; e += kSelThreads) {
+        int32_t pos;
+        uint32_t key;
+        if (load(e, pos, key)) {
+            atomicAdd(&s.h[key >> kHistShift], 1u);
+            ++cnt;
+        }
+    }
+    uint32_t total;
+    cta_exclusive_scan(s, cnt, &total);
+    __syncthreads();
+    const uint32_t keff = min((uint32_t)a.k, total);
+    if (keff > 0) {
+        find_bin(s, s.h, kHistBins, keff);
+        const uint32_t bstar = s.digit, above = s.above2;
+        if (tid == 0) {
+            s.base_sel = 0;  // output cursor
+            s.base_tie = 0;  // candidates of the boundary bin
+        }
+        __syncthreads();
+        for (long long e = tid; e < n; e += kSelThreads) {
+            int32_t pos;
+            uint32_t key;
+            if (!load(e, pos, key))
+                continue;
+            const uint32_t bin = key >> kHistShift;
+            if (bin > bstar) {
+                const uint32_t o = atomicAdd(&s.base_sel, 1u);
+                if (o < keff) {
+                    orow[o] = pos;
+                    if (vrow)
+                        vrow[o] = f32_from_order_key(key);
+                }
+            } else if (bin == bstar) {
+                const uint32_t q = atomicAdd(&s.base_tie, 1u);
+                if (q < (uint32_t)kTieCap) {
+                    s.tpos[q] = pos;
+                    s.tkey[q] = key;
+                }
+            }
+        }
+        __syncthreads();
+        const uint32_t need = keff > above ? keff - above : 0u;
+        const uint32_t ntie = s.base_tie;
+        const bool cached = ntie <= (uint32_t)kTieCap;
+        // the boundary bin's candidates: from shared memory, or the lists again
+        auto each_tie = [&](auto &&fn) {
+            if (cached) {
+                for (uint32_t e = tid; e < ntie; e += kSelThreads)
+                    fn(s.tpos[e], s.tkey[e]);
+            } else {
+                for (long long e = tid; e < n; e += kSelThreads) {
+                    int32_t pos;
+                    uint32_t key;
+                    if (load(e, pos, key) && (key >> kHistShift) == bstar)
+                        fn(pos, key);
+                }
+            }
+        };
+        auto emit = [&](int32_t pos, uint32_t key) {
+            const uint32_t o = atomicAdd(&s.base_sel, 1u);
+            if (o < keff) {
+                orow[o] = pos;
+                if (vrow)
+                    vrow[o] = f32_from_order_key(key);
+            }
+        };
+        if (need >= ntie) {
+            each_tie(emit);
+        } else if (need > 0) {
+            for (int e = tid; e < kHistBins; e += kSelThreads)
+                s.h[e] = 0;
+            __syncthreads();
+            each_tie([&](int32_t, uint32_t key) { atomicAdd(&s.h[(key >> 10) & 2047u], 1u); });
+            __syncthreads();
+            find_bin(s, s.h, kHistBins, need);
+            const uint32_t d2 = s.digit, need2 = need - s.above2;
+            __syncthreads();
+            for (int e = tid; e < 1024; e += kSelThreads)
+                s.h[e] = 0;
+            __syncthreads();
+            each_tie([&](int32_t, uint32_t key) {
+                if (((key >> 10) & 2047u) == d2)
+                    atomicAdd(&s.h[key & 1023u], 1u);
+            });
+            __syncthreads();
+            find_bin(s, s.h, 1024, need2);
+            const uint32_t T = (bstar << kHistShift) | (d2 << 10) | s.digit;  // the k-th largest key
+            const uint32_t eq_need = need2 - s.above2;
+            if (tid == 0)
+                s.eq_taken = 0;
+            __syncthreads();
+            each_tie([&](int32_t pos, uint32_t key) {
+                bool take = key > T;
+                if (key == T)
+                    take = atomicAdd(&s.eq_taken, 1u) < eq_need;
+                if (take)
+                    emit(pos, key);
+            });
+        }
+    }
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    for (int e = (int)keff + tid; e < a.k; e += kSelThreads) {
+        orow[e] = -1;
+        if (vrow)
+            vrow[e] = NEG_INF;
+    }
 }
 
 }  // namespace pmqa

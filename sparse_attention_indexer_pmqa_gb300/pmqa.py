@@ -36,7 +36,8 @@ PMQA_STAGE_SELECT = 2
 EXPORTED = (
     "pmqa_workspace_bytes", "pmqa_workspace_init", "pmqa_logits", "pmqa_topk",
     "pmqa_logits_topk", "pmqa_logits_topk_stages", "pmqa_logits_topk_noalloc",
-    "pmqa_mqa_logits", "pmqa_read_device_status",
+    "pmqa_logits_topk_range",
+    "pmqa_mqa_logits", "pmqa_topk_merge", "pmqa_read_device_status",
     "pmqa_status_string", "pmqa_version",
 )
 
@@ -112,7 +113,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pmqa_logits_topk": ([PP, I32, V, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_logits_topk_stages": ([PP, I32, V, V, V, V, SZ, V, I32], ctypes.c_int),
         "pmqa_logits_topk_noalloc": ([PP, I32, V, V, V, V], ctypes.c_int),
+        "pmqa_logits_topk_range": ([PP, V, V, I32, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_mqa_logits": ([PM, V, V, SZ, V], ctypes.c_int),
+        "pmqa_topk_merge": ([V, V, I32, I32, I32, I32, V, V, V], ctypes.c_int),
         "pmqa_read_device_status": ([V, V], ctypes.c_int),
         "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pmqa_version": ([], ctypes.c_int),
@@ -259,6 +262,29 @@ def pmqa_logits_topk_noalloc(q, kv_cache, weights, context_lens, block_tables,
     return idx
 
 
+def pmqa_logits_topk_range(q, kv_cache, weights, context_lens, block_tables, max_model_len: int,
+                           k: int, token_begin, token_end, *, idx=None, vals=None,
+                           want_vals: bool = False, ws=None, stream=None):
+    """The fused call on the slice [token_begin[i], token_end[i]) of each
+    request's tokens; positions in idx are the requests' own (global) ones."""
+    import torch
+
+    p = make_problem(q, kv_cache, weights, context_lens, block_tables, max_model_len)
+    rows = p.bs * p.next_n
+    for t in (token_begin, token_end):
+        assert t.is_cuda and t.is_contiguous() and t.dtype == torch.int32 and t.numel() == p.bs
+    if idx is None:
+        idx = torch.empty((rows, k), dtype=torch.int32, device=q.device)
+    if vals is None and want_vals:
+        vals = torch.empty((rows, k), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(p.bs, p.next_n, max_model_len, k, PMQA_OP_LOGITS_TOPK, q.device, stream)
+    _check(load().pmqa_logits_topk_range(ctypes.byref(p), _ptr(token_begin), _ptr(token_end), k,
+                                         _ptr(idx), _ptr(vals), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "pmqa_logits_topk_range")
+    return (idx, vals) if want_vals or vals is not None else idx
+
+
 def make_mqa_problem(q, k, k_scale, weights, ks, ke) -> MqaProblem:
     """Fill a pmqa_mqa_problem from tensors shaped as in the C header."""
     m, heads, head_dim = q.shape
@@ -283,6 +309,23 @@ def pmqa_mqa_logits(q, k, k_scale, weights, ks, ke, *, out=None, ws=None, stream
     _check(load().pmqa_mqa_logits(ctypes.byref(p), _ptr(out), _ptr(ws), ws.numel(),
                                   _stream(stream)), "pmqa_mqa_logits")
     return out
+
+
+def pmqa_topk_merge(idx, vals, k: int, *, out_idx=None, out_vals=None, want_vals: bool = False,
+                    stream=None):
+    """Top-k per row of the union of candidate lists idx/vals [lists, rows, k_in]
+    (-1 marks an empty slot); returns out_idx [rows, k] (and out_vals)."""
+    import torch
+
+    lists, rows, k_in = idx.shape
+    assert vals.shape == idx.shape and idx.is_contiguous() and vals.is_contiguous()
+    if out_idx is None:
+        out_idx = torch.empty((rows, k), dtype=torch.int32, device=idx.device)
+    if out_vals is None and want_vals:
+        out_vals = torch.empty((rows, k), dtype=torch.float32, device=idx.device)
+    _check(load().pmqa_topk_merge(_ptr(idx), _ptr(vals), lists, rows, k_in, k, _ptr(out_idx),
+                                  _ptr(out_vals), _stream(stream)), "pmqa_topk_merge")
+    return (out_idx, out_vals) if want_vals or out_vals is not None else out_idx
 
 
 def pmqa_read_device_status(ws, stream=None) -> int:

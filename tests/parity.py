@@ -36,21 +36,28 @@ def check_logits(gpu: np.ndarray, ref: np.ndarray, tol: np.ndarray) -> float:
 
 
 def check_topk_rows(idx: np.ndarray, ref64: np.ndarray, tol: np.ndarray, ctx, nn: int, k: int,
-                    vals: np.ndarray | None = None) -> int:
-    """Check GPU top-k against oracle values; returns the number of tie swaps."""
+                    vals: np.ndarray | None = None, begin=None, end=None) -> int:
+    """Check GPU top-k against oracle values; returns the number of tie swaps.
+    With begin/end (per request) the rows choose only among the admitted
+    positions inside [begin_i, end_i)."""
     ctx = np.asarray(ctx)
     swaps = 0
     for r in range(idx.shape[0]):
         i, j = divmod(r, nn)
         n = valid_len(int(ctx[i]), nn, j)
-        ke = min(k, n)
+        lo = 0
+        if begin is not None:
+            lo = min(max(int(begin[i]), 0), int(ctx[i]))
+            n = max(lo, min(n, max(lo, min(int(end[i]), int(ctx[i])))))
+        ke = min(k, n - lo)
         sel = idx[r, :ke]
         assert np.all(idx[r, ke:] == -1), f"row {r}: slots past k_eff not -1"
-        assert np.all((sel >= 0) & (sel < n)), f"row {r}: position outside the window"
+        assert np.all((sel >= lo) & (sel < n)), f"row {r}: position outside the window"
         assert len(np.unique(sel)) == ke, f"row {r}: repeated positions"
         if ke == 0:
             continue
-        row = ref64[r, :n]
+        row = np.full(n, -np.inf)
+        row[lo:n] = ref64[r, lo:n]
         order = np.lexsort((np.arange(n), -row))
         ref_set = order[:ke]
         kth = row[ref_set[-1]]

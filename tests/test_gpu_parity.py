@@ -269,6 +269,23 @@ def test_context_longer_than_max_model_len_is_flagged(cuda_lib):
     assert cuda_lib.pmqa_read_device_status(ws) & cuda_lib.PMQA_DEV_BAD_CONTEXT
 
 
+@pytest.mark.parametrize("k", [100, 2048, 3000])
+def test_fused_topk_with_every_logit_equal(cuda_lib, k):
+    """Zero weights make every admitted logit exactly 0: the whole row sits in
+    one key bin, more candidates than the selection keeps in shared memory,
+    and any k_eff of them are a correct answer."""
+    prob = make_problem(3, 2, 64, 16, [5000, 2100, 130], 5120, seed=5, table="perm",
+                        extra_blocks=2)
+    prob.weights[:] = 0.0
+    ref, r64, tol = oracle_all(prob)
+    for ws in (None, cuda_lib.workspace(3, 2, 5120, k, cuda_lib.PMQA_OP_LOGITS_TOPK)):
+        idx, vals = gpu_fused(cuda_lib, prob, k, ws=ws)
+        check_topk_rows(idx, r64, tol, prob.context_lens, prob.next_n, k, vals=vals)
+        assert np.all(vals[idx >= 0] == 0.0)
+        if ws is not None:
+            assert cuda_lib.pmqa_read_device_status(ws) == 0
+
+
 def test_context_beyond_the_block_table_is_clamped_in_the_fused_call(cuda_lib):
     """A context longer than block_size * max_blocks_per_seq (but within
     max_model_len): the KV pass and the selection clamp it to the table's reach
