@@ -11,7 +11,7 @@ namespace pmqa {
 
 static_assert(kMaxThreads <= 32 * 32, "CtaCtl holds per-warp sums for at most 32 warps");
 
-template <int H>
+template <int H, bool SLICED>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     pmqa_main_kernel(const __grid_constant__ MainArgs a)
 {
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (warp == 0)
         tmem_alloc(&ctl.tmem_base, (uint32_t)a.tmem_cols);
 
-    balance_schedule(a.bs, [&](int i) { return (long long)tiles_of(a, i); }, ctl);
+    balance_schedule(a.bs, [&](int i) { return (long long)tiles_of<SLICED>(a, i); }, ctl);
     for (int n = threadIdx.x; n < kCtxCache; n += blockDim.x)
         ctl.ctx[n] = ctl.i0 + n < a.bs ? ctx_of(a, ctl.i0 + n) : 0;
     if (blockIdx.x == 0) {
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     }
 
-    group_role<H>(a, smem, ctl, warp >> 2, warp & 3);
+    group_role<H, SLICED>(a, smem, ctl, warp >> 2, warp & 3);
 
     tc_fence_before_sync();
     __syncthreads();

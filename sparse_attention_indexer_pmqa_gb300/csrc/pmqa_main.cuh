@@ -174,8 +174,10 @@ __device__ void balance_schedule(int n_items, LenFn len_of, CtaCtl &c)
 }
 
 // Context lengths of the CTA's requests: from the shared-memory cache while it
-// covers them, else from global memory (clamped); and the slice of each
-// request's tokens to score.
+// covers them, else from global memory (clamped); and, when SLICED, the slice
+// of each request's tokens to score (else all of them: the kernel is compiled
+// for each case so the common one carries no slice bounds).
+template <bool SLICED>
 struct ReqCtx {
     int bs, i0, lim;
     const int *cache;  // clamped contexts of requests i0 .. i0 + kCtxCache - 1
@@ -199,7 +201,7 @@ struct ReqCtx {
     // tokens [tb, te) of request r (context ctx) are scored
     __device__ void bounds(int r, int ctx, int &tb, int &te) const
     {
-        if (tok_begin) {
+        if constexpr (SLICED) {
             tb = clamp_ctx(__ldg(tok_begin + r), (long long)ctx);
             te = max(tb, clamp_ctx(__ldg(tok_end + r), (long long)ctx));
         } else {
@@ -221,11 +223,12 @@ __device__ __forceinline__ void tile_span(int tb, int te, int &mb, int &nt)
 }
 
 // Tiles of request i to score (the length of its work item in the schedule).
+template <bool SLICED>
 __device__ __forceinline__ int tiles_of(const MainArgs &a, int i)
 {
     const int ctx = ctx_of(a, i);
     int tb = 0, te = ctx, mb, nt;
-    if (a.tok_begin) {
+    if constexpr (SLICED) {
         tb = clamp_ctx(__ldg(a.tok_begin + i), (long long)ctx);
         te = max(tb, clamp_ctx(__ldg(a.tok_end + i), (long long)ctx));
     }
@@ -235,21 +238,28 @@ __device__ __forceinline__ int tiles_of(const MainArgs &a, int i)
 
 // Position (request i, tile m of the tiles [mb, nt) covering its tokens
 // [tb, te), context ctx) in the CTA's walk over (request, tile) pairs;
-// requests without tiles are skipped.
+// requests without tiles are skipped. Without slices mb = tb = 0, te = ctx.
+template <bool SLICED>
 struct TilePos {
     int i, m, mb, nt, ctx, tb, te;
-    __device__ void set_request(const ReqCtx &rc, int r)
+    __device__ void set_request(const ReqCtx<SLICED> &rc, int r)
     {
         i = r;
         ctx = rc.ctx_at(r);
-        rc.bounds(r, ctx, tb, te);
-        tile_span(tb, te, mb, nt);
+        if constexpr (SLICED) {
+            rc.bounds(r, ctx, tb, te);
+            tile_span(tb, te, mb, nt);
+        } else {
+            tb = mb = 0;
+            te = ctx;
+            nt = (ctx + kTileTokens - 1) / kTileTokens;
+        }
     }
     __device__ void clear()
     {
         m = mb = nt = ctx = tb = te = 0;
     }
-    __device__ void init(const ReqCtx &rc, const CtaCtl &cc)
+    __device__ void init(const ReqCtx<SLICED> &rc, const CtaCtl &cc)
     {
         if (cc.i0 < rc.bs) {
             set_request(rc, cc.i0);
@@ -259,7 +269,7 @@ struct TilePos {
             clear();
         }
     }
-    __device__ void next(const ReqCtx &rc)
+    __device__ void next(const ReqCtx<SLICED> &rc)
     {
         if (++m < nt)
             return;
@@ -273,26 +283,22 @@ struct TilePos {
         } while (nt == 0);
         m = mb;
     }
-    __device__ void skip(const ReqCtx &rc, int n)
-    {
-        for (int u = 0; u < n; ++u)
-            next(rc);
-    }
     __device__ bool last_of_request() const { return m == nt - 1; }
 };
 
 // Steps from request to request of the CTA's range: `first` is the CTA tile
 // index of the current request's first tile here.
+template <bool SLICED>
 struct ReqWalk {
-    TilePos p;
+    TilePos<SLICED> p;
     int first;
-    __device__ void init(const ReqCtx &rc, const CtaCtl &c)
+    __device__ void init(const ReqCtx<SLICED> &rc, const CtaCtl &c)
     {
         p.init(rc, c);
         first = 0;
     }
     __device__ bool valid(int count) const { return p.nt > 0 && first < count; }
-    __device__ void advance(const ReqCtx &rc)
+    __device__ void advance(const ReqCtx<SLICED> &rc)
     {
         first += p.nt - p.m;
         p.m = p.nt - 1;
@@ -457,10 +463,11 @@ __device__ __forceinline__ void epi_dispatch(int nr, bool all_pos, uint32_t tadd
 // Position in the CTA's tile range: `cur` is tile kk. step(n) moves n tiles on
 // and counts the request ends it passes (the last tile of a request, and the
 // range's last tile).
+template <bool SLICED>
 struct Walk {
-    TilePos cur;
+    TilePos<SLICED> cur;
     int kk;
-    __device__ int step(const ReqCtx &rc, int n, int count)
+    __device__ int step(const ReqCtx<SLICED> &rc, int n, int count)
     {
         // common case: the n tiles left behind lie inside one request and
         // before the range's last tile
@@ -534,22 +541,24 @@ struct TileGather {
     __device__ int page_of(int tok) const { return p_pow2 ? tok >> p_shift : tok / P; }
 
     // Block-table entry of this thread's row in tile p (-1 past the context).
-    __device__ int32_t table_entry(const TilePos &p) const
+    template <bool SLICED>
+    __device__ int32_t table_entry(const TilePos<SLICED> &p) const
     {
         const int tok = p.m * kTileTokens + (int)R;
-        return (p.nt > 0 && tok >= p.tb && tok < p.te) ? __ldg(bt + (long long)p.i * W + page_of(tok))
-                                                        : -1;
+        const bool in = SLICED ? (tok >= p.tb && tok < p.te) : tok < p.ctx;
+        return (p.nt > 0 && in) ? __ldg(bt + (long long)p.i * W + page_of(tok)) : -1;
     }
 
     // Copies of this warp's 32 rows of tile p (this row's table entry b) into
     // the staging slot; returns the row's repack metadata: 4 | misalignment / 4
     // when the row is valid, else 0.
-    __device__ uint32_t issue(const TilePos &p, int32_t b)
+    template <bool SLICED>
+    __device__ uint32_t issue(const TilePos<SLICED> &p, int32_t b)
     {
         const int t = p.m * kTileTokens + (int)R;
         bool v = false;
         long long o = 0;  // byte offset of the row in the pool
-        if (t >= p.tb && t < p.te) {
+        if (SLICED ? (t >= p.tb && t < p.te) : t < p.ctx) {
             if (b >= 0 && (long long)b < num_blocks) {
                 const int in_page = p_pow2 ? (t & (P - 1)) : t - page_of(t) * P;
                 o = ((long long)b * P + in_page) * kKvRowBytes;
@@ -690,16 +699,19 @@ struct TileGather {
 // tokens) sits in slot n % QS; at each request end every warpgroup meets the
 // others (a CTA barrier), then thread 0 loads the query of the request QS
 // ahead into the slot just freed.
+template <bool SLICED>
 struct QuerySlots {
-    int ord;     // request ends this warpgroup has passed = ordinal of its current request
-    bool have;   // the warpgroup has waited for its current request's slot
-    int loads;   // query loads issued (thread 0)
-    ReqWalk nxt; // next request whose query is to be loaded (thread 0)
+    int slot;        // slot of this warpgroup's current request
+    uint32_t phase;  // parity of that slot's fill
+    bool have;       // the warpgroup has waited for its current request's slot
+    int loads;       // query loads issued (thread 0)
+    ReqWalk<SLICED> nxt;  // next request whose query is to be loaded (thread 0)
 
-    __device__ void init(const MainArgs &a, uint8_t *smem, const Bars &B, const ReqCtx &rc,
+    __device__ void init(const MainArgs &a, uint8_t *smem, const Bars &B, const ReqCtx<SLICED> &rc,
                          const CtaCtl &c, int count)
     {
-        ord = 0;
+        slot = 0;
+        phase = 0;
         have = false;
         loads = 0;
         nxt.init(rc, c);
@@ -712,24 +724,25 @@ struct QuerySlots {
                 nxt.advance(rc);
             }
     }
-    __device__ void pass_ends(const MainArgs &a, uint8_t *smem, const Bars &B, const ReqCtx &rc,
-                              const CtaCtl &c, int count, int ends)
+    __device__ void pass_ends(const MainArgs &a, uint8_t *smem, const Bars &B,
+                              const ReqCtx<SLICED> &rc, const CtaCtl &c, int count, int ends)
     {
         for (int u = 0; u < ends; ++u) {
             named_bar_sync(kCtaBarrier, kMaxThreads);
             if (threadIdx.x == 0) {
                 if (nxt.valid(count) && !aborted(c)) {
-                    load_query(a, smem, B, ord % a.QS, nxt.p.i);
+                    load_query(a, smem, B, slot, nxt.p.i);
                     ++loads;
                 }
                 nxt.advance(rc);
             }
-            ++ord;
+            if (++slot == a.QS) {
+                slot = 0;
+                phase ^= 1u;
+            }
             have = false;
         }
     }
-    __device__ int slot(int n, int QS) const { return n % QS; }
-    __device__ uint32_t phase(int n, int QS) const { return (uint32_t)(n / QS) & 1u; }
     // after an abort, query loads nobody consumed land before the CTA exits (bounded)
     __device__ void drain(const Bars &B, int QS) const
     {
@@ -761,8 +774,9 @@ struct TokenOut {
     }
 };
 
-__device__ __forceinline__ TokenOut token_out(const MainArgs &a, const TilePos &it, uint32_t R,
-                                              uint64_t keep_pol)
+template <bool SLICED>
+__device__ __forceinline__ TokenOut token_out(const MainArgs &a, const TilePos<SLICED> &it,
+                                              uint32_t R, uint64_t keep_pol)
 {
     TokenOut o;
     o.logits = a.logits;
@@ -770,7 +784,9 @@ __device__ __forceinline__ TokenOut token_out(const MainArgs &a, const TilePos &
     o.mml = a.mml;
     o.t = it.m * kTileTokens + (int)R;
     o.lim0 = it.ctx - a.nn + 1;  // draft row j admits t < lim0 + j
-    o.in_slice = o.t >= it.tb && o.t < it.te;
+    // without slices every token below ctx is in range: the window test
+    // (t < lim0 + j <= ctx) already bounds it
+    o.in_slice = SLICED ? (o.t >= it.tb && o.t < it.te) : true;
     o.obase = (long long)it.i * a.nn * o.mml + o.t;
     o.hrow = a.hist ? a.hist + (long long)it.i * a.nn * kHistBins : nullptr;
     o.keep_pol = keep_pol;
@@ -780,7 +796,7 @@ __device__ __forceinline__ TokenOut token_out(const MainArgs &a, const TilePos &
 // Warpgroup g, warp quadrant qd (warp % 4): CTA tiles g, g + 4, g + 8, ...,
 // each carried through every step by this warpgroup alone. Shared memory is
 // addressed through 32-bit shared addresses throughout.
-template <int H>
+template <int H, bool SLICED>
 static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int g, int qd)
 {
     const Bars B(a, smem);
@@ -808,16 +824,16 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     const int npass = (nn + kRpp - 1) / kRpp;
     const uint64_t keep_pol = l2_evict_last_policy();
 
-    ReqCtx rc;
+    ReqCtx<SLICED> rc;
     rc.init(a, c);
-    QuerySlots qs;
+    QuerySlots<SLICED> qs;
     qs.init(a, smem, B, rc, c, count);
 
-    Walk w;  // the group's current tile
+    Walk<SLICED> w;  // the group's current tile
     w.cur.init(rc, c);
     w.kk = 0;
     qs.pass_ends(a, smem, B, rc, c, count, w.step(rc, g, count));
-    Walk nx = w;  // the group's next tile to gather
+    Walk<SLICED> nx = w;  // the group's next tile to gather
     uint32_t meta = 0;
     if (w.kk < count)
         meta = G.issue(w.cur, G.table_entry(w.cur));
@@ -841,9 +857,9 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
         tc_fence_before_sync();
         named_bar_sync(wg_bar, 128);
         tc_fence_after_sync();
-        const int q_slot = qs.slot(qs.ord, QS);
+        const int q_slot = qs.slot;
         if (!qs.have) {
-            ok = mbar_wait(&B.qfull[q_slot], qs.phase(qs.ord, QS), &c.abort) && ok;
+            ok = mbar_wait(&B.qfull[q_slot], qs.phase, &c.abort) && ok;
             qs.have = true;
         }
         // weights of the request: valid after the query-slot wait above

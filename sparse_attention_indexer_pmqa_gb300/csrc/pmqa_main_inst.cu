@@ -14,16 +14,23 @@
 
 namespace pmqa {
 
-cudaError_t PMQA_CAT(launch_main_h, PMQA_HEADS)(const MainArgs &a, int grid, int threads,
-                                                cudaStream_t stream)
+template <bool SLICED>
+static cudaError_t launch(const MainArgs &a, int grid, int threads, cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(pmqa_main_kernel<PMQA_HEADS>,
+    cudaError_t e = cudaFuncSetAttribute(pmqa_main_kernel<PMQA_HEADS, SLICED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)a.smem_bytes);
     if (e != cudaSuccess)
         return e;
-    pmqa_main_kernel<PMQA_HEADS><<<grid, threads, a.smem_bytes, stream>>>(a);
+    pmqa_main_kernel<PMQA_HEADS, SLICED><<<grid, threads, a.smem_bytes, stream>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t PMQA_CAT(launch_main_h, PMQA_HEADS)(const MainArgs &a, int grid, int threads,
+                                                cudaStream_t stream)
+{
+    return a.tok_begin ? launch<true>(a, grid, threads, stream)
+                       : launch<false>(a, grid, threads, stream);
 }
 
 }  // namespace pmqa
