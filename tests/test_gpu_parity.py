@@ -352,9 +352,10 @@ def test_many_short_requests(cuda_lib, nn, H):
 
 
 # Row lengths that pick each selection kernel: up to 32768 positions (one CTA
-# per row, logits in shared memory), up to 65536 (one CTA per row, logits read
-# in place), above (several CTAs per row).
-@pytest.mark.parametrize("mml", [32768, 40000, 65536, 70000])
+# per row, logits in shared memory), up to 65536 (one CTA per row, the logits
+# in two halves through shared memory), above (several CTAs per row, here up
+# to 64 and 74 of them).
+@pytest.mark.parametrize("mml", [32768, 40000, 65536, 70000, 262144, 300000])
 @pytest.mark.parametrize("ties", [False, True])
 def test_standalone_topk_each_selection_kernel(cuda_lib, mml, ties):
     ctx, nn, k = [mml, mml - 1, 33000, 2049, 1], 1, 2048
@@ -381,7 +382,7 @@ def test_fused_topk_with_rows_read_in_place(cuda_lib):
     check_topk_rows(idx, r64, tol, prob.context_lens, prob.next_n, 2048, vals=vals)
 
 
-@pytest.mark.parametrize("mml", [4096, 40000, 70000])
+@pytest.mark.parametrize("mml", [4096, 40000, 70000, 300000])
 def test_fused_call_replays_from_a_cuda_graph(cuda_lib, mml):
     """The fused call (KV pass + programmatic-dependent selection) captured in a
     CUDA graph and replayed gives what the direct call gives, with the same
