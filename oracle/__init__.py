@@ -1,5 +1,6 @@
 """CPU oracle for the FP8 MQA-logits indexer (paged decode and non-paged
-prefill) and its per-row top-k.
+prefill), its per-row top-k, and the sparse MLA decode that consumes the
+top-k positions.
 
 TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg import this package. The product library never
@@ -12,7 +13,9 @@ there cites the passage of the pages it follows.
 Parity pins: every function here is pinned by tests under ``tests/`` marked
 ``not gpu`` (fp8 code points and a full comparison with torch's e4m3fn decode,
 one-hot and sign-flip closed forms, library GEMV special cases, invariants,
-brute-force top-k); none is "parity unpinned".
+brute-force top-k; for the MLA decode a worked two-token example, the
+uniform-weight and one-hot closed forms and torch's scaled dot-product
+attention on a dense listing); none is "parity unpinned".
 """
 
 from __future__ import annotations
@@ -57,6 +60,10 @@ def _load():
         lib.pmqa_ref_mqa_logits.argtypes = [P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int]
         lib.pmqa_ref_mqa_logits.restype = ctypes.c_int
+        D, I = ctypes.c_double, ctypes.c_int
+        lib.pmqa_ref_sparse_mla.argtypes = [P, D, P, D, P, P, P, I, I, I, I, I, ctypes.c_int64,
+                                            D, P, P, P, P, P, I]
+        lib.pmqa_ref_sparse_mla.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -156,3 +163,36 @@ def topk(vals: np.ndarray, context_lens, next_n: int, k: int, *, nthreads: int |
 def valid_len(context_len: int, next_n: int, j: int) -> int:
     """Entries of draft row j that the causal window admits."""
     return max(0, min(context_len - next_n + j + 1, context_len))
+
+
+def sparse_mla(prob, *, rows=None, want_tol: bool = False, nthreads: int | None = None):
+    """Sparse MLA decode of ``prob`` (a synth.mla.MlaProblem, or any object
+    with its fields): (out [R, heads, 512] fp64, lse [R, heads] fp64, tol)
+    where tol is None or a dict of the per-entry aggregates a_abs, d_abs
+    [R, heads, 512] and s_abs [R, heads]. ``rows`` restricts the call to those
+    query rows (in that order)."""
+    lib = _load()
+    nn = prob.next_n
+    all_rows = np.arange(prob.bs * nn) if rows is None else np.asarray(rows, dtype=np.int64)
+    q = np.ascontiguousarray(prob.q.reshape(prob.bs * nn, prob.heads, -1)[all_rows],
+                             dtype=np.uint8)
+    idx = np.ascontiguousarray(prob.indices[all_rows], dtype=np.int32)
+    req = np.ascontiguousarray(all_rows // nn, dtype=np.int32)
+    kv = np.ascontiguousarray(prob.kv, dtype=np.uint8)
+    bt = np.ascontiguousarray(prob.block_tables, dtype=np.int32)
+    R, H = q.shape[0], q.shape[1]
+    assert q.shape[2] == 576 and kv.shape[2] == 576
+    out = np.empty((R, H, 512), dtype=np.float64)
+    lse = np.empty((R, H), dtype=np.float64)
+    a_abs = np.empty_like(out) if want_tol else None
+    d_abs = np.empty_like(out) if want_tol else None
+    s_abs = np.empty_like(lse) if want_tol else None
+    rc = lib.pmqa_ref_sparse_mla(_ptr(q), prob.q_scale, _ptr(kv), prob.kv_scale, _ptr(idx),
+                                 _ptr(req), _ptr(bt), R, H, idx.shape[1], kv.shape[1],
+                                 bt.shape[1], kv.shape[0], prob.sm_scale, _ptr(out), _ptr(lse),
+                                 _ptr(a_abs), _ptr(d_abs), _ptr(s_abs),
+                                 nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle pmqa_ref_sparse_mla failed with %d" % rc)
+    tol = dict(a_abs=a_abs, d_abs=d_abs, s_abs=s_abs) if want_tol else None
+    return out, lse, tol

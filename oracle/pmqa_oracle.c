@@ -36,6 +36,9 @@
  * Top-k [P1]: per row, the entries t < valid_len sorted by (value descending,
  * index ascending); the first min(k, valid_len) indices, the rest -1.
  *
+ * The last section of this file is the oracle of the sparse MLA decode that
+ * consumes the top-k positions; its sources and readings are listed there.
+ *
  * Readings where the pages leave a step open: the reference function names a
  * "bf16 reference" but computes in fp32; here the arithmetic is the exact real
  * one (double). NaN inputs propagate as they do under IEEE rules (relu keeps a
@@ -520,4 +523,238 @@ int pmqa_ref_mqa_logits(const uint8_t *q, const uint8_t *k, const float *k_scale
     free(th);
     pthread_mutex_destroy(&J.lock);
     return J.error ? -4 : 0;
+}
+
+/* ---- sparse MLA decode ----------------------------------------------------
+ *
+ * Sources (page titles and sections):
+ *   [P1] "[Bug] aiter ops triton attention pa", section "Downstream impact":
+ *        the indexer's top-k positions are the ones the sparse MLA attention
+ *        of the same decode step attends to.
+ *   [P2] "[Bug][ROCm]: ROCM_AITER_MLA can select an aiter MLA decode kernel
+ *        that silently returns uncorrelated output" (chat-gpts.plus summary):
+ *        the MLA decode with fp8 Q and fp8 KV, 16 query heads sharing one
+ *        latent KV head (gqa_ratio 16), 1..4 query rows per request
+ *        (decode_qlen), and a log-sum-exp output used by decode context
+ *        parallelism.
+ *   [P3] "[Bugfix][Hardware][AMD] Fix last_page_len calculation in AITER MLA
+ *        decode", section "The Bug": the MLA KV cache uses pages of one token
+ *        (the paged form with larger pages is the same lookup).
+ *
+ * Readings where the pages are silent: a cached token is one latent row of
+ * 576 fp8 values whose first 512 are also its value vector (the MLA layout of
+ * a 512-wide compressed KV plus a 64-wide rotary key); q and the cache carry
+ * one fp32 scale each (per tensor); the score of position t for head h is
+ * sm_scale * q_h . k_t on the dequantised values; every listed position counts
+ * once per listing (a repeated position twice), -1 entries are skipped.
+ *
+ * For row r (request i = row_req[r]) and head h, over its listed positions t:
+ *   s_t      = sm_scale * sum_d (q_scale * q[r][h][d]) * (kv_scale * k_t[d]),  d < 576
+ *   out[d]   = sum_t exp(s_t - m) * kv_scale * k_t[d] / sum_t exp(s_t - m),    d < 512
+ *   lse      = m + log(sum_t exp(s_t - m)),   m = max_t s_t
+ * (the softmax-weighted mean of the value rows; the shift by m changes
+ * nothing mathematically and keeps exp finite). A row with no listed
+ * position gives out = 0 and lse = -inf.
+ * Beside them, for the parity tolerance: a_abs[d] = sum_t p_t |v_t[d]|,
+ * d_abs[d] = sum_t p_t |v_t[d] - out[d]| and s_abs = max_t sm_scale *
+ * sum_d |q_d k_t[d]| (dequantised), with p_t the normalised weights.
+ */
+#define PMQA_REF_MLA_DIM 576
+#define PMQA_REF_MLA_VDIM 512
+
+typedef struct {
+    const uint8_t *q, *kv;
+    const int32_t *idx, *row_req, *bt;
+    double q_scale, kv_scale, sm_scale;
+    int R, H, topk, P, W;
+    int64_t num_blocks;
+    double *out, *lse, *a_abs, *d_abs, *s_abs;
+    double table[256];
+    int next_row;
+    pthread_mutex_t lock;
+    int error;
+} mla_job;
+
+/* Slot of position t of request i, or -1 when the table does not cover it. */
+static int64_t mla_slot(const mla_job *J, int i, int64_t t)
+{
+    if (t < 0 || t >= (int64_t)J->W * J->P)
+        return -1;
+    const int64_t page = J->bt[(int64_t)i * J->W + t / J->P];
+    if (page < 0 || page >= J->num_blocks)
+        return -1;
+    return page * J->P + t % J->P;
+}
+
+static int mla_row(mla_job *J, int r, double *kd, double *s, int64_t *slot)
+{
+    const int H = J->H, D = PMQA_REF_MLA_DIM, V = PMQA_REF_MLA_VDIM;
+    const int i = J->row_req[r];
+    int n = 0;
+    for (int e = 0; e < J->topk; ++e) {
+        const int32_t t = J->idx[(int64_t)r * J->topk + e];
+        if (t < 0)
+            continue;
+        const int64_t sl = mla_slot(J, i, t);
+        if (sl < 0)
+            return -2;
+        slot[n++] = sl;
+    }
+    for (int h = 0; h < H; ++h) {
+        const uint8_t *qrow = J->q + ((int64_t)r * H + h) * D;
+        double *o = J->out + ((int64_t)r * H + h) * V;
+        double qd[PMQA_REF_MLA_DIM];
+        for (int d = 0; d < D; ++d)
+            qd[d] = J->q_scale * J->table[qrow[d]];
+        double m = -INFINITY, smag = 0.0;
+        for (int e = 0; e < n; ++e) {
+            const uint8_t *krow = J->kv + slot[e] * D;
+            double dot = 0.0, mag = 0.0;
+            for (int d = 0; d < D; ++d) {
+                const double kv = J->kv_scale * J->table[krow[d]];
+                dot += qd[d] * kv;
+                mag += fabs(qd[d] * kv);
+            }
+            s[e] = J->sm_scale * dot;
+            if (s[e] > m)
+                m = s[e];
+            if (J->sm_scale * mag > smag)
+                smag = J->sm_scale * mag;
+        }
+        for (int d = 0; d < V; ++d)
+            o[d] = 0.0;
+        if (J->s_abs)
+            J->s_abs[(int64_t)r * H + h] = smag;
+        if (n == 0) {
+            J->lse[(int64_t)r * H + h] = -INFINITY;
+            if (J->a_abs)
+                for (int d = 0; d < V; ++d)
+                    J->a_abs[((int64_t)r * H + h) * V + d] = 0.0;
+            if (J->d_abs)
+                for (int d = 0; d < V; ++d)
+                    J->d_abs[((int64_t)r * H + h) * V + d] = 0.0;
+            continue;
+        }
+        double l = 0.0;
+        for (int e = 0; e < n; ++e) {
+            s[e] = exp(s[e] - m); /* s now holds the unnormalised weight */
+            l += s[e];
+        }
+        for (int e = 0; e < n; ++e) {
+            const uint8_t *krow = J->kv + slot[e] * D;
+            const double p = s[e] / l;
+            for (int d = 0; d < V; ++d)
+                o[d] += p * (J->kv_scale * J->table[krow[d]]);
+        }
+        J->lse[(int64_t)r * H + h] = m + log(l);
+        if (J->a_abs || J->d_abs) {
+            double *aa = J->a_abs ? J->a_abs + ((int64_t)r * H + h) * V : NULL;
+            double *da = J->d_abs ? J->d_abs + ((int64_t)r * H + h) * V : NULL;
+            for (int d = 0; d < V; ++d) {
+                if (aa)
+                    aa[d] = 0.0;
+                if (da)
+                    da[d] = 0.0;
+            }
+            for (int e = 0; e < n; ++e) {
+                const uint8_t *krow = J->kv + slot[e] * D;
+                const double p = s[e] / l;
+                for (int d = 0; d < V; ++d) {
+                    kd[d] = J->kv_scale * J->table[krow[d]];
+                    if (aa)
+                        aa[d] += p * fabs(kd[d]);
+                    if (da)
+                        da[d] += p * fabs(kd[d] - o[d]);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+static void *mla_worker(void *arg)
+{
+    mla_job *J = (mla_job *)arg;
+    double *kd = (double *)malloc(sizeof(double) * PMQA_REF_MLA_VDIM);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(J->topk > 0 ? J->topk : 1));
+    int64_t *slot = (int64_t *)malloc(sizeof(int64_t) * (size_t)(J->topk > 0 ? J->topk : 1));
+    if (!kd || !s || !slot) {
+        J->error = -4;
+    } else {
+        for (;;) {
+            pthread_mutex_lock(&J->lock);
+            int r = J->next_row++;
+            pthread_mutex_unlock(&J->lock);
+            if (r >= J->R || J->error)
+                break;
+            int rc = mla_row(J, r, kd, s, slot);
+            if (rc) {
+                pthread_mutex_lock(&J->lock);
+                J->error = rc;
+                pthread_mutex_unlock(&J->lock);
+            }
+        }
+    }
+    free(kd);
+    free(s);
+    free(slot);
+    return NULL;
+}
+
+/*
+ * q        [R, heads, 576] e4m3fn bytes (row r's query heads)
+ * kv       [num_blocks, P, 576] e4m3fn bytes (one latent row per slot)
+ * indices  [R, topk] int32 positions in the row's request, -1 = no entry
+ * row_req  [R] int32: the request (block-table row) of each query row
+ * block_tables [bs, W] int32
+ * out      [R, heads, 512] double; lse [R, heads] double
+ * a_abs, d_abs [R, heads, 512] and s_abs [R, heads] double, or NULL
+ * Returns 0, -1 for bad sizes, -2 for a listed position that the table does
+ * not map into the pool, -4 when out of memory.
+ */
+int pmqa_ref_sparse_mla(const uint8_t *q, double q_scale, const uint8_t *kv, double kv_scale,
+                        const int32_t *indices, const int32_t *row_req,
+                        const int32_t *block_tables, int R, int heads, int topk, int P, int W,
+                        int64_t num_blocks, double sm_scale, double *out, double *lse,
+                        double *a_abs, double *d_abs, double *s_abs, int nthreads)
+{
+    if (R < 0 || heads < 1 || topk < 0 || P < 1 || W < 0 || num_blocks < 0)
+        return -1;
+    mla_job J;
+    memset(&J, 0, sizeof J);
+    J.q = q;
+    J.kv = kv;
+    J.idx = indices;
+    J.row_req = row_req;
+    J.bt = block_tables;
+    J.q_scale = q_scale;
+    J.kv_scale = kv_scale;
+    J.sm_scale = sm_scale;
+    J.R = R;
+    J.H = heads;
+    J.topk = topk;
+    J.P = P;
+    J.W = W;
+    J.num_blocks = num_blocks;
+    J.out = out;
+    J.lse = lse;
+    J.a_abs = a_abs;
+    J.d_abs = d_abs;
+    J.s_abs = s_abs;
+    pmqa_ref_e4m3fn_table(J.table);
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1)
+        nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int started = 0;
+    for (int t = 0; th && t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, mla_worker, &J) == 0)
+            ++started;
+    if (started == 0)
+        mla_worker(&J);
+    for (int t = 0; t < started; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return J.error;
 }

@@ -1,7 +1,8 @@
-"""Seeded synthetic inputs for the FP8 paged MQA-logits indexer.
+"""Seeded synthetic inputs for the FP8 paged MQA-logits indexer and the
+sparse MLA decode that consumes its top-k positions.
 
 This module only draws random numbers and packs them into the byte layouts the
-indexer consumes. It holds none of the indexer's arithmetic, and both the CPU
+indexer and the decode consume. It holds none of their arithmetic, and both the CPU
 oracle and the CUDA path take their inputs from here.
 """
 
@@ -17,3 +18,4 @@ from .inputs import (  # noqa: F401
     prefill_config,
     prefill_ranges,
 )
+from .mla import MLA_CONFIGS, MlaProblem, make_mla_problem, mla_config  # noqa: F401,E402
