@@ -1,7 +1,8 @@
 /*
  * pmqa.h -- C ABI of libpmqa: the FP8 paged MQA-logits indexer and its per-row
- * top-k, and the non-paged (prefill) MQA logits, as hand-written CUDA kernels
- * for sm_103a (GB300).
+ * top-k, the non-paged (prefill) MQA logits, and the sparse MLA decode that
+ * consumes the top-k positions, as hand-written CUDA kernels for sm_103a
+ * (GB300).
  *
  * What is computed. Sources: the page "[Bug] aiter ops triton attention pa"
  * (stepcodex.com issue mirror), section "Minimal reproduction" (the reference
@@ -259,6 +260,75 @@ typedef struct pmqa_mqa_problem {
  */
 int pmqa_mqa_logits(const pmqa_mqa_problem *p, float *logits, void *ws, size_t ws_bytes,
                     pmqa_stream_t stream);
+
+/*
+ * Sparse MLA decode over the indexer's top-k positions: the attention step of
+ * the same decode step, which attends only to the positions the top-k
+ * selected. Sources: the page "[Bug] aiter ops triton attention pa", section
+ * "Downstream impact" (the sparse MLA attention attends to the indexer's top-k
+ * positions); the page "[Bug][ROCm]: ROCM_AITER_MLA can select an aiter MLA
+ * decode kernel that silently returns uncorrelated output" (chat-gpts.plus
+ * summary: fp8 Q and fp8 KV, 16 query heads per latent KV head, 1..4 query
+ * rows per request, a log-sum-exp output for decode context parallelism); the
+ * page "[Bugfix][Hardware][AMD] Fix last_page_len calculation in AITER MLA
+ * decode", section "The Bug" (the MLA cache in pages of one token; larger
+ * pages use the same lookup). The pages give no widths: a cached token is one
+ * latent row of 576 fp8 values whose first 512 are its value vector (the MLA
+ * layout of a 512-wide compressed KV plus a 64-wide rotary key), and q and the
+ * cache carry one fp32 scale each.
+ *
+ *   For query row r = i*next_n + j, head h and each listed position t of row r
+ *   (indices[r][e] >= 0; a position listed twice counts twice):
+ *     phys    = block_tables[i][t / block_size] * block_size + t % block_size
+ *     s_t     = sm_scale * sum_d (q_scale * q[r][h][d]) * (kv_scale * kv[phys][d]),  d < 576
+ *     out[r][h][d] = sum_t softmax(s)_t * kv_scale * kv[phys][d],   d < 512
+ *     lse[r][h]    = ln sum_t exp(s_t)
+ *   A row with no listed position gives out = 0 and lse = -inf.
+ *
+ *   q             fp8 e4m3fn [bs * next_n, heads, head_dim], contiguous, 16-byte aligned
+ *   kv_cache      fp8 e4m3fn [num_blocks, block_size, head_dim], contiguous,
+ *                 16-byte aligned; only the rows of listed positions are read
+ *   indices       int32 [bs * next_n, topk]: positions in the row's request
+ *                 (what pmqa_logits_topk returns), -1 for an empty entry
+ *   block_tables  int32 [bs, max_blocks_per_seq], row-major
+ * heads must be 16, head_dim 576 and v_head_dim 512 (PMQA_ERR_UNSUPPORTED
+ * otherwise); the scales must be finite.
+ */
+typedef struct pmqa_mla_problem {
+    const void *q;
+    const void *kv_cache;
+    const int32_t *indices;
+    const int32_t *block_tables;
+    float q_scale;
+    float kv_scale;
+    float sm_scale;
+    int32_t bs;
+    int32_t next_n;
+    int32_t heads;
+    int32_t head_dim;
+    int32_t v_head_dim;
+    int32_t topk;
+    int32_t block_size;
+    int32_t max_blocks_per_seq;
+    int64_t num_blocks;
+} pmqa_mla_problem;
+
+/* Bytes of workspace for pmqa_sparse_mla_decode over `rows` query rows (about
+   17 MB plus 4 bytes per row); 0 for rows < 0. */
+size_t pmqa_sparse_mla_workspace_bytes(int32_t rows);
+
+/*
+ * out: bf16 [bs * next_n, heads, 512], 4-byte aligned; lse: fp32
+ * [bs * next_n, heads] or NULL. ws: pmqa_sparse_mla_workspace_bytes(rows)
+ * bytes, 256-byte aligned, zero-filled before its first use
+ * (pmqa_workspace_init); every call leaves it zero-filled again except the
+ * status word. A listed position past the block table sets PMQA_DEV_BAD_CONTEXT,
+ * a table entry outside [0, num_blocks) PMQA_DEV_BAD_BLOCK_ID (the position
+ * is then skipped); a pipeline wait that ran out sets PMQA_DEV_TIMEOUT (results
+ * invalid, re-initialise the workspace). One kernel launch.
+ */
+int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, float *lse, void *ws,
+                           size_t ws_bytes, pmqa_stream_t stream);
 
 /*
  * Synchronise the stream, return the device status bits recorded since the

@@ -1,0 +1,730 @@
+// pmqa_mla.cu -- sparse MLA decode over the indexer's top-k positions, and its
+// C ABI (pmqa_sparse_mla_decode, pmqa_sparse_mla_workspace_bytes).
+//
+// What is computed. Sources: the page "[Bug] aiter ops triton attention pa",
+// section "Downstream impact" (the sparse MLA attention of a decode step
+// attends to the positions the indexer's top-k selected); the page
+// "[Bug][ROCm]: ROCM_AITER_MLA can select an aiter MLA decode kernel that
+// silently returns uncorrelated output" (chat-gpts.plus summary: fp8 Q and fp8
+// KV, 16 query heads per latent KV head, 1..4 query rows per request, an LSE
+// output for decode context parallelism); the page "[Bugfix][Hardware][AMD] Fix
+// last_page_len calculation in AITER MLA decode", section "The Bug" (pages of
+// one token). For query row r and head h, over the row's listed positions t:
+//   out[r][h] = sum_t softmax_t(sm_scale * q_h . k_t) * v_t,   v_t = k_t[0..511]
+//   lse[r][h] = ln sum_t exp(sm_scale * q_h . k_t)
+// with q and k_t the fp8 codes times their per-tensor scales.
+//
+// One persistent CTA per SM walks a contiguous range of the flattened
+// (row, 128-position tile) sequence. Per tile:
+//   * 128 producer threads gather the 128 listed latent rows (576 bytes each)
+//     with 16-byte cp.async straight into the 128-byte-swizzled operand layout:
+//     four 16 KB blocks of value columns and one block for the rotary columns;
+//   * one thread issues S^T = K . Q^T on the tensor cores (M = 128 positions,
+//     N = 16 heads, K = 576) into TMEM;
+//   * 128 softmax threads (one TMEM lane = one position each) take the tile's
+//     per-head maximum, keep a running reference maximum that moves only when
+//     it would be exceeded by more than 2^8, form p = 2^(x - m) and write it
+//     as two fp8 terms p_hi = e4m3(p), p_lo = e4m3(16 (p - p_hi)) into a
+//     K-major operand of 32 rows (16 hi + 16 lo heads);
+//   * the thread issues O^T += V^T . P^T (M = 128 value columns per block, four
+//     blocks, N = 32, K = 128 positions), reading the SAME gathered tile as an
+//     MN-major operand, into four TMEM accumulators of 32 columns.
+// A row's tiles split over at most a few CTAs: each writes its unnormalised
+// part (O, m, l) to the workspace and the last to arrive combines them.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/pmqa.h"
+#include "pmqa_ptx.cuh"
+
+namespace pmqa {
+namespace mla {
+
+constexpr int kDim = 576;    // latent row: 512 value columns + 64 rotary columns
+constexpr int kVDim = 512;   // value columns
+constexpr int kHeads = 16;   // query heads per latent KV head
+constexpr int kTile = 128;   // listed positions per tile (the first product's M)
+constexpr int kChunks = kDim / 16;
+constexpr uint32_t kBlk = 128u * 128u;          // one 128-byte column block of a tile
+constexpr uint32_t kStageBytes = 5u * kBlk;     // 4 value blocks + the rotary block
+constexpr uint32_t kQBlk = 16u * 128u;          // one column block of the 16 query heads
+constexpr uint32_t kQBytes = 5u * kQBlk;
+constexpr uint32_t kPBytes = 32u * 128u;        // 32 rows (hi, lo) x 128 positions
+constexpr int kProducers = 128;
+constexpr int kSoftmax = 128;
+constexpr int kThreads = kProducers + kSoftmax + 32;
+constexpr int kMmaWarp = (kProducers + kSoftmax) / 32;
+constexpr int kMaxCtas = 256;                   // workspace parts: 2 per CTA
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;                   // 2 x 16 score columns
+constexpr uint32_t kColO = 128;                 // 4 x 32 output columns
+constexpr float kLoScale = 16.0f;               // p_lo holds 16 (p - p_hi)
+constexpr float kRescaleSlack = 8.0f;           // p <= 2^8 before the maximum moves
+
+constexpr uint32_t kOffKV = 0;
+constexpr uint32_t kOffQ = 2u * kStageBytes;
+constexpr uint32_t kOffP = kOffQ + 2u * kQBytes;
+constexpr uint32_t kOffFlags = kOffP + 2u * kPBytes;
+constexpr uint32_t kOffRed = kOffFlags + 2u * kTile;          // [2][4 warps][16] floats
+constexpr uint32_t kOffLred = kOffRed + 2u * 4u * 16u * 4u;   // [4 warps][16] floats
+constexpr uint32_t kOffBar = kOffLred + 4u * 16u * 4u;
+enum {
+    kBarFull = 0,      // [2] tile (and query) rows landed: 128 producer arrivals
+    kBarKvEmpty = 2,   // [2] products of the tile done: MMA commit
+    kBarSFull = 4,     // [2] scores in TMEM: MMA commit
+    kBarSFree = 6,     // [2] scores read: one arrival per softmax warp
+    kBarPFull = 8,     // [2] P written (and O rescaled): one arrival per softmax warp
+    kBarPEmpty = 10,   // [2] P read by the second product: MMA commit
+    kBarQEmpty = 12,   // [2] query buffer read: MMA commit after a row's last tile
+    kBarFlags = 14,    // [2] tile position flags written: one arrival per producer warp
+    kBarDrain = 16,    // MMAs drained before TMEM is freed
+    kNumBars = 17
+};
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8u;  // tmem base, abort flag, last flag
+constexpr uint32_t kSmemBytes = kOffMisc + 64u + 1024u;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kIdescQK = idesc_e4m3_f32(128, kHeads);
+constexpr uint32_t kIdescPV = idesc_e4m3_f32(128, 2 * kHeads) | kIdescAMnMajor;
+
+struct Args {
+    const uint8_t *q;     // [R, 16, 576]
+    const uint8_t *kv;    // [num_blocks * P, 576]
+    const int32_t *idx;   // [R, topk]
+    const int32_t *bt;    // [bs, W]
+    float c_log2;         // sm_scale * q_scale * kv_scale * log2(e)
+    float kv_scale;
+    int next_n, topk, T, P, W;
+    long long num_blocks;
+    long long N;          // R * T tiles
+    int G;                // CTAs
+    uint16_t *out;        // bf16 [R, 16, 512]
+    float *lse;           // [R, 16] or null
+    uint32_t *status;
+    uint32_t *cnt;        // [R] arrivals of a row's parts
+    float *ml;            // [2 G][16][2] (m, l) of each part
+    float *part;          // [2 G][16][512] unnormalised output of each part
+};
+
+__device__ __forceinline__ long long tile_start(const Args &a, int b)
+{
+    return (long long)b * a.N / a.G;
+}
+
+// The CTA whose range holds tile x.
+__device__ __forceinline__ int cta_of(const Args &a, long long x)
+{
+    return (int)(((x + 1) * (long long)a.G - 1) / a.N);
+}
+
+// Reduce 16 per-lane values over the warp; lane returns the result for head
+// (lane >> 1) & 15 (halves exchanged by lane bits 4, 3, 2, 1, then bit 0).
+template <bool MAX>
+__device__ __forceinline__ float warp_reduce_scatter16(const float (&v)[16], int lane)
+{
+    constexpr uint32_t kFull = 0xFFFFFFFFu;
+    auto op = [](float x, float y) { return MAX ? fmaxf(x, y) : x + y; };
+    float a8[8], a4[4], a2[2];
+    const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0, u4 = (lane & 4) != 0,
+               u2 = (lane & 2) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float send = u16 ? v[i] : v[i + 8];
+        const float keep = u16 ? v[i + 8] : v[i];
+        a8[i] = op(keep, __shfl_xor_sync(kFull, send, 16));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = u8 ? a8[i] : a8[i + 4];
+        const float keep = u8 ? a8[i + 4] : a8[i];
+        a4[i] = op(keep, __shfl_xor_sync(kFull, send, 8));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = u4 ? a4[i] : a4[i + 2];
+        const float keep = u4 ? a4[i + 2] : a4[i];
+        a2[i] = op(keep, __shfl_xor_sync(kFull, send, 4));
+    }
+    const float send = u2 ? a2[0] : a2[1];
+    const float keep = u2 ? a2[1] : a2[0];
+    const float a1 = op(keep, __shfl_xor_sync(kFull, send, 2));
+    return op(a1, __shfl_xor_sync(kFull, a1, 1));
+}
+
+// v[i] for a run-time i < 16 without indexing the array (which would move it
+// to local memory).
+__device__ __forceinline__ float pick16(const float (&v)[16], int i)
+{
+    float r = v[0];
+#pragma unroll
+    for (int h = 1; h < 16; ++h)
+        r = i == h ? v[h] : r;
+    return r;
+}
+
+// Byte offset of (row n, position s) in a P buffer: K-major, 128-byte swizzle.
+__device__ __forceinline__ uint32_t p_offset(int n, int s)
+{
+    return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((((s >> 4) ^ (n & 7)) & 7) << 4) +
+                      (s & 15));
+}
+
+__device__ __forceinline__ void st_shared_u8(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ float ld_cg(const float *p)
+{
+    return __ldcg(p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    uint8_t *flags = smem + kOffFlags;
+    float *red = reinterpret_cast<float *>(smem + kOffRed);
+    float *lred = reinterpret_cast<float *>(smem + kOffLred);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar[kBarFull + i], kProducers);
+            mbar_init(&bar[kBarKvEmpty + i], 1);
+            mbar_init(&bar[kBarSFull + i], 1);
+            mbar_init(&bar[kBarSFree + i], kSoftmax / 32);
+            mbar_init(&bar[kBarPFull + i], kSoftmax / 32);
+            mbar_init(&bar[kBarPEmpty + i], 1);
+            mbar_init(&bar[kBarQEmpty + i], 1);
+            mbar_init(&bar[kBarFlags + i], kProducers / 32);
+        }
+        mbar_init(&bar[kBarDrain], 1);
+        misc[1] = 0;
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp)
+        tmem_alloc(misc, kTmemCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    const long long x0 = tile_start(a, blockIdx.x), x1 = tile_start(a, blockIdx.x + 1);
+    auto fail = [&]() {
+        atomicOr(a.status, (uint32_t)PMQA_DEV_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (tid < kProducers) {
+        // ------------------------------------------------------------ producer
+        const int pw = tid >> 5;
+        int seg = -1;
+        for (long long x = x0; x < x1; ++x) {
+            const int it = (int)(x - x0), stage = it & 1;
+            const uint32_t kph = (uint32_t)(it >> 1) & 1u;
+            const long long r = x / a.T;
+            const int j = (int)(x - r * a.T);
+            const bool first = x == x0 || j == 0;
+            if (first)
+                ++seg;
+            // this lane's position of the tile and its pool row (-1: none)
+            const int tok = pw * 32 + lane;
+            const int e = j * kTile + tok;
+            long long srow = -1;
+            if (e < a.topk) {
+                const int pos = __ldg(a.idx + r * a.topk + e);
+                if (pos >= 0) {
+                    if ((long long)pos < (long long)a.W * a.P) {
+                        const long long i = r / a.next_n;
+                        const int page = __ldg(a.bt + i * a.W + pos / a.P);
+                        if (page >= 0 && (long long)page < a.num_blocks)
+                            srow = (long long)page * a.P + pos % a.P;
+                        else
+                            atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_BLOCK_ID);
+                    } else {
+                        atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_CONTEXT);
+                    }
+                }
+            }
+            if (first) {
+                // the query buffer of segment seg is free once the products of
+                // segment seg - 2 have read it
+                if (!__all_sync(0xFFFFFFFFu,
+                                mbar_wait(&bar[kBarQEmpty + (seg & 1)],
+                                          ((uint32_t)(seg >> 1) & 1u) ^ 1u, abort_flag))) {
+                    fail();
+                    break;
+                }
+                const uint8_t *qsrc = a.q + r * (long long)(kHeads * kDim);
+                const uint32_t qdst = sbase + kOffQ + (uint32_t)(seg & 1) * kQBytes;
+                for (int c = tid; c < kHeads * kChunks; c += kProducers) {
+                    const int h = c / kChunks, ch = c - h * kChunks, kb = ch >> 3, cc = ch & 7;
+                    cp_async_16(qdst + (uint32_t)kb * kQBlk + (uint32_t)h * 128u +
+                                    ((uint32_t)(cc ^ (h & 7)) << 4),
+                                qsrc + h * kDim + ch * 16, 16u);
+                }
+            }
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarKvEmpty + stage], kph ^ 1u, abort_flag))) {
+                fail();
+                break;
+            }
+            flags[stage * kTile + tok] = srow >= 0 ? 1 : 0;
+            const uint32_t dst0 = sbase + kOffKV + (uint32_t)stage * kStageBytes;
+            // value columns: one row per instruction, lane = 16-byte chunk
+#pragma unroll 4
+            for (int tt = 0; tt < 32; ++tt) {
+                const long long sr = __shfl_sync(0xFFFFFFFFu, srow, tt);
+                const int t = pw * 32 + tt;
+                const int kb = lane >> 3, cc = lane & 7;
+                const uint8_t *src = a.kv + (sr >= 0 ? sr : 0ll) * kDim + 16 * lane;
+                cp_async_16(dst0 + (uint32_t)kb * kBlk + (uint32_t)t * 128u +
+                                ((uint32_t)(cc ^ (t & 7)) << 4),
+                            src, sr >= 0 ? 16u : 0u);
+            }
+            // rotary columns: 4 chunks per row, 8 rows per instruction
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int tt = g * 8 + (lane >> 2), cc = lane & 3;
+                const long long sr = __shfl_sync(0xFFFFFFFFu, srow, tt);
+                const int t = pw * 32 + tt;
+                const uint8_t *src = a.kv + (sr >= 0 ? sr : 0ll) * kDim + kVDim + 16 * cc;
+                cp_async_16(dst0 + 4u * kBlk + (uint32_t)t * 128u + ((uint32_t)(cc ^ (t & 7)) << 4),
+                            src, sr >= 0 ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(&bar[kBarFull + stage]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bar[kBarFlags + stage]);
+        }
+        cp_async_wait_all();
+    } else if (tid < kProducers + kSoftmax) {
+        // ------------------------------------------------------------ softmax
+        // Exits are uniform over the 128 threads: a failed wait only clears
+        // `ok`, and the group leaves together at its next barrier (bar.red.and).
+        const int s = tid - kProducers, w4 = s >> 5;
+        const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
+        const int hsel = (lane >> 1) & 15;
+        float m[kHeads], l[kHeads];
+        int seg = -1;
+        bool ok = true;
+        for (long long x = x0; x < x1; ++x) {
+            const int it = (int)(x - x0), stage = it & 1;
+            const uint32_t kph = (uint32_t)(it >> 1) & 1u;
+            const long long r = x / a.T;
+            const int j = (int)(x - r * a.T);
+            const bool first = x == x0 || j == 0;
+            const bool last = x == x1 - 1 || j == a.T - 1;
+            if (first) {
+                ++seg;
+#pragma unroll
+                for (int h = 0; h < kHeads; ++h) {
+                    m[h] = -INFINITY;
+                    l[h] = 0.0f;
+                }
+            }
+            // scores and flags of the tile; the P buffer free once the second
+            // product of tile it - 2 has read it
+            ok = ok && mbar_wait(&bar[kBarSFull + stage], kph, abort_flag) &&
+                 mbar_wait(&bar[kBarFlags + stage], kph, abort_flag) &&
+                 mbar_wait(&bar[kBarPEmpty + stage], kph ^ 1u, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            uint32_t sr[16];
+            if (ok) {
+                tc_fence_after_sync();
+                tmem_ld16(tmem + kColS + (uint32_t)stage * kHeads + lane_off, sr);
+                tmem_ld_wait();
+                reg_fence16(sr);
+                tc_fence_before_sync();
+            } else {
+#pragma unroll
+                for (int h = 0; h < kHeads; ++h)
+                    sr[h] = 0u;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bar[kBarSFree + stage]);
+            const bool valid = flags[stage * kTile + s] != 0;
+            float xs[kHeads];
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h)
+                xs[h] = valid ? __uint_as_float(sr[h]) * a.c_log2 : -INFINITY;
+            // the tile's maximum per head over the 128 positions
+            const float wmax = warp_reduce_scatter16<true>(xs, lane);
+            float *rs = red + stage * 64;
+            if ((lane & 1) == 0)
+                rs[w4 * 16 + hsel] = wmax;
+            if (!named_bar_and(1, kSoftmax, ok)) {
+                fail();
+                break;
+            }
+            float alpha[kHeads];
+            bool resc = false;
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h) {
+                const float tmax = fmaxf(fmaxf(rs[h], rs[16 + h]), fmaxf(rs[32 + h], rs[48 + h]));
+                const float mn = tmax > m[h] + kRescaleSlack ? tmax : m[h];
+                const bool had = m[h] != -INFINITY;
+                alpha[h] = had ? ex2_approx(m[h] - mn) : 1.0f;
+                resc |= had && mn != m[h];
+                m[h] = mn;
+            }
+            float p[kHeads];
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h) {
+                p[h] = ex2_approx(xs[h] - (m[h] == -INFINITY ? 0.0f : m[h]));
+                l[h] = l[h] * alpha[h] + p[h];
+            }
+            const uint32_t pb = sbase + kOffP + (uint32_t)stage * kPBytes;
+#pragma unroll
+            for (int h = 0; h < kHeads; h += 2) {
+                const uint32_t hi = f32x2_to_e4m3x2(p[h], p[h + 1]);
+                float b0, b1;
+                e4m3x2_to_f32x2(hi, b0, b1);
+                const uint32_t lo =
+                    f32x2_to_e4m3x2((p[h] - b0) * kLoScale, (p[h + 1] - b1) * kLoScale);
+                st_shared_u8(pb + p_offset(h, s), hi & 0xFFu);
+                st_shared_u8(pb + p_offset(h + 1, s), hi >> 8);
+                st_shared_u8(pb + p_offset(kHeads + h, s), lo & 0xFFu);
+                st_shared_u8(pb + p_offset(kHeads + h + 1, s), lo >> 8);
+            }
+            if (resc && !first) {
+                // O holds the segment's earlier tiles: wait for the product of
+                // tile it - 1, then scale every column by its head's alpha
+                ok = mbar_wait(&bar[kBarPEmpty + (stage ^ 1)], (uint32_t)((it - 1) >> 1) & 1u,
+                               abort_flag);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (ok) {
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int kb = 0; kb < 4; ++kb) {
+                        uint32_t o[32];
+                        const uint32_t ta = tmem + kColO + (uint32_t)kb * 32u + lane_off;
+                        tmem_ld32(ta, o);
+                        tmem_ld_wait();
+                        reg_fence16(o);
+                        reg_fence16(o + 16);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha[c & 15]);
+                        tmem_st32(ta, o);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bar[kBarPFull + stage]);
+            if (!last)
+                continue;
+
+            // ---------------------------------------------- segment epilogue
+            ok = ok && mbar_wait(&bar[kBarPEmpty + stage], kph, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            const float wl = warp_reduce_scatter16<false>(l, lane);
+            if ((lane & 1) == 0)
+                lred[w4 * 16 + hsel] = wl;
+            if (!named_bar_and(1, kSoftmax, ok)) {
+                fail();
+                break;
+            }
+            tc_fence_after_sync();
+            float L[kHeads];
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h)
+                L[h] = (lred[h] + lred[16 + h]) + (lred[32 + h] + lred[48 + h]);
+            const long long row0 = r * a.T;
+            const int bfirst = cta_of(a, row0);
+            const int nseg = cta_of(a, row0 + a.T - 1) - bfirst + 1;
+            const float ln2 = 0.69314718055994531f;
+            if (nseg == 1) {
+#pragma unroll 1
+                for (int kb = 0; kb < 4; ++kb) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + kColO + (uint32_t)kb * 32u + lane_off, o);
+                    tmem_ld_wait();
+                    reg_fence16(o);
+                    reg_fence16(o + 16);
+#pragma unroll
+                    for (int h = 0; h < kHeads; ++h) {
+                        const float v = __uint_as_float(o[h]) +
+                                        __uint_as_float(o[kHeads + h]) * (1.0f / kLoScale);
+                        const float y = L[h] > 0.0f ? v * (a.kv_scale / L[h]) : 0.0f;
+                        a.out[(r * kHeads + h) * kVDim + kb * 128 + s] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(y));
+                    }
+                }
+                if (a.lse && s < kHeads) {
+                    const float Ls = pick16(L, s), ms = pick16(m, s);
+                    a.lse[r * kHeads + s] = Ls > 0.0f ? (ms + log2f(Ls)) * ln2 : -INFINITY;
+                }
+            } else {
+                const int slot = 2 * (int)blockIdx.x + (seg == 0 ? 0 : 1);
+                float *pp = a.part + (long long)slot * kHeads * kVDim;
+#pragma unroll 1
+                for (int kb = 0; kb < 4; ++kb) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + kColO + (uint32_t)kb * 32u + lane_off, o);
+                    tmem_ld_wait();
+                    reg_fence16(o);
+                    reg_fence16(o + 16);
+#pragma unroll
+                    for (int h = 0; h < kHeads; ++h)
+                        __stcg(pp + h * kVDim + kb * 128 + s,
+                               __uint_as_float(o[h]) +
+                                   __uint_as_float(o[kHeads + h]) * (1.0f / kLoScale));
+                }
+                if (s < kHeads) {
+                    __stcg(a.ml + (slot * kHeads + s) * 2, pick16(m, s));
+                    __stcg(a.ml + (slot * kHeads + s) * 2 + 1, pick16(L, s));
+                }
+                __threadfence();
+                named_bar_sync(1, kSoftmax);
+                if (s == 0) {
+                    const uint32_t old = atomicAdd(a.cnt + r, 1u);
+                    __threadfence();
+                    misc[2] = old == (uint32_t)(nseg - 1) ? 1u : 0u;
+                }
+                named_bar_sync(1, kSoftmax);
+                if (misc[2]) {
+                    // the last part of the row to arrive: combine all of them
+                    __threadfence();
+                    float M[kHeads], Lt[kHeads];
+#pragma unroll
+                    for (int h = 0; h < kHeads; ++h) {
+                        M[h] = -INFINITY;
+                        Lt[h] = 0.0f;
+                    }
+                    for (int q = 0; q < nseg; ++q) {
+                        const int bb = bfirst + q;
+                        const int sl = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
+#pragma unroll
+                        for (int h = 0; h < kHeads; ++h)
+                            M[h] = fmaxf(M[h], ld_cg(a.ml + (sl * kHeads + h) * 2));
+                    }
+                    float acc[4][kHeads];
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+                        for (int h = 0; h < kHeads; ++h)
+                            acc[kb][h] = 0.0f;
+                    for (int q = 0; q < nseg; ++q) {
+                        const int bb = bfirst + q;
+                        const int sl = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
+                        const float *sp = a.part + (long long)sl * kHeads * kVDim;
+#pragma unroll
+                        for (int h = 0; h < kHeads; ++h) {
+                            const float mq = ld_cg(a.ml + (sl * kHeads + h) * 2);
+                            const float lq = ld_cg(a.ml + (sl * kHeads + h) * 2 + 1);
+                            const float wq = mq == -INFINITY ? 0.0f : ex2_approx(mq - M[h]);
+                            Lt[h] += wq * lq;
+#pragma unroll
+                            for (int kb = 0; kb < 4; ++kb)
+                                acc[kb][h] += wq * ld_cg(sp + h * kVDim + kb * 128 + s);
+                        }
+                    }
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+                        for (int h = 0; h < kHeads; ++h) {
+                            const float y =
+                                Lt[h] > 0.0f ? acc[kb][h] * (a.kv_scale / Lt[h]) : 0.0f;
+                            a.out[(r * kHeads + h) * kVDim + kb * 128 + s] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(y));
+                        }
+                    if (a.lse && s < kHeads) {
+                        const float Ls = pick16(Lt, s), Ms = pick16(M, s);
+                        a.lse[r * kHeads + s] = Ls > 0.0f ? (Ms + log2f(Ls)) * ln2 : -INFINITY;
+                    }
+                    if (s == 0)
+                        a.cnt[r] = 0u;  // ready for the next call
+                }
+            }
+        }
+    } else if (warp == kMmaWarp && lane == 0) {
+        // ------------------------------------------------------------ MMA issue
+        int seg = -1, prev_it = -1;
+        bool prev_first = false, ok = true;
+        auto issue_pv = [&](int pit, bool pfirst) -> bool {
+            const int st = pit & 1;
+            if (!mbar_wait(&bar[kBarPFull + st], (uint32_t)(pit >> 1) & 1u, abort_flag))
+                return false;
+            tc_fence_after_sync();
+            const uint32_t kvs = sbase + kOffKV + (uint32_t)st * kStageBytes;
+            const uint32_t pb = sbase + kOffP + (uint32_t)st * kPBytes;
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_e4m3(tmem + kColO + (uint32_t)kb * 32u,
+                              sw128_mnmajor_desc(kvs + (uint32_t)kb * kBlk + (uint32_t)ks * 4096u,
+                                                 kBlk, 1024u),
+                              sw128_kmajor_desc(pb + (uint32_t)ks * 32u), kIdescPV,
+                              (pfirst && ks == 0) ? 0u : 1u);
+            umma_commit(&bar[kBarKvEmpty + st]);
+            umma_commit(&bar[kBarPEmpty + st]);
+            return true;
+        };
+        for (long long x = x0; x < x1 && ok; ++x) {
+            const int it = (int)(x - x0), stage = it & 1;
+            const uint32_t kph = (uint32_t)(it >> 1) & 1u;
+            const long long r = x / a.T;
+            const int j = (int)(x - r * a.T);
+            const bool first = x == x0 || j == 0;
+            const bool last = x == x1 - 1 || j == a.T - 1;
+            if (first)
+                ++seg;
+            if (!mbar_wait(&bar[kBarFull + stage], kph, abort_flag) ||
+                !mbar_wait(&bar[kBarSFree + stage], kph ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
+            tc_fence_after_sync();
+            const uint32_t kvs = sbase + kOffKV + (uint32_t)stage * kStageBytes;
+            const uint32_t qs = sbase + kOffQ + (uint32_t)(seg & 1) * kQBytes;
+#pragma unroll
+            for (int kb = 0; kb < 5; ++kb)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    if (kb == 4 && ks >= 2)
+                        break;  // the rotary block holds 64 columns
+                    umma_e4m3(tmem + kColS + (uint32_t)stage * kHeads,
+                              sw128_kmajor_desc(kvs + (uint32_t)kb * kBlk + (uint32_t)ks * 32u),
+                              sw128_kmajor_desc(qs + (uint32_t)kb * kQBlk + (uint32_t)ks * 32u),
+                              kIdescQK, (kb | ks) != 0 ? 1u : 0u);
+                }
+            umma_commit(&bar[kBarSFull + stage]);
+            if (last)
+                umma_commit(&bar[kBarQEmpty + (seg & 1)]);
+            if (prev_it >= 0 && !issue_pv(prev_it, prev_first)) {
+                ok = false;
+                break;
+            }
+            prev_it = it;
+            prev_first = first;
+        }
+        if (ok && prev_it >= 0)
+            ok = issue_pv(prev_it, prev_first);
+        if (!ok)
+            fail();
+        umma_commit(&bar[kBarDrain]);
+        if (!mbar_wait(&bar[kBarDrain], 0u, nullptr))
+            atomicOr(a.status, (uint32_t)PMQA_DEV_TIMEOUT);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Workspace: status word | per-row arrival counters | (m, l) of each part |
+// the parts' unnormalised outputs.
+struct WsLayout {
+    size_t cnt, ml, part, total;
+};
+
+bool ws_layout(long long rows, WsLayout *L)
+{
+    if (rows < 0)
+        return false;
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    L->cnt = 256;
+    L->ml = L->cnt + up((size_t)rows * 4);
+    L->part = L->ml + up((size_t)2 * kMaxCtas * kHeads * 2 * 4);
+    L->total = L->part + (size_t)2 * kMaxCtas * kHeads * kVDim * 4;
+    return true;
+}
+
+}  // namespace mla
+}  // namespace pmqa
+
+using namespace pmqa::mla;
+
+extern "C" size_t pmqa_sparse_mla_workspace_bytes(int32_t rows)
+{
+    WsLayout L;
+    if (!ws_layout(rows, &L))
+        return 0;
+    return L.total;
+}
+
+extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, float *lse, void *ws,
+                                      size_t ws_bytes, pmqa_stream_t stream)
+{
+    auto aligned = [](const void *ptr, uintptr_t al) {
+        return (reinterpret_cast<uintptr_t>(ptr) % al) == 0;
+    };
+    if (!p || p->bs < 0 || p->next_n < 1 || p->topk < 0 || p->block_size < 1 ||
+        p->max_blocks_per_seq < 1 || p->num_blocks < 1 || p->heads < 1 || p->head_dim < 1 ||
+        p->v_head_dim < 1)
+        return PMQA_ERR_INVALID_ARG;
+    if (p->heads != kHeads || p->head_dim != kDim || p->v_head_dim != kVDim)
+        return PMQA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(p->q_scale) && std::isfinite(p->kv_scale) && std::isfinite(p->sm_scale)))
+        return PMQA_ERR_INVALID_ARG;
+    const long long rows = (long long)p->bs * p->next_n;
+    WsLayout L;
+    if (!ws_layout(rows, &L))
+        return PMQA_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, 256))
+        return PMQA_ERR_INVALID_ARG;
+    if (ws_bytes < L.total)
+        return PMQA_ERR_WORKSPACE;
+    if (rows == 0)
+        return PMQA_OK;
+    if (!p->q || !p->kv_cache || !p->indices || !p->block_tables || !out)
+        return PMQA_ERR_INVALID_ARG;
+    if (!aligned(p->q, 16) || !aligned(p->kv_cache, 16) || !aligned(p->indices, 4) ||
+        !aligned(p->block_tables, 4) || !aligned(out, 4) || (lse && !aligned(lse, 4)))
+        return PMQA_ERR_INVALID_ARG;
+    const long long T = std::max<long long>(1, (p->topk + kTile - 1) / kTile);
+    if (rows * T > (1ll << 40))
+        return PMQA_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PMQA_ERR_CUDA;
+    Args a{};
+    a.q = static_cast<const uint8_t *>(p->q);
+    a.kv = static_cast<const uint8_t *>(p->kv_cache);
+    a.idx = p->indices;
+    a.bt = p->block_tables;
+    a.c_log2 = (float)((double)p->sm_scale * (double)p->q_scale * (double)p->kv_scale *
+                       1.4426950408889634);
+    a.kv_scale = p->kv_scale;
+    a.next_n = p->next_n;
+    a.topk = p->topk;
+    a.T = (int)T;
+    a.P = p->block_size;
+    a.W = p->max_blocks_per_seq;
+    a.num_blocks = p->num_blocks;
+    a.N = rows * T;
+    a.G = (int)std::min<long long>(a.N, std::min(sms, kMaxCtas));
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    a.out = static_cast<uint16_t *>(out);
+    a.lse = lse;
+    a.status = reinterpret_cast<uint32_t *>(wsb);
+    a.cnt = reinterpret_cast<uint32_t *>(wsb + L.cnt);
+    a.ml = reinterpret_cast<float *>(wsb + L.ml);
+    a.part = reinterpret_cast<float *>(wsb + L.part);
+    if (cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+        return PMQA_ERR_CUDA;
+    sparse_mla_kernel<<<a.G, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
+}

@@ -37,8 +37,8 @@ EXPORTED = (
     "pmqa_workspace_bytes", "pmqa_workspace_init", "pmqa_logits", "pmqa_topk",
     "pmqa_logits_topk", "pmqa_logits_topk_stages", "pmqa_logits_topk_noalloc",
     "pmqa_logits_topk_range",
-    "pmqa_mqa_logits", "pmqa_topk_merge", "pmqa_read_device_status",
-    "pmqa_status_string", "pmqa_version",
+    "pmqa_mqa_logits", "pmqa_topk_merge", "pmqa_sparse_mla_workspace_bytes",
+    "pmqa_sparse_mla_decode", "pmqa_read_device_status", "pmqa_status_string", "pmqa_version",
 )
 
 
@@ -85,6 +85,29 @@ class MqaProblem(ctypes.Structure):
     ]
 
 
+class MlaProblem(ctypes.Structure):
+    """Mirror of struct pmqa_mla_problem."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("kv_cache", ctypes.c_void_p),
+        ("indices", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p),
+        ("q_scale", ctypes.c_float),
+        ("kv_scale", ctypes.c_float),
+        ("sm_scale", ctypes.c_float),
+        ("bs", ctypes.c_int32),
+        ("next_n", ctypes.c_int32),
+        ("heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("v_head_dim", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int64),
+    ]
+
+
 _lib = None
 
 
@@ -105,6 +128,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     PP = ctypes.POINTER(Problem)
     PM = ctypes.POINTER(MqaProblem)
+    PL = ctypes.POINTER(MlaProblem)
     sig = {
         "pmqa_workspace_bytes": ([I32, I32, I32, I32, ctypes.c_int], SZ),
         "pmqa_workspace_init": ([V, SZ, V], ctypes.c_int),
@@ -116,6 +140,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pmqa_logits_topk_range": ([PP, V, V, I32, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_mqa_logits": ([PM, V, V, SZ, V], ctypes.c_int),
         "pmqa_topk_merge": ([V, V, I32, I32, I32, I32, V, V, V], ctypes.c_int),
+        "pmqa_sparse_mla_workspace_bytes": ([I32], SZ),
+        "pmqa_sparse_mla_decode": ([PL, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_read_device_status": ([V, V], ctypes.c_int),
         "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pmqa_version": ([], ctypes.c_int),
@@ -326,6 +352,61 @@ def pmqa_topk_merge(idx, vals, k: int, *, out_idx=None, out_vals=None, want_vals
     _check(load().pmqa_topk_merge(_ptr(idx), _ptr(vals), lists, rows, k_in, k, _ptr(out_idx),
                                   _ptr(out_vals), _stream(stream)), "pmqa_topk_merge")
     return (out_idx, out_vals) if want_vals or out_vals is not None else out_idx
+
+
+def make_mla_problem(q, kv_cache, indices, block_tables, next_n: int, q_scale: float,
+                     kv_scale: float, sm_scale: float) -> MlaProblem:
+    """Fill a pmqa_mla_problem from tensors shaped as in the C header (q may
+    also be given as [bs, next_n, heads, 576])."""
+    bs = block_tables.shape[0]
+    heads, head_dim = q.shape[-2], q.shape[-1]
+    rows = q.numel() // (heads * head_dim)
+    assert rows == bs * next_n and indices.shape[0] == rows
+    num_blocks, block_size = kv_cache.shape[0], kv_cache.shape[1]
+    assert kv_cache.shape[-1] == head_dim
+    for t in (q, kv_cache, indices, block_tables):
+        assert t.is_cuda and t.is_contiguous()
+    return MlaProblem(q=q.data_ptr(), kv_cache=kv_cache.data_ptr(), indices=indices.data_ptr(),
+                      block_tables=block_tables.data_ptr(), q_scale=q_scale, kv_scale=kv_scale,
+                      sm_scale=sm_scale, bs=bs, next_n=next_n, heads=heads, head_dim=head_dim,
+                      v_head_dim=512, topk=indices.shape[1], block_size=block_size,
+                      max_blocks_per_seq=block_tables.shape[1], num_blocks=num_blocks)
+
+
+def pmqa_sparse_mla_workspace_bytes(rows: int) -> int:
+    return int(load().pmqa_sparse_mla_workspace_bytes(rows))
+
+
+def mla_workspace(rows: int, device=None, stream=None):
+    """A zero-initialised workspace for pmqa_sparse_mla_decode."""
+    import torch
+
+    n = pmqa_sparse_mla_workspace_bytes(rows)
+    if n == 0:
+        raise PmqaError(PMQA_ERR_INVALID_ARG, "pmqa_sparse_mla_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    pmqa_workspace_init(ws, stream=stream)
+    return ws
+
+
+def pmqa_sparse_mla_decode(q, kv_cache, indices, block_tables, next_n: int, q_scale: float,
+                           kv_scale: float, sm_scale: float, *, out=None, lse=None,
+                           want_lse: bool = False, ws=None, stream=None):
+    """Sparse MLA decode over the listed positions: bf16 out [rows, heads, 512]
+    (and fp32 lse [rows, heads] when asked for or given)."""
+    import torch
+
+    p = make_mla_problem(q, kv_cache, indices, block_tables, next_n, q_scale, kv_scale, sm_scale)
+    rows = p.bs * p.next_n
+    if out is None:
+        out = torch.empty((rows, p.heads, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((rows, p.heads), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = mla_workspace(rows, q.device, stream)
+    _check(load().pmqa_sparse_mla_decode(ctypes.byref(p), _ptr(out), _ptr(lse), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "pmqa_sparse_mla_decode")
+    return (out, lse) if want_lse or lse is not None else out
 
 
 def pmqa_read_device_status(ws, stream=None) -> int:

@@ -1,0 +1,171 @@
+"""Sparse MLA decode on the GPU against the oracle, element by element.
+
+Tolerance per output entry (derived from the kernel's arithmetic): scores
+within e_s = 2^-9 * s_abs of exact (fp8 products summed on the tensor cores),
+which moves an output by at most e_s * d_abs; the softmax weights enter the
+second product as two fp8 terms (relative error 2^-8), at most 2^-7 * a_abs
+with margin; the bf16 output rounds by 2^-9 relative, 2^-8 |out| with margin.
+lse within e_s + 1e-4; empty rows exactly 0 and -inf. a_abs, d_abs and s_abs
+are the oracle's (sum p |v|, sum p |v - out|, max score magnitude).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth.inputs import to_e4m3fn_bytes
+from synth.mla import MLA_DIM, MlaProblem, make_mla_problem, mla_config
+
+pytestmark = pytest.mark.gpu
+
+
+def run(lib, prob, *, ws=None):
+    dev = "cuda"
+    q = torch.from_numpy(prob.q.reshape(prob.rows, prob.heads, MLA_DIM)).to(dev)
+    kv = torch.from_numpy(prob.kv).to(dev)
+    idx = torch.from_numpy(prob.indices).to(dev)
+    bt = torch.from_numpy(prob.block_tables).to(dev)
+    if ws is None:
+        ws = lib.mla_workspace(prob.rows)
+    out, lse = lib.pmqa_sparse_mla_decode(q, kv, idx, bt, prob.next_n, prob.q_scale,
+                                          prob.kv_scale, prob.sm_scale, want_lse=True, ws=ws)
+    torch.cuda.synchronize()
+    status = lib.pmqa_read_device_status(ws)
+    return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), status
+
+
+def check(out, lse, prob, rows=None):
+    ref, lref, tol = oracle.sparse_mla(prob, rows=rows, want_tol=True)
+    if rows is not None:
+        out, lse = out[rows], lse[rows]
+    e_s = 2.0 ** -9 * tol["s_abs"]
+    bound = e_s[..., None] * tol["d_abs"] + 2.0 ** -7 * tol["a_abs"] + 2.0 ** -8 * np.abs(ref) + 1e-6
+    err = np.abs(out - ref)
+    bad = err > bound
+    assert not bad.any(), (
+        f"{int(bad.sum())} outputs beyond tolerance; worst excess "
+        f"{float((err - bound).max()):.3g} at {np.unravel_index(np.argmax(err - bound), err.shape)}")
+    empty = np.isneginf(lref)
+    assert np.array_equal(np.isneginf(lse), empty), "-inf pattern of lse"
+    assert (out[empty] == 0).all()
+    fin = ~empty
+    lerr = np.abs(lse[fin] - lref[fin])
+    assert (lerr <= e_s[fin] + 1e-4).all(), f"lse error {lerr.max():.3g}"
+    # the pages' agreement measure: cos_diff = 1 - 2 <x, y> / (|x|^2 + |y|^2)
+    den = (out * out).sum() + (ref * ref).sum()
+    cos_diff = 1.0 - 2.0 * (out * ref).sum() / den if den > 0 else 0.0
+    return float(err.max()), float(cos_diff)
+
+
+@pytest.mark.parametrize("bs,nn,P,ctx,topk,kw", [
+    (1, 1, 1, [300], 2048, {}),                               # one row, ragged last tile
+    (2, 3, 1, [900, 3000], 512, dict(holes=0.1)),             # holes anywhere
+    (2, 4, 1, [5000, 2049], 2048, dict(repeats=0.05)),        # repeated positions
+    (3, 2, 64, [7000, 129, 4097], 1000, {}),                  # pages of 64, topk % 128 != 0
+    (4, 1, 1, [0, 3, 1, 2500], 256, {}),                      # empty and tiny rows
+])
+def test_parity_small(cuda_lib, bs, nn, P, ctx, topk, kw):
+    prob = make_mla_problem(bs, nn, 16, P, ctx, topk=topk, seed=sum(ctx) + topk, **kw)
+    out, lse, status = run(cuda_lib, prob)
+    assert status == 0
+    check(out, lse, prob)
+
+
+@pytest.mark.parametrize("scale", [4.0, 16.0])
+def test_peaked_scores_move_the_running_maximum(cuda_lib, scale):
+    """sm_scale 4x and 16x the default: scores spread over tens of units, so
+    the reference maximum moves inside a row and O is rescaled in TMEM."""
+    prob = make_mla_problem(4, 2, 16, 1, [6000, 3000, 9000, 2048], seed=int(scale),
+                            sm_scale=scale * MLA_DIM ** -0.5)
+    out, lse, status = run(cuda_lib, prob)
+    assert status == 0
+    check(out, lse, prob)
+
+
+def test_increasing_scores_rescale_every_tile(cuda_lib):
+    """Listed positions ordered so each tile's scores exceed the last by more
+    than the rescale slack: O is rescaled at every tile of the row."""
+    prob = make_mla_problem(1, 1, 16, 1, [2048], seed=11, sm_scale=8 * MLA_DIM ** -0.5)
+    ref, _, _ = oracle.sparse_mla(prob)
+    # order the row's positions by their head-0 score, lowest first
+    qd = oracle.e4m3fn_table()[prob.q.reshape(16, MLA_DIM)[0].astype(np.int64)]
+    kd = oracle.e4m3fn_table()[prob.kv[prob.block_tables[0, prob.indices[0]], 0].astype(np.int64)]
+    prob.indices[0] = prob.indices[0][np.argsort(kd @ qd)]
+    out, lse, status = run(cuda_lib, prob)
+    assert status == 0
+    check(out, lse, prob)
+
+
+def test_zero_query_is_the_mean(cuda_lib):
+    prob = make_mla_problem(2, 2, 16, 1, [3000, 700], seed=3)
+    prob.q[:] = 0
+    out, lse, status = run(cuda_lib, prob)
+    assert status == 0
+    check(out, lse, prob)
+    n = (prob.indices >= 0).sum(axis=1)
+    np.testing.assert_allclose(lse, np.log(n)[:, None].repeat(16, axis=1), rtol=0, atol=1e-5)
+
+
+def test_one_dominant_position(cuda_lib):
+    """One listed position scores 448 * 448 above the rest: its value row
+    comes out (to bf16 rounding)."""
+    prob = make_mla_problem(1, 1, 16, 1, [4000], topk=2048, seed=5)
+    q = np.zeros((16, MLA_DIM), dtype=np.uint8)
+    q[:, 0] = to_e4m3fn_bytes(np.array([448.0], dtype=np.float32))[0]
+    prob.q[:] = q.reshape(prob.q.shape)
+    slots = prob.block_tables[0, prob.indices[0]]
+    prob.kv[slots, 0, 0] = 0
+    prob.kv[slots[1500], 0, 0] = to_e4m3fn_bytes(np.array([448.0], dtype=np.float32))[0]
+    prob.sm_scale = 1.0
+    out, lse, status = run(cuda_lib, prob)
+    assert status == 0
+    check(out, lse, prob)
+
+
+def test_many_rows_split_over_ctas(cuda_lib):
+    """More tiles than CTAs with rows split at arbitrary tile boundaries (parts
+    combined by the last CTA to finish), and fewer tiles than SMs (every CTA
+    one tile, a row combined from up to 16 parts)."""
+    for bs, nn, seed in ((37, 3, 1), (1, 4, 2)):
+        ctx = np.random.default_rng(seed).integers(2100, 9000, size=bs)
+        prob = make_mla_problem(bs, nn, 16, 1, ctx, seed=seed)
+        out, lse, status = run(cuda_lib, prob)
+        assert status == 0
+        check(out, lse, prob)
+
+
+def test_workspace_is_reusable(cuda_lib):
+    """The arrival counters return to zero: three calls on one workspace agree
+    bit for bit."""
+    prob = make_mla_problem(9, 4, 16, 1, [4000] * 9, seed=8)
+    ws = cuda_lib.mla_workspace(prob.rows)
+    first = run(cuda_lib, prob, ws=ws)
+    for _ in range(2):
+        again = run(cuda_lib, prob, ws=ws)
+        assert np.array_equal(again[0], first[0]) and np.array_equal(again[1], first[1])
+
+
+def test_positions_outside_the_table_are_skipped_and_flagged(cuda_lib):
+    prob = make_mla_problem(1, 2, 16, 1, [1000], topk=256, seed=4)
+    bad = prob.indices.copy()
+    bad[0, 7] = prob.max_blocks_per_seq + 5      # past the table
+    prob_bad = MlaProblem(**{**prob.__dict__, "indices": bad})
+    out, lse, status = run(cuda_lib, prob_bad)
+    assert status & cuda_lib.PMQA_DEV_BAD_CONTEXT
+    skipped = MlaProblem(**{**prob.__dict__, "indices": bad.copy()})
+    skipped.indices[0, 7] = -1
+    check(out, lse, skipped)
+
+
+@pytest.mark.parametrize("name", ["M0", "M1", "M2"])
+def test_workloads_sampled_rows(cuda_lib, name):
+    """The full workloads in the benchmark's launch; the oracle checks a sample
+    of rows (all rows of M0)."""
+    prob = mla_config(name)
+    out, lse, status = run(cuda_lib, prob)
+    assert status == 0
+    rng = np.random.default_rng(0)
+    rows = None if prob.rows <= 8 else np.sort(rng.choice(prob.rows, 8, replace=False))
+    _, cos_diff = check(out, lse, prob, rows=rows)
+    assert cos_diff < 1e-4
