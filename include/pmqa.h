@@ -314,18 +314,18 @@ typedef struct pmqa_mla_problem {
 } pmqa_mla_problem;
 
 /* Bytes of workspace for pmqa_sparse_mla_decode over `rows` query rows (about
-   17 MB plus 4 bytes per row); 0 for rows < 0. */
+   17 MB, whatever the row count); 0 for rows < 0. */
 size_t pmqa_sparse_mla_workspace_bytes(int32_t rows);
 
 /*
  * out: bf16 [bs * next_n, heads, 512], 4-byte aligned; lse: fp32
  * [bs * next_n, heads] or NULL. ws: pmqa_sparse_mla_workspace_bytes(rows)
- * bytes, 256-byte aligned, zero-filled before its first use
- * (pmqa_workspace_init); every call leaves it zero-filled again except the
- * status word. A listed position past the block table sets PMQA_DEV_BAD_CONTEXT,
- * a table entry outside [0, num_blocks) PMQA_DEV_BAD_BLOCK_ID (the position
- * is then skipped); a pipeline wait that ran out sets PMQA_DEV_TIMEOUT (results
- * invalid, re-initialise the workspace). One kernel launch.
+ * bytes, 256-byte aligned, its status word zero before the first use
+ * (pmqa_workspace_init). A listed position past the block table sets
+ * PMQA_DEV_BAD_CONTEXT, a table entry outside [0, num_blocks)
+ * PMQA_DEV_BAD_BLOCK_ID (the position is then skipped); a pipeline wait that
+ * ran out sets PMQA_DEV_TIMEOUT (results invalid). Two kernel launches: the
+ * attention, and the combination of rows whose tiles were split over CTAs.
  */
 int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, float *lse, void *ws,
                            size_t ws_bytes, pmqa_stream_t stream);

@@ -16,9 +16,13 @@
 //
 // One persistent CTA per SM walks a contiguous range of the flattened
 // (row, 128-position tile) sequence. Per tile:
-//   * 128 producer threads gather the 128 listed latent rows (576 bytes each)
-//     with 16-byte cp.async straight into the 128-byte-swizzled operand layout:
-//     four 16 KB blocks of value columns and one block for the rotary columns;
+//   * one warp looks up the 128 listed positions in the block table (two
+//     tiles ahead) and moves each latent row (576 bytes) with one 1-D bulk
+//     copy; the rows of 8 positions land back to back in a 5120-byte group;
+//   * four warps permute each group in place into the operand layout: five
+//     1024-byte blocks of 8 rows x 128 bytes in the 128-byte swizzle (four
+//     blocks of value columns, one of rotary columns, half used), groups 5120
+//     bytes apart, so every swizzle atom stays 1024-byte aligned;
 //   * one thread issues S^T = K . Q^T on the tensor cores (M = 128 positions,
 //     N = 16 heads, K = 576) into TMEM;
 //   * 128 softmax threads (one TMEM lane = one position each) take the tile's
@@ -27,7 +31,7 @@
 //     as two fp8 terms p_hi = e4m3(p), p_lo = e4m3(16 (p - p_hi)) into a
 //     K-major operand of 32 rows (16 hi + 16 lo heads);
 //   * the thread issues O^T += V^T . P^T (M = 128 value columns per block, four
-//     blocks, N = 32, K = 128 positions), reading the SAME gathered tile as an
+//     blocks, N = 32, K = 128 positions), reading the SAME tile as an
 //     MN-major operand, into four TMEM accumulators of 32 columns.
 // A row's tiles split over at most a few CTAs: each writes its unnormalised
 // part (O, m, l) to the workspace and the last to arrive combines them.
@@ -50,21 +54,23 @@ constexpr int kVDim = 512;   // value columns
 constexpr int kHeads = 16;   // query heads per latent KV head
 constexpr int kTile = 128;   // listed positions per tile (the first product's M)
 constexpr int kChunks = kDim / 16;
-constexpr uint32_t kBlk = 128u * 128u;          // one 128-byte column block of a tile
-constexpr uint32_t kStageBytes = 5u * kBlk;     // 4 value blocks + the rotary block
-constexpr uint32_t kQBlk = 16u * 128u;          // one column block of the 16 query heads
-constexpr uint32_t kQBytes = 5u * kQBlk;
-constexpr uint32_t kPBytes = 32u * 128u;        // 32 rows (hi, lo) x 128 positions
-constexpr int kProducers = 128;
-constexpr int kSoftmax = 128;
-constexpr int kThreads = kProducers + kSoftmax + 32;
-constexpr int kMmaWarp = (kProducers + kSoftmax) / 32;
-constexpr int kMaxCtas = 256;                   // workspace parts: 2 per CTA
+constexpr uint32_t kGroup = 5u * 1024u;           // 8 rows: 5 swizzled 1024-byte blocks
+constexpr uint32_t kStageBytes = 16u * kGroup;    // 128 rows
+constexpr uint32_t kQBytes = 2u * kGroup;         // 16 query heads
+constexpr uint32_t kPBytes = 32u * 128u;          // 32 rows (hi, lo) x 128 positions
+constexpr int kProducers = 128;                   // warps 0-3
+constexpr int kSoftmax = 128;                     // warps 4-7
+constexpr int kMmaWarp = 8;
+constexpr int kThreads = 288;
+constexpr int kMaxCtas = 256;                     // workspace parts: 2 per CTA
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;                   // 2 x 16 score columns
-constexpr uint32_t kColO = 128;                 // 4 x 32 output columns
-constexpr float kLoScale = 16.0f;               // p_lo holds 16 (p - p_hi)
-constexpr float kRescaleSlack = 8.0f;           // p <= 2^8 before the maximum moves
+constexpr uint32_t kColS = 0;                     // 2 x 16 score columns
+constexpr uint32_t kColO = 128;                   // 4 x 32 output columns
+constexpr float kLoScale = 16.0f;                 // p_lo holds 16 (p - p_hi)
+constexpr float kRescaleSlack = 8.0f;             // p <= 2^8 before the maximum moves
+#ifndef PMQA_MLA_MIN_TILES
+#define PMQA_MLA_MIN_TILES 1                      // fewest tiles a CTA takes (small problems)
+#endif
 
 constexpr uint32_t kOffKV = 0;
 constexpr uint32_t kOffQ = 2u * kStageBytes;
@@ -74,14 +80,14 @@ constexpr uint32_t kOffRed = kOffFlags + 2u * kTile;          // [2][4 warps][16
 constexpr uint32_t kOffLred = kOffRed + 2u * 4u * 16u * 4u;   // [4 warps][16] floats
 constexpr uint32_t kOffBar = kOffLred + 4u * 16u * 4u;
 enum {
-    kBarFull = 0,      // [2] tile (and query) rows landed: 128 producer arrivals
-    kBarKvEmpty = 2,   // [2] products of the tile done: MMA commit
-    kBarSFull = 4,     // [2] scores in TMEM: MMA commit
-    kBarSFree = 6,     // [2] scores read: one arrival per softmax warp
-    kBarPFull = 8,     // [2] P written (and O rescaled): one arrival per softmax warp
-    kBarPEmpty = 10,   // [2] P read by the second product: MMA commit
-    kBarQEmpty = 12,   // [2] query buffer read: MMA commit after a row's last tile
-    kBarFlags = 14,    // [2] tile position flags written: one arrival per producer warp
+    kBarFlags = 0,     // [2] tile position flags written: one arrival per producer warp
+    kBarReady = 2,     // [2] tile (and query) rows landed: 128 producer cp.async arrivals
+    kBarKvEmpty = 4,   // [2] products of the tile done: MMA commit
+    kBarSFull = 6,     // [2] scores in TMEM: MMA commit
+    kBarSFree = 8,     // [2] scores read: one arrival per softmax warp
+    kBarPFull = 10,    // [2] P written (and O rescaled): one arrival per softmax warp
+    kBarPEmpty = 12,   // [2] P read by the second product: MMA commit
+    kBarQEmpty = 14,   // [2] query buffer read: MMA commit after a row's last tile
     kBarDrain = 16,    // MMAs drained before TMEM is freed
     kNumBars = 17
 };
@@ -91,6 +97,14 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdescQK = idesc_e4m3_f32(128, kHeads);
 constexpr uint32_t kIdescPV = idesc_e4m3_f32(128, 2 * kHeads) | kIdescAMnMajor;
+
+// Byte offset, inside a tile or the query buffer, of 16-byte chunk c (0..35)
+// of row t in the operand layout.
+__host__ __device__ constexpr uint32_t chunk_offset(int t, int c)
+{
+    return (uint32_t)(t >> 3) * kGroup + (uint32_t)(c >> 3) * 1024u + (uint32_t)(t & 7) * 128u +
+           ((uint32_t)((c & 7) ^ (t & 7)) << 4);
+}
 
 struct Args {
     const uint8_t *q;     // [R, 16, 576]
@@ -106,7 +120,6 @@ struct Args {
     uint16_t *out;        // bf16 [R, 16, 512]
     float *lse;           // [R, 16] or null
     uint32_t *status;
-    uint32_t *cnt;        // [R] arrivals of a row's parts
     float *ml;            // [2 G][16][2] (m, l) of each part
     float *part;          // [2 G][16][512] unnormalised output of each part
 };
@@ -200,14 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar[kBarFull + i], kProducers);
+            mbar_init(&bar[kBarFlags + i], kProducers / 32);
+            mbar_init(&bar[kBarReady + i], kProducers);
             mbar_init(&bar[kBarKvEmpty + i], 1);
             mbar_init(&bar[kBarSFull + i], 1);
             mbar_init(&bar[kBarSFree + i], kSoftmax / 32);
             mbar_init(&bar[kBarPFull + i], kSoftmax / 32);
             mbar_init(&bar[kBarPEmpty + i], 1);
             mbar_init(&bar[kBarQEmpty + i], 1);
-            mbar_init(&bar[kBarFlags + i], kProducers / 32);
         }
         mbar_init(&bar[kBarDrain], 1);
         misc[1] = 0;
@@ -220,15 +233,63 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
     tc_fence_after_sync();
     const uint32_t tmem = misc[0];
 
+    // the combining kernel may be scheduled now; it waits for this grid
+    griddep_launch_dependents();
     const long long x0 = tile_start(a, blockIdx.x), x1 = tile_start(a, blockIdx.x + 1);
     auto fail = [&]() {
         atomicOr(a.status, (uint32_t)PMQA_DEV_TIMEOUT);
         *abort_flag = 1;
     };
 
-    if (tid < kProducers) {
+    if (warp < kProducers / 32) {
         // ------------------------------------------------------------ producer
-        const int pw = tid >> 5;
+        // Thread tok owns position tok of every tile; warp w copies the rows
+        // of positions 32w .. 32w+31, one row per instruction (lane = 16-byte
+        // chunk), straight into the operand layout. Lookups run ahead of the
+        // copies: the listed position of tile it + 3 and the block table
+        // entry of tile it + 2 load while tile it is issued, and the row of
+        // tile it + 1 is prefetched into L2.
+        const int pw = warp, tok = tid;
+        const long long wp = (long long)a.W * a.P;
+        auto load_pos = [&](long long x) -> int {
+            if (x >= x1)
+                return -1;
+            const long long r = x / a.T;
+            const int e = (int)(x - r * a.T) * kTile + tok;
+            return e < a.topk ? __ldg(a.idx + r * a.topk + e) : -1;
+        };
+        auto load_page = [&](long long x, int pos) -> int {
+            if (x >= x1 || pos < 0 || (long long)pos >= wp)
+                return -1;
+            return __ldg(a.bt + (x / a.T) / a.next_n * a.W + pos / a.P);
+        };
+        // pool row of a looked-up position, -1 for none; `report` records bad entries
+        auto row_of = [&](int pos, int page, bool report) -> long long {
+            if (pos < 0)
+                return -1;
+            if ((long long)pos >= wp) {
+                if (report)
+                    atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_CONTEXT);
+                return -1;
+            }
+            if (page < 0 || (long long)page >= a.num_blocks) {
+                if (report)
+                    atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_BLOCK_ID);
+                return -1;
+            }
+            return (long long)page * a.P + pos % a.P;
+        };
+        auto prefetch_row = [&](long long row) {
+            if (row < 0)
+                return;
+            const uint8_t *p = a.kv + row * kDim;
+#pragma unroll
+            for (int k = 0; k < 5; ++k)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128 * k));
+        };
+        int pos0 = load_pos(x0), pos1 = load_pos(x0 + 1), pos2 = load_pos(x0 + 2);
+        int page0 = load_page(x0, pos0), page1 = load_page(x0 + 1, pos1);
+        prefetch_row(row_of(pos0, page0, false));
         int seg = -1;
         for (long long x = x0; x < x1; ++x) {
             const int it = (int)(x - x0), stage = it & 1;
@@ -238,25 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
             const bool first = x == x0 || j == 0;
             if (first)
                 ++seg;
-            // this lane's position of the tile and its pool row (-1: none)
-            const int tok = pw * 32 + lane;
-            const int e = j * kTile + tok;
-            long long srow = -1;
-            if (e < a.topk) {
-                const int pos = __ldg(a.idx + r * a.topk + e);
-                if (pos >= 0) {
-                    if ((long long)pos < (long long)a.W * a.P) {
-                        const long long i = r / a.next_n;
-                        const int page = __ldg(a.bt + i * a.W + pos / a.P);
-                        if (page >= 0 && (long long)page < a.num_blocks)
-                            srow = (long long)page * a.P + pos % a.P;
-                        else
-                            atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_BLOCK_ID);
-                    } else {
-                        atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_CONTEXT);
-                    }
-                }
-            }
+            const int pos3 = load_pos(x + 3);
+            const int page2 = load_page(x + 2, pos2);
+            prefetch_row(row_of(pos1, page1, false));
+            const long long srow = row_of(pos0, page0, true);
+            pos0 = pos1;
+            page0 = page1;
+            pos1 = pos2;
+            page1 = page2;
+            pos2 = pos3;
             if (first) {
                 // the query buffer of segment seg is free once the products of
                 // segment seg - 2 have read it
@@ -269,46 +320,41 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 const uint8_t *qsrc = a.q + r * (long long)(kHeads * kDim);
                 const uint32_t qdst = sbase + kOffQ + (uint32_t)(seg & 1) * kQBytes;
                 for (int c = tid; c < kHeads * kChunks; c += kProducers) {
-                    const int h = c / kChunks, ch = c - h * kChunks, kb = ch >> 3, cc = ch & 7;
-                    cp_async_16(qdst + (uint32_t)kb * kQBlk + (uint32_t)h * 128u +
-                                    ((uint32_t)(cc ^ (h & 7)) << 4),
-                                qsrc + h * kDim + ch * 16, 16u);
+                    const int h = c / kChunks, ch = c - h * kChunks;
+                    cp_async_16(qdst + chunk_offset(h, ch), qsrc + h * kDim + ch * 16, 16u);
                 }
             }
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarKvEmpty + stage], kph ^ 1u, abort_flag))) {
+            if (!__all_sync(0xFFFFFFFFu,
+                            mbar_wait(&bar[kBarKvEmpty + stage], kph ^ 1u, abort_flag))) {
                 fail();
                 break;
             }
             flags[stage * kTile + tok] = srow >= 0 ? 1 : 0;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bar[kBarFlags + stage]);
             const uint32_t dst0 = sbase + kOffKV + (uint32_t)stage * kStageBytes;
             // value columns: one row per instruction, lane = 16-byte chunk
 #pragma unroll 4
             for (int tt = 0; tt < 32; ++tt) {
                 const long long sr = __shfl_sync(0xFFFFFFFFu, srow, tt);
                 const int t = pw * 32 + tt;
-                const int kb = lane >> 3, cc = lane & 7;
-                const uint8_t *src = a.kv + (sr >= 0 ? sr : 0ll) * kDim + 16 * lane;
-                cp_async_16(dst0 + (uint32_t)kb * kBlk + (uint32_t)t * 128u +
-                                ((uint32_t)(cc ^ (t & 7)) << 4),
-                            src, sr >= 0 ? 16u : 0u);
+                cp_async_16(dst0 + chunk_offset(t, lane), a.kv + (sr >= 0 ? sr : 0ll) * kDim + 16 * lane,
+                            sr >= 0 ? 16u : 0u);
             }
             // rotary columns: 4 chunks per row, 8 rows per instruction
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const int tt = g * 8 + (lane >> 2), cc = lane & 3;
+                const int tt = g * 8 + (lane >> 2), cc = 32 + (lane & 3);
                 const long long sr = __shfl_sync(0xFFFFFFFFu, srow, tt);
                 const int t = pw * 32 + tt;
-                const uint8_t *src = a.kv + (sr >= 0 ? sr : 0ll) * kDim + kVDim + 16 * cc;
-                cp_async_16(dst0 + 4u * kBlk + (uint32_t)t * 128u + ((uint32_t)(cc ^ (t & 7)) << 4),
-                            src, sr >= 0 ? 16u : 0u);
+                cp_async_16(dst0 + chunk_offset(t, cc), a.kv + (sr >= 0 ? sr : 0ll) * kDim + 16 * cc,
+                            sr >= 0 ? 16u : 0u);
             }
-            cp_async_arrive_noinc(&bar[kBarFull + stage]);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bar[kBarFlags + stage]);
+            cp_async_arrive_noinc(&bar[kBarReady + stage]);
         }
         cp_async_wait_all();
-    } else if (tid < kProducers + kSoftmax) {
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ softmax
         // Exits are uniform over the 128 threads: a failed wait only clears
         // `ok`, and the group leaves together at its next barrier (bar.red.and).
@@ -360,24 +406,40 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
             for (int h = 0; h < kHeads; ++h)
                 xs[h] = valid ? __uint_as_float(sr[h]) * a.c_log2 : -INFINITY;
             // the tile's maximum per head over the 128 positions
-            const float wmax = warp_reduce_scatter16<true>(xs, lane);
-            float *rs = red + stage * 64;
-            if ((lane & 1) == 0)
-                rs[w4 * 16 + hsel] = wmax;
-            if (!named_bar_and(1, kSoftmax, ok)) {
-                fail();
-                break;
-            }
-            float alpha[kHeads];
-            bool resc = false;
+            // The running maximum moves only where a position exceeds it by
+            // more than the slack (at a segment's first tile, always): one
+            // barrier tells whether any thread saw that (or a failed wait);
+            // only then is the tile's maximum per head exchanged.
+            bool exceed = !ok;
 #pragma unroll
-            for (int h = 0; h < kHeads; ++h) {
-                const float tmax = fmaxf(fmaxf(rs[h], rs[16 + h]), fmaxf(rs[32 + h], rs[48 + h]));
-                const float mn = tmax > m[h] + kRescaleSlack ? tmax : m[h];
-                const bool had = m[h] != -INFINITY;
-                alpha[h] = had ? ex2_approx(m[h] - mn) : 1.0f;
-                resc |= had && mn != m[h];
-                m[h] = mn;
+            for (int h = 0; h < kHeads; ++h)
+                exceed |= xs[h] > m[h] + kRescaleSlack;
+            float alpha[kHeads];
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h)
+                alpha[h] = 1.0f;
+            bool resc = false;
+            if (named_bar_or(1, kSoftmax, exceed)) {
+                const float wmax = warp_reduce_scatter16<true>(xs, lane);
+                float *rs = red + stage * 64;
+                if ((lane & 1) == 0)
+                    rs[w4 * 16 + hsel] = wmax;
+                if (!named_bar_and(1, kSoftmax, ok)) {
+                    fail();
+                    break;
+                }
+#pragma unroll
+                for (int h = 0; h < kHeads; ++h) {
+                    const float tmax =
+                        fmaxf(fmaxf(rs[h], rs[16 + h]), fmaxf(rs[32 + h], rs[48 + h]));
+                    if (tmax > m[h] + kRescaleSlack) {
+                        if (m[h] != -INFINITY) {
+                            alpha[h] = ex2_approx(m[h] - tmax);
+                            resc = true;
+                        }
+                        m[h] = tmax;
+                    }
+                }
             }
             float p[kHeads];
 #pragma unroll
@@ -490,134 +552,97 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                     __stcg(a.ml + (slot * kHeads + s) * 2, pick16(m, s));
                     __stcg(a.ml + (slot * kHeads + s) * 2 + 1, pick16(L, s));
                 }
-                __threadfence();
-                named_bar_sync(1, kSoftmax);
-                if (s == 0) {
-                    const uint32_t old = atomicAdd(a.cnt + r, 1u);
-                    __threadfence();
-                    misc[2] = old == (uint32_t)(nseg - 1) ? 1u : 0u;
-                }
-                named_bar_sync(1, kSoftmax);
-                if (misc[2]) {
-                    // the last part of the row to arrive: combine all of them
-                    __threadfence();
-                    float M[kHeads], Lt[kHeads];
-#pragma unroll
-                    for (int h = 0; h < kHeads; ++h) {
-                        M[h] = -INFINITY;
-                        Lt[h] = 0.0f;
-                    }
-                    for (int q = 0; q < nseg; ++q) {
-                        const int bb = bfirst + q;
-                        const int sl = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
-#pragma unroll
-                        for (int h = 0; h < kHeads; ++h)
-                            M[h] = fmaxf(M[h], ld_cg(a.ml + (sl * kHeads + h) * 2));
-                    }
-                    float acc[4][kHeads];
-#pragma unroll
-                    for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-                        for (int h = 0; h < kHeads; ++h)
-                            acc[kb][h] = 0.0f;
-                    for (int q = 0; q < nseg; ++q) {
-                        const int bb = bfirst + q;
-                        const int sl = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
-                        const float *sp = a.part + (long long)sl * kHeads * kVDim;
-#pragma unroll
-                        for (int h = 0; h < kHeads; ++h) {
-                            const float mq = ld_cg(a.ml + (sl * kHeads + h) * 2);
-                            const float lq = ld_cg(a.ml + (sl * kHeads + h) * 2 + 1);
-                            const float wq = mq == -INFINITY ? 0.0f : ex2_approx(mq - M[h]);
-                            Lt[h] += wq * lq;
-#pragma unroll
-                            for (int kb = 0; kb < 4; ++kb)
-                                acc[kb][h] += wq * ld_cg(sp + h * kVDim + kb * 128 + s);
-                        }
-                    }
-#pragma unroll
-                    for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-                        for (int h = 0; h < kHeads; ++h) {
-                            const float y =
-                                Lt[h] > 0.0f ? acc[kb][h] * (a.kv_scale / Lt[h]) : 0.0f;
-                            a.out[(r * kHeads + h) * kVDim + kb * 128 + s] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(y));
-                        }
-                    if (a.lse && s < kHeads) {
-                        const float Ls = pick16(Lt, s), Ms = pick16(M, s);
-                        a.lse[r * kHeads + s] = Ls > 0.0f ? (Ms + log2f(Ls)) * ln2 : -INFINITY;
-                    }
-                    if (s == 0)
-                        a.cnt[r] = 0u;  // ready for the next call
-                }
+                // combined by the second kernel
             }
         }
     } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------------ MMA issue
-        int seg = -1, prev_it = -1;
-        bool prev_first = false, ok = true;
-        auto issue_pv = [&](int pit, bool pfirst) -> bool {
-            const int st = pit & 1;
-            if (!mbar_wait(&bar[kBarPFull + st], (uint32_t)(pit >> 1) & 1u, abort_flag))
-                return false;
-            tc_fence_after_sync();
-            const uint32_t kvs = sbase + kOffKV + (uint32_t)st * kStageBytes;
-            const uint32_t pb = sbase + kOffP + (uint32_t)st * kPBytes;
+        // Two streams of products, each issued as soon as its inputs are
+        // ready (polled without suspending): the scores of tile nq (its rows
+        // in operand layout, its score buffer read, the row's query landed)
+        // and the output update of tile np (its P written). Issuing the
+        // update without waiting for the next tile frees a staging slot as
+        // early as possible.
+        const int n = (int)(x1 - x0);
+        int nq = 0, np = 0, seg = -1, idle = 0;
+        uint64_t idle_since = 0;
+        bool ok = true;
+        while (np < n) {
+            bool prog = false;
+            // the output update first: it frees a staging slot
+            if (np < nq) {
+                const int st = np & 1;
+                if (mbar_test(&bar[kBarPFull + st], (uint32_t)(np >> 1) & 1u)) {
+                    const long long x = x0 + np;
+                    const bool pfirst = x == x0 || (x % a.T) == 0;
+                    tc_fence_after_sync();
+                    const uint32_t kvs = sbase + kOffKV + (uint32_t)st * kStageBytes;
+                    const uint32_t pb = sbase + kOffP + (uint32_t)st * kPBytes;
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb)
+                    for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_e4m3(tmem + kColO + (uint32_t)kb * 32u,
-                              sw128_mnmajor_desc(kvs + (uint32_t)kb * kBlk + (uint32_t)ks * 4096u,
-                                                 kBlk, 1024u),
-                              sw128_kmajor_desc(pb + (uint32_t)ks * 32u), kIdescPV,
-                              (pfirst && ks == 0) ? 0u : 1u);
-            umma_commit(&bar[kBarKvEmpty + st]);
-            umma_commit(&bar[kBarPEmpty + st]);
-            return true;
-        };
-        for (long long x = x0; x < x1 && ok; ++x) {
-            const int it = (int)(x - x0), stage = it & 1;
-            const uint32_t kph = (uint32_t)(it >> 1) & 1u;
-            const long long r = x / a.T;
-            const int j = (int)(x - r * a.T);
-            const bool first = x == x0 || j == 0;
-            const bool last = x == x1 - 1 || j == a.T - 1;
-            if (first)
-                ++seg;
-            if (!mbar_wait(&bar[kBarFull + stage], kph, abort_flag) ||
-                !mbar_wait(&bar[kBarSFree + stage], kph ^ 1u, abort_flag)) {
-                ok = false;
-                break;
-            }
-            fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
-            tc_fence_after_sync();
-            const uint32_t kvs = sbase + kOffKV + (uint32_t)stage * kStageBytes;
-            const uint32_t qs = sbase + kOffQ + (uint32_t)(seg & 1) * kQBytes;
-#pragma unroll
-            for (int kb = 0; kb < 5; ++kb)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    if (kb == 4 && ks >= 2)
-                        break;  // the rotary block holds 64 columns
-                    umma_e4m3(tmem + kColS + (uint32_t)stage * kHeads,
-                              sw128_kmajor_desc(kvs + (uint32_t)kb * kBlk + (uint32_t)ks * 32u),
-                              sw128_kmajor_desc(qs + (uint32_t)kb * kQBlk + (uint32_t)ks * 32u),
-                              kIdescQK, (kb | ks) != 0 ? 1u : 0u);
+                        for (int ks = 0; ks < 4; ++ks)
+                            umma_e4m3(tmem + kColO + (uint32_t)kb * 32u,
+                                      sw128_mnmajor_desc(kvs + (uint32_t)kb * 1024u + (uint32_t)ks * 4u * kGroup,
+                                                         1024u, kGroup),
+                                      sw128_kmajor_desc(pb + (uint32_t)ks * 32u), kIdescPV,
+                                      (pfirst && ks == 0) ? 0u : 1u);
+                    umma_commit(&bar[kBarKvEmpty + st]);
+                    umma_commit(&bar[kBarPEmpty + st]);
+                    ++np;
+                    prog = true;
                 }
-            umma_commit(&bar[kBarSFull + stage]);
-            if (last)
-                umma_commit(&bar[kBarQEmpty + (seg & 1)]);
-            if (prev_it >= 0 && !issue_pv(prev_it, prev_first)) {
+            }
+            if (nq < n) {
+                const int st = nq & 1;
+                const uint32_t ph = (uint32_t)(nq >> 1) & 1u;
+                const long long x = x0 + nq;
+                const long long r = x / a.T;
+                const int j = (int)(x - r * a.T);
+                const bool qfirst = x == x0 || j == 0;
+                const int qseg = seg + (qfirst ? 1 : 0);
+                if (mbar_test(&bar[kBarReady + st], ph) && mbar_test(&bar[kBarSFree + st], ph ^ 1u)) {
+                    seg = qseg;
+                    fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
+                    tc_fence_after_sync();
+                    const uint32_t kvs = sbase + kOffKV + (uint32_t)st * kStageBytes;
+                    const uint32_t qs = sbase + kOffQ + (uint32_t)(seg & 1) * kQBytes;
+#pragma unroll
+                    for (int kb = 0; kb < 5; ++kb)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            if (kb == 4 && ks >= 2)
+                                break;  // the rotary block holds 64 columns
+                            umma_e4m3(tmem + kColS + (uint32_t)st * kHeads,
+                                      sw128_kmajor_desc_sbo(kvs + (uint32_t)kb * 1024u + (uint32_t)ks * 32u, kGroup),
+                                      sw128_kmajor_desc_sbo(qs + (uint32_t)kb * 1024u + (uint32_t)ks * 32u, kGroup),
+                                      kIdescQK, (kb | ks) != 0 ? 1u : 0u);
+                        }
+                    umma_commit(&bar[kBarSFull + st]);
+                    if (x == x1 - 1 || j == a.T - 1)
+                        umma_commit(&bar[kBarQEmpty + (seg & 1)]);
+                    ++nq;
+                    prog = true;
+                }
+            }
+            if (prog) {
+                idle = 0;
+                idle_since = 0;
+                continue;
+            }
+            // nothing ready: every 64 empty polls, check the abort flag and
+            // how long nothing has been ready
+            if (++idle < 64)
+                continue;
+            idle = 0;
+            const uint64_t now = global_timer_ns();
+            if (idle_since == 0) {
+                idle_since = now;
+            } else if (*abort_flag || now - idle_since > kWaitLimitNs) {
                 ok = false;
                 break;
             }
-            prev_it = it;
-            prev_first = first;
         }
-        if (ok && prev_it >= 0)
-            ok = issue_pv(prev_it, prev_first);
         if (!ok)
             fail();
         umma_commit(&bar[kBarDrain]);
@@ -632,10 +657,80 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
     }
 }
 
-// Workspace: status word | per-row arrival counters | (m, l) of each part |
-// the parts' unnormalised outputs.
+// The parts of every row split over several CTAs, combined: block (r, y)
+// takes heads 4y .. 4y+3 of row r, thread d one value column. Rows held by a
+// single CTA were written by the first kernel. Launched as a programmatic
+// dependent of the first kernel: it waits for that grid's results. The parts'
+// weights are staged in shared memory first, so the output loads of all parts
+// are independent and in flight together.
+__global__ void __launch_bounds__(kVDim) sparse_mla_combine_kernel(const Args a)
+{
+    __shared__ int s_slot[2 * kMaxCtas];
+    __shared__ float s_w[2 * kMaxCtas][4];
+    __shared__ float s_m[4], s_l[4];
+    griddep_wait();
+    const long long r = blockIdx.x;
+    const long long row0 = r * a.T;
+    const int bfirst = cta_of(a, row0);
+    const int nseg = cta_of(a, row0 + a.T - 1) - bfirst + 1;
+    if (nseg == 1)
+        return;
+    const int d = threadIdx.x, h0 = (int)blockIdx.y * 4;
+    // part q of the row is slot 2 b + (the row starts inside CTA b's range ? 0 : 1)
+    for (int q = d; q < nseg; q += kVDim) {
+        const int bb = bfirst + q;
+        s_slot[q] = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
+    }
+    __syncthreads();
+    if (d < 4 * 32) {
+        // warp hh: the maximum and the weights of head h0 + hh over the parts
+        const int hh = d >> 5, ln = d & 31, h = h0 + hh;
+        float M = -INFINITY;
+        for (int q = ln; q < nseg; q += 32)
+            M = fmaxf(M, a.ml[(s_slot[q] * kHeads + h) * 2]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        float L = 0.0f;
+        for (int q = ln; q < nseg; q += 32) {
+            const float mq = a.ml[(s_slot[q] * kHeads + h) * 2];
+            const float w = mq == -INFINITY ? 0.0f : ex2_approx(mq - M);
+            s_w[q][hh] = w;
+            L += w * a.ml[(s_slot[q] * kHeads + h) * 2 + 1];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        if (ln == 0) {
+            s_m[hh] = M;
+            s_l[hh] = L;
+        }
+    }
+    __syncthreads();
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+    for (int q = 0; q < nseg; ++q) {
+        const float *pp = a.part + ((long long)s_slot[q] * kHeads + h0) * kVDim + d;
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+            acc[hh] += s_w[q][hh] * pp[hh * kVDim];
+    }
+    const float ln2 = 0.69314718055994531f;
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+        const int h = h0 + hh;
+        const float L = s_l[hh];
+        const float y = L > 0.0f ? acc[hh] * (a.kv_scale / L) : 0.0f;
+        a.out[(r * kHeads + h) * kVDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+        if (a.lse && d == 0)
+            a.lse[r * kHeads + h] = L > 0.0f ? (s_m[hh] + log2f(L)) * ln2 : -INFINITY;
+    }
+}
+
+// Workspace: status word | (m, l) of each part | the parts' unnormalised
+// outputs.
 struct WsLayout {
-    size_t cnt, ml, part, total;
+    size_t ml, part, total;
 };
 
 bool ws_layout(long long rows, WsLayout *L)
@@ -643,8 +738,7 @@ bool ws_layout(long long rows, WsLayout *L)
     if (rows < 0)
         return false;
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-    L->cnt = 256;
-    L->ml = L->cnt + up((size_t)rows * 4);
+    L->ml = 256;
     L->part = L->ml + up((size_t)2 * kMaxCtas * kHeads * 2 * 4);
     L->total = L->part + (size_t)2 * kMaxCtas * kHeads * kVDim * 4;
     return true;
@@ -714,17 +808,35 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
     a.W = p->max_blocks_per_seq;
     a.num_blocks = p->num_blocks;
     a.N = rows * T;
-    a.G = (int)std::min<long long>(a.N, std::min(sms, kMaxCtas));
+    const long long want = (a.N + PMQA_MLA_MIN_TILES - 1) / PMQA_MLA_MIN_TILES;
+    a.G = (int)std::min<long long>(want, std::min(sms, kMaxCtas));
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
     a.status = reinterpret_cast<uint32_t *>(wsb);
-    a.cnt = reinterpret_cast<uint32_t *>(wsb + L.cnt);
     a.ml = reinterpret_cast<float *>(wsb + L.ml);
     a.part = reinterpret_cast<float *>(wsb + L.part);
     if (cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return PMQA_ERR_CUDA;
-    sparse_mla_kernel<<<a.G, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    sparse_mla_kernel<<<a.G, kThreads, kSmemBytes, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess)
+        return PMQA_ERR_CUDA;
+    if (a.T > 1) {
+        // rows may be split over CTAs: the combining kernel, its launch
+        // overlapping the first kernel's end (rows held whole return at once)
+        cudaLaunchConfig_t cfg = {};
+        cfg.stream = st;
+        cfg.gridDim = dim3((unsigned)rows, kHeads / 4);
+        cfg.blockDim = dim3(kVDim);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, sparse_mla_combine_kernel, a) != cudaSuccess)
+            return PMQA_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }

@@ -450,6 +450,33 @@ __device__ __forceinline__ void tmem_st_wait()
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Non-blocking test of an mbarrier phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major, with groups of
+// 8 rows `sbo` bytes apart (a multiple of 1024; the group base 1024-aligned).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc_sbo(uint32_t smem_addr, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // Shared-memory matrix descriptor for an MN-major operand in the 128-byte
 // swizzle: rows of 128 bytes run along M (or N), one row per K index, 16-byte
 // chunk c of row k at chunk c ^ (k & 7); groups of 8 K rows are `sbo` bytes
@@ -529,6 +556,22 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %3, 0;\n\t"
         "bar.red.and.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+// Named barrier that also returns whether `pred` held in any participating
+// thread.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "bar.red.or.pred q, %1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
