@@ -66,6 +66,8 @@ enum {
                                       the kernel clamps it */
 #define PMQA_DEV_TIMEOUT 0x4u      /* a pipeline wait exceeded its limit; results are invalid */
 #define PMQA_DEV_OVERFLOW 0x8u     /* top-k candidate storage exceeded; results are invalid */
+#define PMQA_DEV_INTERNAL 0x10u    /* a kernel found its shared memory misaligned and did no work;
+                                      results are invalid */
 
 /* Workspace-size selector for pmqa_workspace_bytes. For PMQA_OP_MQA_LOGITS (the
    prefill entry point) bs is the number of query rows m and the other sizes

@@ -54,9 +54,12 @@ constexpr int kVDim = 512;   // value columns
 constexpr int kHeads = 16;   // query heads per latent KV head
 constexpr int kTile = 128;   // listed positions per tile (the first product's M)
 constexpr int kChunks = kDim / 16;
-constexpr uint32_t kGroup = 5u * 1024u;           // 8 rows: 5 swizzled 1024-byte blocks
-constexpr uint32_t kStageBytes = 16u * kGroup;    // 128 rows
-constexpr uint32_t kQBytes = 2u * kGroup;         // 16 query heads
+constexpr uint32_t kVGroup = 4u * 1024u;          // 8 rows x 4 value blocks of 128 bytes
+constexpr uint32_t kVStage = 16u * kVGroup;       // 128 rows of value columns (64 KB)
+constexpr uint32_t kRGroup = 512u;                // 8 rows x 64 rotary bytes
+constexpr uint32_t kRStage = 16u * kRGroup;       // 128 rows of rotary columns (8 KB)
+constexpr int kVStages = 3;                       // value ring
+constexpr int kRStages = 2;                       // rotary ring (free once the scores are done)
 constexpr uint32_t kPBytes = 32u * 128u;          // 32 rows (hi, lo) x 128 positions
 constexpr int kProducers = 128;                   // warps 0-3
 constexpr int kSoftmax = 128;                     // warps 4-7
@@ -72,38 +75,51 @@ constexpr float kRescaleSlack = 8.0f;             // p <= 2^8 before the maximum
 #define PMQA_MLA_MIN_TILES 1                      // fewest tiles a CTA takes (small problems)
 #endif
 
-constexpr uint32_t kOffKV = 0;
-constexpr uint32_t kOffQ = 2u * kStageBytes;
-constexpr uint32_t kOffP = kOffQ + 2u * kQBytes;
+// Shared memory (the dynamic base is 1024-byte aligned; checked at entry).
+constexpr uint32_t kOffV = 0;
+constexpr uint32_t kOffR = kOffV + kVStages * kVStage;
+constexpr uint32_t kOffQV = kOffR + kRStages * kRStage;      // 16 query heads, value part
+constexpr uint32_t kOffQR = kOffQV + 2u * kVGroup;           // 16 query heads, rotary part
+constexpr uint32_t kOffP = kOffQR + 2u * kRGroup;
 constexpr uint32_t kOffFlags = kOffP + 2u * kPBytes;
-constexpr uint32_t kOffRed = kOffFlags + 2u * kTile;          // [2][4 warps][16] floats
-constexpr uint32_t kOffLred = kOffRed + 2u * 4u * 16u * 4u;   // [4 warps][16] floats
+constexpr uint32_t kOffRed = kOffFlags + kVStages * kTile;   // [2][4 warps][16] floats
+constexpr uint32_t kOffLred = kOffRed + 2u * 4u * 16u * 4u;  // [4 warps][16] floats
 constexpr uint32_t kOffBar = kOffLred + 4u * 16u * 4u;
 enum {
-    kBarFlags = 0,     // [2] tile position flags written: one arrival per producer warp
-    kBarReady = 2,     // [2] tile (and query) rows landed: 128 producer cp.async arrivals
-    kBarKvEmpty = 4,   // [2] products of the tile done: MMA commit
-    kBarSFull = 6,     // [2] scores in TMEM: MMA commit
-    kBarSFree = 8,     // [2] scores read: one arrival per softmax warp
-    kBarPFull = 10,    // [2] P written (and O rescaled): one arrival per softmax warp
-    kBarPEmpty = 12,   // [2] P read by the second product: MMA commit
-    kBarQEmpty = 14,   // [2] query buffer read: MMA commit after a row's last tile
-    kBarDrain = 16,    // MMAs drained before TMEM is freed
-    kNumBars = 17
+    kBarFlags = 0,     // [3] tile position flags written: one arrival per producer warp
+    kBarReady = 3,     // [3] tile (and query) rows landed: 128 producer cp.async arrivals
+    kBarVEmpty = 6,    // [3] value columns read by the output update: MMA commit
+    kBarREmpty = 9,    // [2] rotary columns read by the scores: MMA commit
+    kBarSFull = 11,    // [2] scores in TMEM: MMA commit
+    kBarSFree = 13,    // [2] scores read: one arrival per softmax warp
+    kBarPFull = 15,    // [2] P written (and O rescaled): one arrival per softmax warp
+    kBarPEmpty = 17,   // [2] P read by the output update: MMA commit
+    kBarQEmpty = 19,   // query buffer read: MMA commit after a row's last tile
+    kBarDrain = 20,    // MMAs drained before TMEM is freed
+    kNumBars = 21
 };
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8u;  // tmem base, abort flag, last flag
-constexpr uint32_t kSmemBytes = kOffMisc + 64u + 1024u;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8u;  // tmem base, abort flag
+constexpr uint32_t kSmemBytes = kOffMisc + 16u;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffR % 1024 == 0 && kOffQV % 1024 == 0 && kOffP % 1024 == 0, "atom alignment");
 
 constexpr uint32_t kIdescQK = idesc_e4m3_f32(128, kHeads);
 constexpr uint32_t kIdescPV = idesc_e4m3_f32(128, 2 * kHeads) | kIdescAMnMajor;
 
-// Byte offset, inside a tile or the query buffer, of 16-byte chunk c (0..35)
-// of row t in the operand layout.
-__host__ __device__ constexpr uint32_t chunk_offset(int t, int c)
+// Byte offset of value chunk c (0..31) of row t: groups of 8 rows 4096 bytes
+// apart, four 1024-byte blocks of 8 rows x 128 bytes, 128-byte swizzle.
+__host__ __device__ constexpr uint32_t v_offset(int t, int c)
 {
-    return (uint32_t)(t >> 3) * kGroup + (uint32_t)(c >> 3) * 1024u + (uint32_t)(t & 7) * 128u +
+    return (uint32_t)(t >> 3) * kVGroup + (uint32_t)(c >> 3) * 1024u + (uint32_t)(t & 7) * 128u +
            ((uint32_t)((c & 7) ^ (t & 7)) << 4);
+}
+
+// Byte offset of rotary chunk c (0..3) of row t: groups of 8 rows x 64 bytes,
+// 64-byte swizzle (chunk c of row r at c ^ (r >> 1)).
+__host__ __device__ constexpr uint32_t r_offset(int t, int c)
+{
+    return (uint32_t)(t >> 3) * kRGroup + (uint32_t)(t & 7) * 64u +
+           ((uint32_t)((c ^ ((t & 7) >> 1)) & 3) << 4);
 }
 
 struct Args {
@@ -199,10 +215,14 @@ __device__ __forceinline__ float ld_cg(const float *p)
 
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
 {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
+    if (sbase & 1023u) {
+        // the operand layouts need 1024-byte aligned atoms
+        if (threadIdx.x == 0)
+            atomicOr(a.status, (uint32_t)PMQA_DEV_INTERNAL);
+        return;
+    }
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
@@ -212,16 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(&bar[kBarFlags + i], kProducers / 32);
             mbar_init(&bar[kBarReady + i], kProducers);
-            mbar_init(&bar[kBarKvEmpty + i], 1);
+            mbar_init(&bar[kBarVEmpty + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar[kBarREmpty + i], 1);
             mbar_init(&bar[kBarSFull + i], 1);
             mbar_init(&bar[kBarSFree + i], kSoftmax / 32);
             mbar_init(&bar[kBarPFull + i], kSoftmax / 32);
             mbar_init(&bar[kBarPEmpty + i], 1);
-            mbar_init(&bar[kBarQEmpty + i], 1);
         }
+        mbar_init(&bar[kBarQEmpty], 1);
         mbar_init(&bar[kBarDrain], 1);
         misc[1] = 0;
         mbar_init_fence();
@@ -290,10 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
         int pos0 = load_pos(x0), pos1 = load_pos(x0 + 1), pos2 = load_pos(x0 + 2);
         int page0 = load_page(x0, pos0), page1 = load_page(x0 + 1, pos1);
         prefetch_row(row_of(pos0, page0, false));
-        int seg = -1;
+        int seg = -1, vs = 0;
+        uint32_t vph = 0;
         for (long long x = x0; x < x1; ++x) {
-            const int it = (int)(x - x0), stage = it & 1;
-            const uint32_t kph = (uint32_t)(it >> 1) & 1u;
+            const int it = (int)(x - x0), rs = it & 1;
+            const uint32_t rph = (uint32_t)(it >> 1) & 1u;
             const long long r = x / a.T;
             const int j = (int)(x - r * a.T);
             const bool first = x == x0 || j == 0;
@@ -309,49 +333,57 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
             page1 = page2;
             pos2 = pos3;
             if (first) {
-                // the query buffer of segment seg is free once the products of
-                // segment seg - 2 have read it
-                if (!__all_sync(0xFFFFFFFFu,
-                                mbar_wait(&bar[kBarQEmpty + (seg & 1)],
-                                          ((uint32_t)(seg >> 1) & 1u) ^ 1u, abort_flag))) {
+                // one query buffer: free once the scores of the previous
+                // segment's last tile are done
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[kBarQEmpty], ((uint32_t)seg & 1u) ^ 1u,
+                                                        abort_flag))) {
                     fail();
                     break;
                 }
                 const uint8_t *qsrc = a.q + r * (long long)(kHeads * kDim);
-                const uint32_t qdst = sbase + kOffQ + (uint32_t)(seg & 1) * kQBytes;
                 for (int c = tid; c < kHeads * kChunks; c += kProducers) {
                     const int h = c / kChunks, ch = c - h * kChunks;
-                    cp_async_16(qdst + chunk_offset(h, ch), qsrc + h * kDim + ch * 16, 16u);
+                    const uint32_t dst = ch < 32 ? sbase + kOffQV + v_offset(h, ch)
+                                                 : sbase + kOffQR + r_offset(h, ch - 32);
+                    cp_async_16(dst, qsrc + h * kDim + ch * 16, 16u);
                 }
             }
+            // the value slot is free once the output update of tile it - 3 read
+            // it, the rotary slot once the scores of tile it - 2 did
             if (!__all_sync(0xFFFFFFFFu,
-                            mbar_wait(&bar[kBarKvEmpty + stage], kph ^ 1u, abort_flag))) {
+                            mbar_wait(&bar[kBarVEmpty + vs], vph ^ 1u, abort_flag) &&
+                                mbar_wait(&bar[kBarREmpty + rs], rph ^ 1u, abort_flag))) {
                 fail();
                 break;
             }
-            flags[stage * kTile + tok] = srow >= 0 ? 1 : 0;
+            flags[vs * kTile + tok] = srow >= 0 ? 1 : 0;
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bar[kBarFlags + stage]);
-            const uint32_t dst0 = sbase + kOffKV + (uint32_t)stage * kStageBytes;
+                mbar_arrive(&bar[kBarFlags + vs]);
+            const uint32_t vdst = sbase + kOffV + (uint32_t)vs * kVStage;
+            const uint32_t rdst = sbase + kOffR + (uint32_t)rs * kRStage;
             // value columns: one row per instruction, lane = 16-byte chunk
 #pragma unroll 4
             for (int tt = 0; tt < 32; ++tt) {
                 const long long sr = __shfl_sync(0xFFFFFFFFu, srow, tt);
                 const int t = pw * 32 + tt;
-                cp_async_16(dst0 + chunk_offset(t, lane), a.kv + (sr >= 0 ? sr : 0ll) * kDim + 16 * lane,
+                cp_async_16(vdst + v_offset(t, lane), a.kv + (sr >= 0 ? sr : 0ll) * kDim + 16 * lane,
                             sr >= 0 ? 16u : 0u);
             }
             // rotary columns: 4 chunks per row, 8 rows per instruction
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const int tt = g * 8 + (lane >> 2), cc = 32 + (lane & 3);
+                const int tt = g * 8 + (lane >> 2), cc = lane & 3;
                 const long long sr = __shfl_sync(0xFFFFFFFFu, srow, tt);
                 const int t = pw * 32 + tt;
-                cp_async_16(dst0 + chunk_offset(t, cc), a.kv + (sr >= 0 ? sr : 0ll) * kDim + 16 * cc,
+                cp_async_16(rdst + r_offset(t, cc), a.kv + (sr >= 0 ? sr : 0ll) * kDim + kVDim + 16 * cc,
                             sr >= 0 ? 16u : 0u);
             }
-            cp_async_arrive_noinc(&bar[kBarReady + stage]);
+            cp_async_arrive_noinc(&bar[kBarReady + vs]);
+            if (++vs == kVStages) {
+                vs = 0;
+                vph ^= 1u;
+            }
         }
         cp_async_wait_all();
     } else if (warp >= 4 && warp < 8) {
@@ -362,11 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
         const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
         const int hsel = (lane >> 1) & 15;
         float m[kHeads], l[kHeads];
-        int seg = -1;
+        int seg = -1, vs = -1;
+        uint32_t vph = 1;
         bool ok = true;
         for (long long x = x0; x < x1; ++x) {
             const int it = (int)(x - x0), stage = it & 1;
             const uint32_t kph = (uint32_t)(it >> 1) & 1u;
+            if (++vs == kVStages || it == 0) {
+                vs = 0;
+                vph ^= 1u;
+            }
             const long long r = x / a.T;
             const int j = (int)(x - r * a.T);
             const bool first = x == x0 || j == 0;
@@ -379,10 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                     l[h] = 0.0f;
                 }
             }
-            // scores and flags of the tile; the P buffer free once the second
-            // product of tile it - 2 has read it
+            // scores and flags of the tile; the P buffer free once the output
+            // update of tile it - 2 has read it
             ok = ok && mbar_wait(&bar[kBarSFull + stage], kph, abort_flag) &&
-                 mbar_wait(&bar[kBarFlags + stage], kph, abort_flag) &&
+                 mbar_wait(&bar[kBarFlags + vs], vph, abort_flag) &&
                  mbar_wait(&bar[kBarPEmpty + stage], kph ^ 1u, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
             uint32_t sr[16];
@@ -400,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bar[kBarSFree + stage]);
-            const bool valid = flags[stage * kTile + s] != 0;
+            const bool valid = flags[vs * kTile + s] != 0;
             float xs[kHeads];
 #pragma unroll
             for (int h = 0; h < kHeads; ++h)
@@ -463,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
             if (resc && !first) {
                 // O holds the segment's earlier tiles: wait for the product of
                 // tile it - 1, then scale every column by its head's alpha
-                ok = mbar_wait(&bar[kBarPEmpty + (stage ^ 1)], (uint32_t)((it - 1) >> 1) & 1u,
-                               abort_flag);
+                ok = ok && mbar_wait(&bar[kBarPEmpty + (stage ^ 1)], (uint32_t)((it - 1) >> 1) & 1u,
+                                     abort_flag);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (ok) {
                     tc_fence_after_sync();
@@ -565,62 +602,72 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
         // early as possible.
         const int n = (int)(x1 - x0);
         int nq = 0, np = 0, seg = -1, idle = 0;
+        int qv = 0, pv = 0;              // value slots of tiles nq and np
+        uint32_t qvph = 0;
         uint64_t idle_since = 0;
         bool ok = true;
         while (np < n) {
             bool prog = false;
             // the output update first: it frees a staging slot
             if (np < nq) {
-                const int st = np & 1;
-                if (mbar_test(&bar[kBarPFull + st], (uint32_t)(np >> 1) & 1u)) {
+                const int sb = np & 1;
+                if (mbar_test(&bar[kBarPFull + sb], (uint32_t)(np >> 1) & 1u)) {
                     const long long x = x0 + np;
                     const bool pfirst = x == x0 || (x % a.T) == 0;
                     tc_fence_after_sync();
-                    const uint32_t kvs = sbase + kOffKV + (uint32_t)st * kStageBytes;
-                    const uint32_t pb = sbase + kOffP + (uint32_t)st * kPBytes;
+                    const uint32_t vb = sbase + kOffV + (uint32_t)pv * kVStage;
+                    const uint32_t pb = sbase + kOffP + (uint32_t)sb * kPBytes;
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
                             umma_e4m3(tmem + kColO + (uint32_t)kb * 32u,
-                                      sw128_mnmajor_desc(kvs + (uint32_t)kb * 1024u + (uint32_t)ks * 4u * kGroup,
-                                                         1024u, kGroup),
+                                      sw128_mnmajor_desc(vb + (uint32_t)kb * 1024u + (uint32_t)ks * 4u * kVGroup,
+                                                         1024u, kVGroup),
                                       sw128_kmajor_desc(pb + (uint32_t)ks * 32u), kIdescPV,
                                       (pfirst && ks == 0) ? 0u : 1u);
-                    umma_commit(&bar[kBarKvEmpty + st]);
-                    umma_commit(&bar[kBarPEmpty + st]);
+                    umma_commit(&bar[kBarVEmpty + pv]);
+                    umma_commit(&bar[kBarPEmpty + sb]);
+                    if (++pv == kVStages)
+                        pv = 0;
                     ++np;
                     prog = true;
                 }
             }
             if (nq < n) {
-                const int st = nq & 1;
+                const int sb = nq & 1;
                 const uint32_t ph = (uint32_t)(nq >> 1) & 1u;
-                const long long x = x0 + nq;
-                const long long r = x / a.T;
-                const int j = (int)(x - r * a.T);
-                const bool qfirst = x == x0 || j == 0;
-                const int qseg = seg + (qfirst ? 1 : 0);
-                if (mbar_test(&bar[kBarReady + st], ph) && mbar_test(&bar[kBarSFree + st], ph ^ 1u)) {
-                    seg = qseg;
+                if (mbar_test(&bar[kBarReady + qv], qvph) && mbar_test(&bar[kBarSFree + sb], ph ^ 1u)) {
+                    const long long x = x0 + nq;
+                    const long long r = x / a.T;
+                    const int j = (int)(x - r * a.T);
+                    if (x == x0 || j == 0)
+                        ++seg;
                     fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
                     tc_fence_after_sync();
-                    const uint32_t kvs = sbase + kOffKV + (uint32_t)st * kStageBytes;
-                    const uint32_t qs = sbase + kOffQ + (uint32_t)(seg & 1) * kQBytes;
+                    const uint32_t vb = sbase + kOffV + (uint32_t)qv * kVStage;
+                    const uint32_t rb = sbase + kOffR + (uint32_t)sb * kRStage;
+                    const uint32_t qvb = sbase + kOffQV, qrb = sbase + kOffQR;
+                    const uint32_t dS = tmem + kColS + (uint32_t)sb * kHeads;
 #pragma unroll
-                    for (int kb = 0; kb < 5; ++kb)
+                    for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            if (kb == 4 && ks >= 2)
-                                break;  // the rotary block holds 64 columns
-                            umma_e4m3(tmem + kColS + (uint32_t)st * kHeads,
-                                      sw128_kmajor_desc_sbo(kvs + (uint32_t)kb * 1024u + (uint32_t)ks * 32u, kGroup),
-                                      sw128_kmajor_desc_sbo(qs + (uint32_t)kb * 1024u + (uint32_t)ks * 32u, kGroup),
+                        for (int ks = 0; ks < 4; ++ks)
+                            umma_e4m3(dS, sw128_kmajor_desc_sbo(vb + (uint32_t)kb * 1024u + (uint32_t)ks * 32u, kVGroup),
+                                      sw128_kmajor_desc_sbo(qvb + (uint32_t)kb * 1024u + (uint32_t)ks * 32u, kVGroup),
                                       kIdescQK, (kb | ks) != 0 ? 1u : 0u);
-                        }
-                    umma_commit(&bar[kBarSFull + st]);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+                        umma_e4m3(dS, sw64_kmajor_desc(rb + (uint32_t)ks * 32u, kRGroup),
+                                  sw64_kmajor_desc(qrb + (uint32_t)ks * 32u, kRGroup), kIdescQK, 1u);
+                    umma_commit(&bar[kBarSFull + sb]);
+                    umma_commit(&bar[kBarREmpty + sb]);
                     if (x == x1 - 1 || j == a.T - 1)
-                        umma_commit(&bar[kBarQEmpty + (seg & 1)]);
+                        umma_commit(&bar[kBarQEmpty]);
+                    if (++qv == kVStages) {
+                        qv = 0;
+                        qvph ^= 1u;
+                    }
                     ++nq;
                     prog = true;
                 }

@@ -477,6 +477,20 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc_sbo(uint32_t smem_addr, ui
     return d;
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle, K-major: rows of 64
+// bytes, 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3), groups of 8 rows
+// (512-byte atoms, 512-byte aligned) `sbo` bytes apart; swizzle mode 4 = 64B.
+__device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t smem_addr, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)4u << 61;
+    return d;
+}
+
 // Shared-memory matrix descriptor for an MN-major operand in the 128-byte
 // swizzle: rows of 128 bytes run along M (or N), one row per K index, 16-byte
 // chunk c of row k at chunk c ^ (k & 7); groups of 8 K rows are `sbo` bytes

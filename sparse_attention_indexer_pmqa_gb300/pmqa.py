@@ -24,6 +24,7 @@ PMQA_DEV_BAD_BLOCK_ID = 0x1
 PMQA_DEV_BAD_CONTEXT = 0x2
 PMQA_DEV_TIMEOUT = 0x4
 PMQA_DEV_OVERFLOW = 0x8
+PMQA_DEV_INTERNAL = 0x10
 
 PMQA_OP_LOGITS = 0
 PMQA_OP_TOPK = 1
