@@ -51,12 +51,14 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--all", action="store_true", default=True,
-                    help="also time every other workload and the prefill (the default)")
+                    help="also time every other workload, the prefill and the sparse MLA decode (the default)")
     ap.add_argument("--headline-only", action="store_true",
                     help="time the headline workload alone (no other workloads, no prefill)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--mla", action="store_true",
+                    help="also time the sparse MLA decode workloads (with --headline-only)")
     ap.add_argument("--prefill", action="store_true",
                     help="also time the prefill (non-paged) logits on PF1 (on with --all)")
     args = ap.parse_args(argv)
@@ -126,26 +128,40 @@ def read_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources each kernel is built from (under the package's csrc/).
+KERNEL_SOURCES = {
+    "indexer": ("pmqa_ptx.cuh", "pmqa_main.cuh", "pmqa_kernel.cuh", "pmqa_main_inst.cu",
+                "pmqa_select.cuh", "pmqa_api.cu"),
+    "prefill": ("pmqa_ptx.cuh", "pmqa_prefill.cuh", "pmqa_prefill_inst.cu", "pmqa_api.cu"),
+    "mla": ("pmqa_ptx.cuh", "pmqa_mla_ptx.cuh", "pmqa_mla.cu"),
+}
+
+
+def kernel_set(workload: str) -> str:
+    return {"P": "prefill", "M": "mla"}.get(workload[:1], "indexer")
+
+
+def kernel_source_hash(kind: str = "indexer") -> str:
+    """Hash of the sources of one kernel family: a counter capture stays
+    valid while they are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_indexer_pmqa_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from a committed ncu summary,
-    or None when absent or taken on different kernel sources."""
+    """DRAM bytes per launch of the workload's main kernel from a committed
+    ncu summary, or None when absent or taken on different kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel_set(workload)):
         return None
     return float(rec["dram_bytes_per_launch"])
 
@@ -536,6 +552,90 @@ def bench_prefill(name, args, device):
     }
 
 
+def mla_cpu_baseline(p, min_seconds: float = 3.0, max_reps: int = 50):
+    """The MLA decode oracle, as it stands, on the whole workload (every query
+    row), repeated until at least `min_seconds` have passed."""
+    import oracle
+
+    oracle.build()
+    nthreads = oracle.default_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.sparse_mla(p, nthreads=nthreads)
+        reps += 1
+        sec = time.perf_counter() - t0
+        if sec >= min_seconds or reps >= max_reps:
+            break
+    return {"value": reps * p.rows / sec, "unit": "query rows/s", "cores": nthreads,
+            "kind": "oracle", "positions_per_s": reps * p.listed / sec,
+            "sample": f"all {p.rows} query rows of {p.name} ({p.listed} listed positions), "
+                      f"{reps} passes in {sec:.2f} s"}
+
+
+def bench_mla(name, args, device):
+    """Sparse MLA decode (pmqa_sparse_mla_decode) over one workload's listed
+    positions: the call (attention kernel + the combining kernel) replayed
+    from a CUDA graph; L2 flushed before each step."""
+    import torch
+
+    from sparse_attention_indexer_pmqa_gb300 import pmqa
+    from synth import MLA_CONFIGS, mla_config
+
+    p = mla_config(name)
+    q = torch.from_numpy(p.q.reshape(p.rows, p.heads, -1)).to(device)
+    kv = torch.from_numpy(p.kv).to(device)
+    idx = torch.from_numpy(p.indices).to(device)
+    bt = torch.from_numpy(p.block_tables).to(device)
+    out = torch.empty((p.rows, p.heads, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((p.rows, p.heads), dtype=torch.float32, device=device)
+    ws = pmqa.mla_workspace(p.rows, device)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    def call():
+        pmqa.pmqa_sparse_mla_decode(q, kv, idx, bt, p.next_n, p.q_scale, p.kv_scale, p.sm_scale,
+                                    out=out, lse=lse, ws=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(3):
+        flush()
+        graph.replay()
+    torch.cuda.synchronize()
+    times = time_steps(graph.replay, min(args.steps, 100), flush)
+    status = pmqa.pmqa_read_device_status(ws)
+    if status:
+        raise RuntimeError(f"device status {status:#x} during the MLA decode steps")
+    ms = statistics.fmean(times)
+    listed = p.listed
+    kv_bytes = listed * 576
+    other = p.rows * p.heads * 576 + p.indices.size * 4 + p.rows * p.heads * (512 * 2 + 4)
+    peak, peak_kind = read_peak()
+    achieved = kv_bytes / (ms * 1e-3) / 1e9
+    return {
+        "workload": f"{name}: {MLA_CONFIGS[name]['desc']}",
+        "ms": ms, "ms_median": statistics.median(times), "us": ms * 1e3,
+        "rows": p.rows, "listed_positions": listed,
+        "rows_per_s": p.rows / (ms * 1e-3), "positions_per_s": listed / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": measured_traffic(name),
+                     "algorithmic_bytes_per_launch": kv_bytes,
+                     "algorithmic": "576 B latent row per listed position",
+                     "other_bytes_per_launch": other,
+                     "kernel": "sparse_mla_kernel + sparse_mla_combine_kernel (one call, timed "
+                               "whole)"},
+        "launches": 2,
+    }
+
+
 def cpu_baseline(prob, min_seconds: float = 10.0, max_reps: int = 60):
     """The oracle, as it stands, on the whole workload (logits + top-k)."""
     import oracle
@@ -678,6 +778,14 @@ def run_ours(args):
             from synth import prefill_config
 
             line["prefill"]["cpu_baseline"] = prefill_cpu_baseline(prefill_config("PF1"))
+    if args.all or args.mla:
+        from synth import MLA_CONFIGS
+
+        line["sparse_mla_decode"] = {wl: bench_mla(wl, args, device) for wl in MLA_CONFIGS}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            from synth import mla_config
+
+            line["sparse_mla_decode"]["M1"]["cpu_baseline"] = mla_cpu_baseline(mla_config("M1"))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob)
     if rank == 0:

@@ -44,7 +44,7 @@
 #include <cstdint>
 
 #include "../../include/pmqa.h"
-#include "pmqa_ptx.cuh"
+#include "pmqa_mla_ptx.cuh"
 
 namespace pmqa {
 namespace mla {

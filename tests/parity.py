@@ -91,3 +91,33 @@ def check_topk_exact(idx: np.ndarray, vals32: np.ndarray, ctx, nn: int, k: int) 
         want = np.sort(vals32[r, :n])[::-1][:ke]
         got = np.sort(vals32[r, sel])[::-1]
         assert np.array_equal(got, want), f"row {r}: selected values differ from the top-{ke}"
+
+
+def check_mla(out, lse, ref, lref, tol):
+    """Sparse MLA decode outputs against the oracle's. Tolerance per output
+    entry, from the kernel's arithmetic: scores within e_s = 2^-9 * s_abs of
+    exact (fp8 products summed on the tensor cores) move an output by at most
+    e_s * d_abs; the softmax weights enter the second product as two fp8 terms
+    (relative error 2^-8), at most 2^-7 * a_abs with margin; the bf16 output
+    rounds by 2^-9 relative, 2^-8 |out| with margin. lse within e_s + 1e-4;
+    rows with no listed position exactly 0 and -inf. Returns (worst error as a
+    fraction of its bound, cos_diff = 1 - 2 <x, y> / (|x|^2 + |y|^2), the
+    agreement measure the pages quote for MLA decode)."""
+    out = np.asarray(out, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    e_s = 2.0 ** -9 * tol["s_abs"]
+    bound = e_s[..., None] * tol["d_abs"] + 2.0 ** -7 * tol["a_abs"] + 2.0 ** -8 * np.abs(ref) + 1e-6
+    err = np.abs(out - ref)
+    bad = err > bound
+    assert not bad.any(), (
+        f"{int(bad.sum())} outputs beyond tolerance; worst excess "
+        f"{float((err - bound).max()):.3g} at {np.unravel_index(np.argmax(err - bound), err.shape)}")
+    empty = np.isneginf(lref)
+    assert np.array_equal(np.isneginf(lse), empty), "-inf pattern of lse"
+    assert (out[empty] == 0).all()
+    fin = ~empty
+    lerr = np.abs(lse[fin] - lref[fin])
+    assert (lerr <= e_s[fin] + 1e-4).all(), f"lse error {lerr.max():.3g}"
+    den = (out * out).sum() + (ref * ref).sum()
+    cos_diff = 1.0 - 2.0 * (out * ref).sum() / den if den > 0 else 0.0
+    return float((err / bound).max()), float(cos_diff)

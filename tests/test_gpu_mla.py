@@ -1,13 +1,7 @@
-"""Sparse MLA decode on the GPU against the oracle, element by element.
-
-Tolerance per output entry (derived from the kernel's arithmetic): scores
-within e_s = 2^-9 * s_abs of exact (fp8 products summed on the tensor cores),
-which moves an output by at most e_s * d_abs; the softmax weights enter the
-second product as two fp8 terms (relative error 2^-8), at most 2^-7 * a_abs
-with margin; the bf16 output rounds by 2^-9 relative, 2^-8 |out| with margin.
-lse within e_s + 1e-4; empty rows exactly 0 and -inf. a_abs, d_abs and s_abs
-are the oracle's (sum p |v|, sum p |v - out|, max score magnitude).
-"""
+"""Sparse MLA decode on the GPU against the oracle, element by element, with
+the tolerance of tests.parity.check_mla (derived from the kernel's
+arithmetic; a_abs, d_abs and s_abs are the oracle's sum p |v|, sum p |v - out|
+and largest score magnitude)."""
 
 import numpy as np
 import pytest
@@ -16,6 +10,7 @@ import torch
 import oracle
 from synth.inputs import to_e4m3fn_bytes
 from synth.mla import MLA_DIM, MlaProblem, make_mla_problem, mla_config
+from tests.parity import check_mla
 
 pytestmark = pytest.mark.gpu
 
@@ -39,23 +34,7 @@ def check(out, lse, prob, rows=None):
     ref, lref, tol = oracle.sparse_mla(prob, rows=rows, want_tol=True)
     if rows is not None:
         out, lse = out[rows], lse[rows]
-    e_s = 2.0 ** -9 * tol["s_abs"]
-    bound = e_s[..., None] * tol["d_abs"] + 2.0 ** -7 * tol["a_abs"] + 2.0 ** -8 * np.abs(ref) + 1e-6
-    err = np.abs(out - ref)
-    bad = err > bound
-    assert not bad.any(), (
-        f"{int(bad.sum())} outputs beyond tolerance; worst excess "
-        f"{float((err - bound).max()):.3g} at {np.unravel_index(np.argmax(err - bound), err.shape)}")
-    empty = np.isneginf(lref)
-    assert np.array_equal(np.isneginf(lse), empty), "-inf pattern of lse"
-    assert (out[empty] == 0).all()
-    fin = ~empty
-    lerr = np.abs(lse[fin] - lref[fin])
-    assert (lerr <= e_s[fin] + 1e-4).all(), f"lse error {lerr.max():.3g}"
-    # the pages' agreement measure: cos_diff = 1 - 2 <x, y> / (|x|^2 + |y|^2)
-    den = (out * out).sum() + (ref * ref).sum()
-    cos_diff = 1.0 - 2.0 * (out * ref).sum() / den if den > 0 else 0.0
-    return float(err.max()), float(cos_diff)
+    return check_mla(out, lse, ref, lref, tol)
 
 
 @pytest.mark.parametrize("bs,nn,P,ctx,topk,kw", [
@@ -125,8 +104,8 @@ def test_one_dominant_position(cuda_lib):
 
 def test_many_rows_split_over_ctas(cuda_lib):
     """More tiles than CTAs with rows split at arbitrary tile boundaries (parts
-    combined by the last CTA to finish), and fewer tiles than SMs (every CTA
-    one tile, a row combined from up to 16 parts)."""
+    combined by the second kernel), and fewer tiles than SMs (every CTA one
+    tile, a row combined from up to 16 parts)."""
     for bs, nn, seed in ((37, 3, 1), (1, 4, 2)):
         ctx = np.random.default_rng(seed).integers(2100, 9000, size=bs)
         prob = make_mla_problem(bs, nn, 16, 1, ctx, seed=seed)
@@ -136,8 +115,8 @@ def test_many_rows_split_over_ctas(cuda_lib):
 
 
 def test_workspace_is_reusable(cuda_lib):
-    """The arrival counters return to zero: three calls on one workspace agree
-    bit for bit."""
+    """The workspace carries nothing from one call to the next: three calls on
+    one workspace agree bit for bit."""
     prob = make_mla_problem(9, 4, 16, 1, [4000] * 9, seed=8)
     ws = cuda_lib.mla_workspace(prob.rows)
     first = run(cuda_lib, prob, ws=ws)
@@ -169,3 +148,24 @@ def test_workloads_sampled_rows(cuda_lib, name):
     rows = None if prob.rows <= 8 else np.sort(rng.choice(prob.rows, 8, replace=False))
     _, cos_diff = check(out, lse, prob, rows=rows)
     assert cos_diff < 1e-4
+
+
+def test_decode_over_the_indexers_top_k(cuda_lib):
+    """The two steps of a decode chained: the fused indexer call selects each
+    row's top-2048 positions, the decode attends to exactly those (a latent
+    cache of the same requests and pages)."""
+    from synth import make_problem
+
+    ctx = [3000, 5000, 2500, 9000]
+    ip = make_problem(4, 2, 64, 1, ctx, 9216, seed=6, table="perm", extra_blocks=2, k=2048)
+    dq = torch.from_numpy(ip.q).cuda().view(torch.float8_e4m3fn)
+    idx = cuda_lib.pmqa_logits_topk(dq, torch.from_numpy(ip.kv).cuda(),
+                                    torch.from_numpy(ip.weights).cuda(),
+                                    torch.from_numpy(ip.context_lens).cuda(),
+                                    torch.from_numpy(ip.block_tables).cuda(), ip.max_model_len,
+                                    ip.k)
+    prob = make_mla_problem(4, 2, 16, 1, ctx, topk=2048, seed=7)
+    prob.indices = idx.cpu().numpy()
+    out, lse, status = run(cuda_lib, prob)
+    assert status == 0
+    check(out, lse, prob)
