@@ -72,7 +72,7 @@ constexpr uint32_t kColO = 128;                   // 4 x 32 output columns
 constexpr float kLoScale = 16.0f;                 // p_lo holds 16 (p - p_hi)
 constexpr float kRescaleSlack = 8.0f;             // p <= 2^8 before the maximum moves
 #ifndef PMQA_MLA_MIN_TILES
-#define PMQA_MLA_MIN_TILES 1                      // fewest tiles a CTA takes (small problems)
+#define PMQA_MLA_MIN_TILES 2                      // fewest tiles a CTA takes (small problems)
 #endif
 
 // Shared memory (the dynamic base is 1024-byte aligned; checked at entry).
@@ -256,8 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
     tc_fence_after_sync();
     const uint32_t tmem = misc[0];
 
-    // the combining kernel may be scheduled now; it waits for this grid
-    griddep_launch_dependents();
     const long long x0 = tile_start(a, blockIdx.x), x1 = tile_start(a, blockIdx.x + 1);
     auto fail = [&]() {
         atomicOr(a.status, (uint32_t)PMQA_DEV_TIMEOUT);
@@ -270,8 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
         // of positions 32w .. 32w+31, one row per instruction (lane = 16-byte
         // chunk), straight into the operand layout. Lookups run ahead of the
         // copies: the listed position of tile it + 3 and the block table
-        // entry of tile it + 2 load while tile it is issued, and the row of
-        // tile it + 1 is prefetched into L2.
+        // entry of tile it + 2 load while tile it is issued.
         const int pw = warp, tok = tid;
         const long long wp = (long long)a.W * a.P;
         auto load_pos = [&](long long x) -> int {
@@ -286,33 +283,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 return -1;
             return __ldg(a.bt + (x / a.T) / a.next_n * a.W + pos / a.P);
         };
-        // pool row of a looked-up position, -1 for none; `report` records bad entries
-        auto row_of = [&](int pos, int page, bool report) -> long long {
+        // pool row of a looked-up position, -1 for none (bad entries recorded)
+        auto row_of = [&](int pos, int page) -> long long {
             if (pos < 0)
                 return -1;
             if ((long long)pos >= wp) {
-                if (report)
-                    atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_CONTEXT);
+                atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_CONTEXT);
                 return -1;
             }
             if (page < 0 || (long long)page >= a.num_blocks) {
-                if (report)
-                    atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_BLOCK_ID);
+                atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_BLOCK_ID);
                 return -1;
             }
             return (long long)page * a.P + pos % a.P;
         };
-        auto prefetch_row = [&](long long row) {
-            if (row < 0)
-                return;
-            const uint8_t *p = a.kv + row * kDim;
-#pragma unroll
-            for (int k = 0; k < 5; ++k)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128 * k));
-        };
         int pos0 = load_pos(x0), pos1 = load_pos(x0 + 1), pos2 = load_pos(x0 + 2);
         int page0 = load_page(x0, pos0), page1 = load_page(x0 + 1, pos1);
-        prefetch_row(row_of(pos0, page0, false));
         int seg = -1, vs = 0;
         uint32_t vph = 0;
         for (long long x = x0; x < x1; ++x) {
@@ -325,8 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 ++seg;
             const int pos3 = load_pos(x + 3);
             const int page2 = load_page(x + 2, pos2);
-            prefetch_row(row_of(pos1, page1, false));
-            const long long srow = row_of(pos0, page0, true);
+            const long long srow = row_of(pos0, page0);
             pos0 = pos1;
             page0 = page1;
             pos1 = pos2;
@@ -705,72 +690,100 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
 }
 
 // The parts of every row split over several CTAs, combined: block (r, y)
-// takes heads 4y .. 4y+3 of row r, thread d one value column. Rows held by a
+// takes heads kHg y .. kHg y + kHg - 1 of row r, thread d one value column. Rows held by a
 // single CTA were written by the first kernel. Launched as a programmatic
-// dependent of the first kernel: it waits for that grid's results. The parts'
-// weights are staged in shared memory first, so the output loads of all parts
-// are independent and in flight together.
+// dependent of the first kernel: it waits for that grid's results. Thread q
+// loads part q's (m, l) (a row has at most 2 kMaxCtas <= 512 parts), the
+// block reduces them, and the parts' weights go through shared memory, so the
+// output loads of all parts are independent and in flight together.
+template <int kHg>
 __global__ void __launch_bounds__(kVDim) sparse_mla_combine_kernel(const Args a)
 {
     __shared__ int s_slot[2 * kMaxCtas];
-    __shared__ float s_w[2 * kMaxCtas][4];
-    __shared__ float s_m[4], s_l[4];
+    __shared__ float s_w[2 * kMaxCtas][kHg];
+    __shared__ float s_red[2][kHg][16];
     griddep_wait();
     const long long r = blockIdx.x;
+    const int h0 = (int)blockIdx.y * kHg;
     const long long row0 = r * a.T;
     const int bfirst = cta_of(a, row0);
     const int nseg = cta_of(a, row0 + a.T - 1) - bfirst + 1;
     if (nseg == 1)
         return;
-    const int d = threadIdx.x, h0 = (int)blockIdx.y * 4;
-    // part q of the row is slot 2 b + (the row starts inside CTA b's range ? 0 : 1)
-    for (int q = d; q < nseg; q += kVDim) {
-        const int bb = bfirst + q;
-        s_slot[q] = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
+    const int d = threadIdx.x, lane = d & 31, wid = d >> 5;
+    float mq[kHg], lq[kHg];
+#pragma unroll
+    for (int hh = 0; hh < kHg; ++hh) {
+        mq[hh] = -INFINITY;
+        lq[hh] = 0.0f;
     }
-    __syncthreads();
-    if (d < 4 * 32) {
-        // warp hh: the maximum and the weights of head h0 + hh over the parts
-        const int hh = d >> 5, ln = d & 31, h = h0 + hh;
-        float M = -INFINITY;
-        for (int q = ln; q < nseg; q += 32)
-            M = fmaxf(M, a.ml[(s_slot[q] * kHeads + h) * 2]);
+    if (d < nseg) {
+        // part q of the row is slot 2 b + (the row starts inside CTA b's range ? 0 : 1)
+        const int bb = bfirst + d;
+        const int sl = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
+        s_slot[d] = sl;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-        float L = 0.0f;
-        for (int q = ln; q < nseg; q += 32) {
-            const float mq = a.ml[(s_slot[q] * kHeads + h) * 2];
-            const float w = mq == -INFINITY ? 0.0f : ex2_approx(mq - M);
-            s_w[q][hh] = w;
-            L += w * a.ml[(s_slot[q] * kHeads + h) * 2 + 1];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
-        if (ln == 0) {
-            s_m[hh] = M;
-            s_l[hh] = L;
+        for (int hh = 0; hh < kHg; ++hh) {
+            mq[hh] = a.ml[(sl * kHeads + h0 + hh) * 2];
+            lq[hh] = a.ml[(sl * kHeads + h0 + hh) * 2 + 1];
         }
     }
+    float M[kHg], L[kHg];
+#pragma unroll
+    for (int hh = 0; hh < kHg; ++hh) {
+        float v = mq[hh];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+        if (lane == 0)
+            s_red[0][hh][wid] = v;
+    }
     __syncthreads();
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int hh = 0; hh < kHg; ++hh) {
+        float v = s_red[0][hh][0];
+#pragma unroll
+        for (int i = 1; i < 16; ++i)
+            v = fmaxf(v, s_red[0][hh][i]);
+        M[hh] = v;
+        const float w = (d < nseg && mq[hh] != -INFINITY) ? ex2_approx(mq[hh] - v) : 0.0f;
+        if (d < nseg)
+            s_w[d][hh] = w;
+        float t = w * lq[hh];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        if (lane == 0)
+            s_red[1][hh][wid] = t;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int hh = 0; hh < kHg; ++hh) {
+        float t = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            t += s_red[1][hh][i];
+        L[hh] = t;
+    }
+    float acc[kHg];
+#pragma unroll
+    for (int hh = 0; hh < kHg; ++hh)
+        acc[hh] = 0.0f;
 #pragma unroll 4
     for (int q = 0; q < nseg; ++q) {
         const float *pp = a.part + ((long long)s_slot[q] * kHeads + h0) * kVDim + d;
 #pragma unroll
-        for (int hh = 0; hh < 4; ++hh)
+        for (int hh = 0; hh < kHg; ++hh)
             acc[hh] += s_w[q][hh] * pp[hh * kVDim];
     }
-    const float ln2 = 0.69314718055994531f;
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
+    for (int hh = 0; hh < kHg; ++hh) {
         const int h = h0 + hh;
-        const float L = s_l[hh];
-        const float y = L > 0.0f ? acc[hh] * (a.kv_scale / L) : 0.0f;
+        const float y = L[hh] > 0.0f ? acc[hh] * (a.kv_scale / L[hh]) : 0.0f;
         a.out[(r * kHeads + h) * kVDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
         if (a.lse && d == 0)
-            a.lse[r * kHeads + h] = L > 0.0f ? (s_m[hh] + log2f(L)) * ln2 : -INFINITY;
+            a.lse[r * kHeads + h] =
+                L[hh] > 0.0f ? (M[hh] + log2f(L[hh])) * 0.69314718055994531f : -INFINITY;
     }
 }
 
@@ -875,14 +888,18 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
         // overlapping the first kernel's end (rows held whole return at once)
         cudaLaunchConfig_t cfg = {};
         cfg.stream = st;
-        cfg.gridDim = dim3((unsigned)rows, kHeads / 4);
         cfg.blockDim = dim3(kVDim);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, sparse_mla_combine_kernel, a) != cudaSuccess)
+        // one head per block for few rows (more blocks in flight), two for many
+        const bool few = rows <= 32;
+        cfg.gridDim = dim3((unsigned)rows, few ? kHeads : kHeads / 2);
+        const cudaError_t e = few ? cudaLaunchKernelEx(&cfg, sparse_mla_combine_kernel<1>, a)
+                                  : cudaLaunchKernelEx(&cfg, sparse_mla_combine_kernel<2>, a);
+        if (e != cudaSuccess)
             return PMQA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
