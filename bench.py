@@ -57,8 +57,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--mla", action="store_true",
-                    help="also time the sparse MLA decode workloads (with --headline-only)")
+    ap.add_argument("--mla", nargs="*", default=None,
+                    help="also time the sparse MLA decode workloads (all of them, or the ones "
+                         "named) under --headline-only")
     ap.add_argument("--prefill", action="store_true",
                     help="also time the prefill (non-paged) logits on PF1 (on with --all)")
     args = ap.parse_args(argv)
@@ -778,11 +779,12 @@ def run_ours(args):
             from synth import prefill_config
 
             line["prefill"]["cpu_baseline"] = prefill_cpu_baseline(prefill_config("PF1"))
-    if args.all or args.mla:
+    if args.all or args.mla is not None:
         from synth import MLA_CONFIGS
 
-        line["sparse_mla_decode"] = {wl: bench_mla(wl, args, device) for wl in MLA_CONFIGS}
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        names = list(MLA_CONFIGS) if args.all or not args.mla else args.mla
+        line["sparse_mla_decode"] = {wl: bench_mla(wl, args, device) for wl in names}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and "M1" in names:
             from synth import mla_config
 
             line["sparse_mla_decode"]["M1"]["cpu_baseline"] = mla_cpu_baseline(mla_config("M1"))

@@ -690,101 +690,76 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
 }
 
 // The parts of every row split over several CTAs, combined: block (r, y)
-// takes heads kHg y .. kHg y + kHg - 1 of row r, thread d one value column. Rows held by a
-// single CTA were written by the first kernel. Launched as a programmatic
-// dependent of the first kernel: it waits for that grid's results. Thread q
-// loads part q's (m, l) (a row has at most 2 kMaxCtas <= 512 parts), the
-// block reduces them, and the parts' weights go through shared memory, so the
-// output loads of all parts are independent and in flight together.
-template <int kHg>
+// takes heads HB y .. HB y + HB - 1 of row r (HB = 16 for many rows, 1 for
+// few, so that there are enough blocks), thread d value column d. Rows held by
+// a single CTA were written by the first kernel. Launched as a programmatic
+// dependent of the first kernel: it waits for that grid's results. The parts'
+// (m, l) load in parallel over (part, head), HB threads turn them into weights
+// in shared memory, and each thread then has HB x parts independent output
+// loads in flight.
+template <int HB>
 __global__ void __launch_bounds__(kVDim) sparse_mla_combine_kernel(const Args a)
 {
-    __shared__ int s_slot[2 * kMaxCtas];
-    __shared__ float s_w[2 * kMaxCtas][kHg];
-    __shared__ float s_red[2][kHg][16];
+    // a row's parts come from distinct CTAs: at most kMaxCtas of them
+    __shared__ int s_slot[kMaxCtas];
+    __shared__ float s_m[kMaxCtas][HB];  // m of (part, head), then its weight
+    __shared__ float s_l[kMaxCtas][HB];
+    __shared__ float s_M[HB], s_L[HB];
     griddep_wait();
     const long long r = blockIdx.x;
-    const int h0 = (int)blockIdx.y * kHg;
+    const int h0 = (int)blockIdx.y * HB;
     const long long row0 = r * a.T;
     const int bfirst = cta_of(a, row0);
     const int nseg = cta_of(a, row0 + a.T - 1) - bfirst + 1;
     if (nseg == 1)
         return;
-    const int d = threadIdx.x, lane = d & 31, wid = d >> 5;
-    float mq[kHg], lq[kHg];
-#pragma unroll
-    for (int hh = 0; hh < kHg; ++hh) {
-        mq[hh] = -INFINITY;
-        lq[hh] = 0.0f;
+    const int d = threadIdx.x;
+    // part q of the row is slot 2 b + (the row starts inside CTA b's range ? 0 : 1)
+    for (int q = d; q < nseg; q += kVDim) {
+        const int bb = bfirst + q;
+        s_slot[q] = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
     }
-    if (d < nseg) {
-        // part q of the row is slot 2 b + (the row starts inside CTA b's range ? 0 : 1)
-        const int bb = bfirst + d;
-        const int sl = 2 * bb + (tile_start(a, bb) >= row0 ? 0 : 1);
-        s_slot[d] = sl;
-#pragma unroll
-        for (int hh = 0; hh < kHg; ++hh) {
-            mq[hh] = a.ml[(sl * kHeads + h0 + hh) * 2];
-            lq[hh] = a.ml[(sl * kHeads + h0 + hh) * 2 + 1];
+    __syncthreads();
+    for (int t = d; t < nseg * HB; t += kVDim) {
+        const int q = t / HB, h = t - q * HB;
+        s_m[q][h] = a.ml[(s_slot[q] * kHeads + h0 + h) * 2];
+        s_l[q][h] = a.ml[(s_slot[q] * kHeads + h0 + h) * 2 + 1];
+    }
+    __syncthreads();
+    if (d < HB) {
+        float M = -INFINITY;
+        for (int q = 0; q < nseg; ++q)
+            M = fmaxf(M, s_m[q][d]);
+        float L = 0.0f;
+        for (int q = 0; q < nseg; ++q) {
+            const float w = s_m[q][d] == -INFINITY ? 0.0f : ex2_approx(s_m[q][d] - M);
+            s_m[q][d] = w;
+            L += w * s_l[q][d];
         }
-    }
-    float M[kHg], L[kHg];
-#pragma unroll
-    for (int hh = 0; hh < kHg; ++hh) {
-        float v = mq[hh];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-        if (lane == 0)
-            s_red[0][hh][wid] = v;
+        s_M[d] = M;
+        s_L[d] = L;
     }
     __syncthreads();
+    float acc[HB];
 #pragma unroll
-    for (int hh = 0; hh < kHg; ++hh) {
-        float v = s_red[0][hh][0];
-#pragma unroll
-        for (int i = 1; i < 16; ++i)
-            v = fmaxf(v, s_red[0][hh][i]);
-        M[hh] = v;
-        const float w = (d < nseg && mq[hh] != -INFINITY) ? ex2_approx(mq[hh] - v) : 0.0f;
-        if (d < nseg)
-            s_w[d][hh] = w;
-        float t = w * lq[hh];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-        if (lane == 0)
-            s_red[1][hh][wid] = t;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int hh = 0; hh < kHg; ++hh) {
-        float t = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            t += s_red[1][hh][i];
-        L[hh] = t;
-    }
-    float acc[kHg];
-#pragma unroll
-    for (int hh = 0; hh < kHg; ++hh)
-        acc[hh] = 0.0f;
-#pragma unroll 4
+    for (int h = 0; h < HB; ++h)
+        acc[h] = 0.0f;
+#pragma unroll 2
     for (int q = 0; q < nseg; ++q) {
         const float *pp = a.part + ((long long)s_slot[q] * kHeads + h0) * kVDim + d;
 #pragma unroll
-        for (int hh = 0; hh < kHg; ++hh)
-            acc[hh] += s_w[q][hh] * pp[hh * kVDim];
+        for (int h = 0; h < HB; ++h)
+            acc[h] += s_m[q][h] * pp[h * kVDim];
     }
 #pragma unroll
-    for (int hh = 0; hh < kHg; ++hh) {
-        const int h = h0 + hh;
-        const float y = L[hh] > 0.0f ? acc[hh] * (a.kv_scale / L[hh]) : 0.0f;
-        a.out[(r * kHeads + h) * kVDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-        if (a.lse && d == 0)
-            a.lse[r * kHeads + h] =
-                L[hh] > 0.0f ? (M[hh] + log2f(L[hh])) * 0.69314718055994531f : -INFINITY;
+    for (int h = 0; h < HB; ++h) {
+        const float L = s_L[h];
+        const float y = L > 0.0f ? acc[h] * (a.kv_scale / L) : 0.0f;
+        a.out[(r * kHeads + h0 + h) * kVDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
     }
+    if (a.lse && d < HB)
+        a.lse[r * kHeads + h0 + d] =
+            s_L[d] > 0.0f ? (s_M[d] + log2f(s_L[d])) * 0.69314718055994531f : -INFINITY;
 }
 
 // Workspace: status word | (m, l) of each part | the parts' unnormalised
@@ -894,11 +869,11 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        // one head per block for few rows (more blocks in flight), two for many
+        // a block per (row, head) for few rows (enough blocks), per row for many
         const bool few = rows <= 32;
-        cfg.gridDim = dim3((unsigned)rows, few ? kHeads : kHeads / 2);
+        cfg.gridDim = dim3((unsigned)rows, few ? kHeads : 1);
         const cudaError_t e = few ? cudaLaunchKernelEx(&cfg, sparse_mla_combine_kernel<1>, a)
-                                  : cudaLaunchKernelEx(&cfg, sparse_mla_combine_kernel<2>, a);
+                                  : cudaLaunchKernelEx(&cfg, sparse_mla_combine_kernel<kHeads>, a);
         if (e != cudaSuccess)
             return PMQA_ERR_CUDA;
     }
