@@ -33,8 +33,10 @@
 //   * the thread issues O^T += V^T . P^T (M = 128 value columns per block, four
 //     blocks, N = 32, K = 128 positions), reading the SAME tile as an
 //     MN-major operand, into four TMEM accumulators of 32 columns.
-// A row's tiles split over at most a few CTAs: each writes its unnormalised
-// part (O, m, l) to the workspace and the last to arrive combines them.
+// With at most as many rows as SMs every row gets the same number of CTAs
+// (one keeps it whole); with more, the tiles split evenly over the CTAs. A
+// CTA that holds part of a row writes the unnormalised part (O, m, l) to the
+// workspace and a second kernel combines the parts.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -843,8 +845,17 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
     a.W = p->max_blocks_per_seq;
     a.num_blocks = p->num_blocks;
     a.N = rows * T;
-    const long long want = (a.N + PMQA_MLA_MIN_TILES - 1) / PMQA_MLA_MIN_TILES;
-    a.G = (int)std::min<long long>(want, std::min(sms, kMaxCtas));
+    const int ctas = std::min(sms, kMaxCtas);
+    if (rows <= ctas) {
+        // the same number of CTAs for every row, so CTA ranges start at row
+        // starts: rows * per CTAs, per = 1 keeps every row whole (no combine)
+        const long long per = std::max<long long>(
+            1, std::min<long long>(T / PMQA_MLA_MIN_TILES, ctas / rows));
+        a.G = (int)(rows * per);
+    } else {
+        const long long want = (a.N + PMQA_MLA_MIN_TILES - 1) / PMQA_MLA_MIN_TILES;
+        a.G = (int)std::min<long long>(want, ctas);
+    }
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
@@ -858,7 +869,7 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
     sparse_mla_kernel<<<a.G, kThreads, kSmemBytes, st>>>(a);
     if (cudaGetLastError() != cudaSuccess)
         return PMQA_ERR_CUDA;
-    if (a.T > 1) {
+    if (a.T > 1 && a.G != rows) {
         // rows may be split over CTAs: the combining kernel, its launch
         // overlapping the first kernel's end (rows held whole return at once)
         cudaLaunchConfig_t cfg = {};

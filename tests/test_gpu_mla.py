@@ -102,11 +102,12 @@ def test_one_dominant_position(cuda_lib):
     check(out, lse, prob)
 
 
-def test_many_rows_split_over_ctas(cuda_lib):
-    """More tiles than CTAs with rows split at arbitrary tile boundaries (parts
-    combined by the second kernel), and fewer tiles than SMs (every CTA one
-    tile, a row combined from up to 16 parts)."""
-    for bs, nn, seed in ((37, 3, 1), (1, 4, 2)):
+def test_rows_split_over_ctas(cuda_lib):
+    """More rows than SMs (the tiles split evenly over the CTAs, rows cut at
+    arbitrary tile boundaries, parts combined by the second kernel), a few
+    rows (each row over the same number of CTAs), and rows held whole by one
+    CTA each (no combine)."""
+    for bs, nn, seed in ((60, 3, 1), (1, 4, 2), (37, 3, 3)):
         ctx = np.random.default_rng(seed).integers(2100, 9000, size=bs)
         prob = make_mla_problem(bs, nn, 16, 1, ctx, seed=seed)
         out, lse, status = run(cuda_lib, prob)
