@@ -191,3 +191,59 @@ def test_mqa_workspace_and_empty_shapes(lib):
     # nothing to compute: no pointer is needed and nothing is launched
     assert lib.pmqa_mqa_logits(ctypes.byref(_mqa(m=0, q=None)), None, WS, 256, None) == 0
     assert lib.pmqa_mqa_logits(ctypes.byref(_mqa(n=0, k=None)), None, WS, need, None) == 0
+
+
+def _mla(**kw):
+    base = dict(q=0x10000, kv_cache=0x20000, indices=0x30000, block_tables=0x40000,
+                q_scale=0.5, kv_scale=2.0, sm_scale=0.04, bs=2, next_n=2, heads=16, head_dim=576,
+                v_head_dim=512, topk=2048, block_size=1, max_blocks_per_seq=64, num_blocks=128)
+    base.update(kw)
+    return pmqa.MlaProblem(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(heads=32), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(head_dim=512), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(v_head_dim=576), pmqa.PMQA_ERR_UNSUPPORTED),
+    (dict(bs=-1), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(next_n=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(topk=-1), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(block_size=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(max_blocks_per_seq=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(q_scale=float("nan")), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(sm_scale=float("inf")), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(q=None), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(indices=None), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(q=0x10008), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(kv_cache=0x20004), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(indices=0x30002), pmqa.PMQA_ERR_INVALID_ARG),
+    (dict(block_tables=0x40001), pmqa.PMQA_ERR_INVALID_ARG),
+])
+def test_mla_problem_validation(lib, kw, code):
+    need = pmqa.pmqa_sparse_mla_workspace_bytes(4)
+    p = _mla(**kw)
+    assert lib.pmqa_sparse_mla_decode(ctypes.byref(p), ctypes.c_void_p(0x60000), None, WS, need,
+                                      None) == code
+
+
+def test_mla_workspace_outputs_and_empty_batch(lib):
+    need = pmqa.pmqa_sparse_mla_workspace_bytes(4)
+    # status word, the parts' (m, l), the parts' outputs: two parts per CTA, at most 256 CTAs
+    assert need == 256 + 2 * 256 * 16 * 2 * 4 + 2 * 256 * 16 * 512 * 4
+    assert pmqa.pmqa_sparse_mla_workspace_bytes(-1) == 0
+    p = _mla()
+    out = ctypes.c_void_p(0x60000)
+    assert lib.pmqa_sparse_mla_decode(None, out, None, WS, need, None) == -1
+    assert lib.pmqa_sparse_mla_decode(ctypes.byref(p), None, None, WS, need, None) == -1
+    assert lib.pmqa_sparse_mla_decode(ctypes.byref(p), ctypes.c_void_p(0x60002), None, WS, need,
+                                      None) == -1
+    assert lib.pmqa_sparse_mla_decode(ctypes.byref(p), out, ctypes.c_void_p(0x70002), WS, need,
+                                      None) == -1
+    assert lib.pmqa_sparse_mla_decode(ctypes.byref(p), out, None, WS, need - 1,
+                                      None) == pmqa.PMQA_ERR_WORKSPACE
+    assert lib.pmqa_sparse_mla_decode(ctypes.byref(p), out, None, ctypes.c_void_p(0x100010), need,
+                                      None) == -1
+    # no rows: nothing is read or launched
+    empty = _mla(bs=0, q=None, kv_cache=None, indices=None, block_tables=None)
+    assert lib.pmqa_sparse_mla_decode(ctypes.byref(empty), None, None, WS, need, None) == 0
