@@ -333,6 +333,33 @@ int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, float *lse, voi
                            size_t ws_bytes, pmqa_stream_t stream);
 
 /*
+ * The decode restricted to a slice of every request's tokens: request i's rows
+ * attend only to their listed positions t with token_begin[i] <= t <
+ * token_end[i] (device int32 [bs] each); the other listed positions are
+ * skipped, so the block table need only map the slice's pages. This is one
+ * GPU's step of a decode split by context (decode context parallelism: the
+ * chat-gpts.plus summary names an LSE output for it): the slices' outputs and
+ * log-sum-exps are gathered and combined by pmqa_sparse_mla_merge. Otherwise
+ * as pmqa_sparse_mla_decode; a row with no position in its slice gives out = 0
+ * and lse = -inf.
+ */
+int pmqa_sparse_mla_decode_range(const pmqa_mla_problem *p, const int32_t *token_begin,
+                                 const int32_t *token_end, void *out, float *lse, void *ws,
+                                 size_t ws_bytes, pmqa_stream_t stream);
+
+/*
+ * Merge of `parts` partial decodes of the same rows (each over a disjoint part
+ * of every row's listed positions, e.g. the slices of a context split):
+ *   outs  bf16 [parts, rows, heads, 512]; lses fp32 [parts, rows, heads]
+ *   out   bf16 [rows, heads, 512] = sum_g w_g outs[g] / sum_g w_g,
+ *         w_g = exp(lses[g] - max_g lses[g]) (a part with lse -inf weighs 0)
+ *   lse   fp32 [rows, heads] or NULL: max_g lses[g] + ln sum_g w_g
+ * heads must be 16. No workspace; one kernel launch.
+ */
+int pmqa_sparse_mla_merge(const void *outs, const float *lses, int32_t parts, int32_t rows,
+                          int32_t heads, void *out, float *lse, pmqa_stream_t stream);
+
+/*
  * Synchronise the stream, return the device status bits recorded since the
  * last read (>= 0) and clear them, or a negative PMQA_ERR_* code.
  */

@@ -10,9 +10,15 @@ sparse-MLA decode path (page "[Bug][ROCm]: ROCM_AITER_MLA can select an aiter
 MLA decode kernel that silently returns uncorrelated output", chat-gpts.plus
 summary, closing notes); the split itself is this library's design.
 
+The same split serves the sparse MLA decode that consumes the top-k: each GPU
+attends only to the listed positions inside its slice
+(pmqa_sparse_mla_decode_range), the slices' outputs and log-sum-exps are
+all-gathered, and every GPU merges them by their LSE (pmqa_sparse_mla_merge);
+the pages name the LSE output as what decode context parallelism uses.
+
 The functions here only compute slice bounds, restrict a block table to a
-slice's pages and move the candidate lists between processes; every step of
-the computation runs in the library's kernels.
+slice's pages and move the candidate lists and partial outputs between
+processes; every step of the computation runs in the library's kernels.
 """
 
 from __future__ import annotations
@@ -72,3 +78,32 @@ def cp_topk(q, kv_cache, weights, context_lens, block_tables, max_model_len: int
                                             want_vals=True, ws=ws, stream=stream)
     all_i, all_v = gather_lists(idx, vals, group)
     return pmqa.pmqa_topk_merge(all_i, all_v, k, want_vals=True, stream=stream)
+
+
+def gather_parts(out, lse, group=None):
+    """All-gather of every rank's partial decode: out [rows, heads, 512] (bf16,
+    moved as its 16-bit patterns) and lse [rows, heads] into [world, ...]
+    tensors in rank order."""
+    import torch
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    bits = out.contiguous().view(torch.int16)
+    out_b = [torch.empty_like(bits) for _ in range(world)]
+    out_l = [torch.empty_like(lse) for _ in range(world)]
+    dist.all_gather(out_b, bits, group=group)
+    dist.all_gather(out_l, lse.contiguous(), group=group)
+    return torch.stack(out_b).view(torch.bfloat16), torch.stack(out_l)
+
+
+def cp_mla_decode(q, kv_cache, indices, block_tables, next_n: int, q_scale: float,
+                  kv_scale: float, sm_scale: float, token_begin, token_end, *, group=None,
+                  ws=None, stream=None):
+    """One context-parallel decode step on this rank: the slice's partial
+    decode, the all-gather of every rank's (out, lse), the merge. Returns
+    (out, lse) of the whole rows, the same on every rank."""
+    out, lse = pmqa.pmqa_sparse_mla_decode_range(q, kv_cache, indices, block_tables, next_n,
+                                                 q_scale, kv_scale, sm_scale, token_begin,
+                                                 token_end, ws=ws, stream=stream)
+    outs, lses = gather_parts(out, lse, group)
+    return pmqa.pmqa_sparse_mla_merge(outs, lses, stream=stream)

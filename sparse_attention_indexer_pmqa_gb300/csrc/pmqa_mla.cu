@@ -137,6 +137,8 @@ struct Args {
     int G;                // CTAs
     uint16_t *out;        // bf16 [R, 16, 512]
     float *lse;           // [R, 16] or null
+    const int32_t *tok_begin;  // [bs] or null: only positions in [tok_begin_i, tok_end_i)
+    const int32_t *tok_end;
     uint32_t *status;
     float *ml;            // [2 G][16][2] (m, l) of each part
     float *part;          // [2 G][16][512] unnormalised output of each part
@@ -286,9 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
             return __ldg(a.bt + (x / a.T) / a.next_n * a.W + pos / a.P);
         };
         // pool row of a looked-up position, -1 for none (bad entries recorded)
-        auto row_of = [&](int pos, int page) -> long long {
+        auto row_of = [&](int pos, int page, long long x) -> long long {
             if (pos < 0)
                 return -1;
+            if (a.tok_begin) {
+                // a slice of the request's tokens: other positions are not this call's
+                const long long i = (x / a.T) / a.next_n;
+                if (pos < __ldg(a.tok_begin + i) || pos >= __ldg(a.tok_end + i))
+                    return -1;
+            }
             if ((long long)pos >= wp) {
                 atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_CONTEXT);
                 return -1;
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 ++seg;
             const int pos3 = load_pos(x + 3);
             const int page2 = load_page(x + 2, pos2);
-            const long long srow = row_of(pos0, page0);
+            const long long srow = row_of(pos0, page0, x);
             pos0 = pos1;
             page0 = page1;
             pos1 = pos2;
@@ -794,8 +802,9 @@ extern "C" size_t pmqa_sparse_mla_workspace_bytes(int32_t rows)
     return L.total;
 }
 
-extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, float *lse, void *ws,
-                                      size_t ws_bytes, pmqa_stream_t stream)
+static int sparse_mla_call(const pmqa_mla_problem *p, const int32_t *tok_begin,
+                           const int32_t *tok_end, void *out, float *lse, void *ws,
+                           size_t ws_bytes, pmqa_stream_t stream)
 {
     auto aligned = [](const void *ptr, uintptr_t al) {
         return (reinterpret_cast<uintptr_t>(ptr) % al) == 0;
@@ -822,6 +831,9 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
         return PMQA_ERR_INVALID_ARG;
     if (!aligned(p->q, 16) || !aligned(p->kv_cache, 16) || !aligned(p->indices, 4) ||
         !aligned(p->block_tables, 4) || !aligned(out, 4) || (lse && !aligned(lse, 4)))
+        return PMQA_ERR_INVALID_ARG;
+    if ((tok_begin != nullptr) != (tok_end != nullptr) ||
+        (tok_begin && (!aligned(tok_begin, 4) || !aligned(tok_end, 4))))
         return PMQA_ERR_INVALID_ARG;
     const long long T = std::max<long long>(1, (p->topk + kTile - 1) / kTile);
     if (rows * T > (1ll << 40))
@@ -857,6 +869,8 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
         a.G = (int)std::min<long long>(want, ctas);
     }
     uint8_t *wsb = static_cast<uint8_t *>(ws);
+    a.tok_begin = tok_begin;
+    a.tok_end = tok_end;
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
     a.status = reinterpret_cast<uint32_t *>(wsb);
@@ -888,5 +902,83 @@ extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, floa
         if (e != cudaSuccess)
             return PMQA_ERR_CUDA;
     }
+    return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
+}
+
+namespace pmqa {
+namespace mla {
+
+// Merge of G partial decodes of the same rows (one per slice of the listed
+// positions): out = sum_g w_g out_g / sum_g w_g and lse = M + ln sum_g w_g with
+// w_g = exp(lse_g - M), M = max_g lse_g; a part with lse = -inf has weight 0.
+// Block (r, h): thread d value column d.
+__global__ void __launch_bounds__(kVDim) sparse_mla_merge_kernel(const uint16_t *outs,
+                                                                 const float *lses, int G,
+                                                                 long long rows, uint16_t *out,
+                                                                 float *lse)
+{
+    const long long r = blockIdx.x;
+    const int h = (int)blockIdx.y, d = (int)threadIdx.x;
+    const long long rh = r * kHeads + h;
+    const long long part_stride = rows * kHeads;  // (row, head) pairs per part
+    float M = -INFINITY;
+    for (int g = 0; g < G; ++g)
+        M = fmaxf(M, __ldg(lses + g * part_stride + rh));
+    float L = 0.0f, acc = 0.0f;
+    for (int g = 0; g < G; ++g) {
+        const float lg = __ldg(lses + g * part_stride + rh);
+        if (lg == -INFINITY)
+            continue;
+        const float w = expf(lg - M);
+        L += w;
+        const uint16_t b = __ldg(outs + (g * part_stride + rh) * kVDim + d);
+        acc += w * __bfloat162float(__ushort_as_bfloat16(b));
+    }
+    const float y = L > 0.0f ? acc / L : 0.0f;
+    out[rh * kVDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+    if (lse && d == 0)
+        lse[rh] = L > 0.0f ? M + logf(L) : -INFINITY;
+}
+
+}  // namespace mla
+}  // namespace pmqa
+
+extern "C" int pmqa_sparse_mla_decode(const pmqa_mla_problem *p, void *out, float *lse, void *ws,
+                                      size_t ws_bytes, pmqa_stream_t stream)
+{
+    return sparse_mla_call(p, nullptr, nullptr, out, lse, ws, ws_bytes, stream);
+}
+
+extern "C" int pmqa_sparse_mla_decode_range(const pmqa_mla_problem *p,
+                                            const int32_t *token_begin,
+                                            const int32_t *token_end, void *out, float *lse,
+                                            void *ws, size_t ws_bytes, pmqa_stream_t stream)
+{
+    if (!token_begin || !token_end)
+        return PMQA_ERR_INVALID_ARG;
+    return sparse_mla_call(p, token_begin, token_end, out, lse, ws, ws_bytes, stream);
+}
+
+extern "C" int pmqa_sparse_mla_merge(const void *outs, const float *lses, int32_t parts,
+                                     int32_t rows, int32_t heads, void *out, float *lse,
+                                     pmqa_stream_t stream)
+{
+    auto aligned = [](const void *ptr, uintptr_t al) {
+        return (reinterpret_cast<uintptr_t>(ptr) % al) == 0;
+    };
+    if (parts < 1 || rows < 0 || heads < 1)
+        return PMQA_ERR_INVALID_ARG;
+    if (heads != kHeads)
+        return PMQA_ERR_UNSUPPORTED;
+    if (rows == 0)
+        return PMQA_OK;
+    if (!outs || !lses || !out || !aligned(outs, 4) || !aligned(lses, 4) || !aligned(out, 4) ||
+        (lse && !aligned(lse, 4)))
+        return PMQA_ERR_INVALID_ARG;
+    if ((long long)rows > 0x7FFFFFFFll)
+        return PMQA_ERR_UNSUPPORTED;
+    sparse_mla_merge_kernel<<<dim3((unsigned)rows, kHeads), kVDim, 0,
+                              reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(outs), lses, parts, rows, static_cast<uint16_t *>(out), lse);
     return cudaGetLastError() == cudaSuccess ? PMQA_OK : PMQA_ERR_CUDA;
 }

@@ -39,7 +39,8 @@ EXPORTED = (
     "pmqa_logits_topk", "pmqa_logits_topk_stages", "pmqa_logits_topk_noalloc",
     "pmqa_logits_topk_range",
     "pmqa_mqa_logits", "pmqa_topk_merge", "pmqa_sparse_mla_workspace_bytes",
-    "pmqa_sparse_mla_decode", "pmqa_read_device_status", "pmqa_status_string", "pmqa_version",
+    "pmqa_sparse_mla_decode", "pmqa_sparse_mla_decode_range", "pmqa_sparse_mla_merge",
+    "pmqa_read_device_status", "pmqa_status_string", "pmqa_version",
 )
 
 
@@ -143,6 +144,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pmqa_topk_merge": ([V, V, I32, I32, I32, I32, V, V, V], ctypes.c_int),
         "pmqa_sparse_mla_workspace_bytes": ([I32], SZ),
         "pmqa_sparse_mla_decode": ([PL, V, V, V, SZ, V], ctypes.c_int),
+        "pmqa_sparse_mla_decode_range": ([PL, V, V, V, V, V, SZ, V], ctypes.c_int),
+        "pmqa_sparse_mla_merge": ([V, V, I32, I32, I32, V, V, V], ctypes.c_int),
         "pmqa_read_device_status": ([V, V], ctypes.c_int),
         "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pmqa_version": ([], ctypes.c_int),
@@ -408,6 +411,46 @@ def pmqa_sparse_mla_decode(q, kv_cache, indices, block_tables, next_n: int, q_sc
     _check(load().pmqa_sparse_mla_decode(ctypes.byref(p), _ptr(out), _ptr(lse), _ptr(ws),
                                          ws.numel(), _stream(stream)), "pmqa_sparse_mla_decode")
     return (out, lse) if want_lse or lse is not None else out
+
+
+def pmqa_sparse_mla_decode_range(q, kv_cache, indices, block_tables, next_n: int, q_scale: float,
+                                 kv_scale: float, sm_scale: float, token_begin, token_end, *,
+                                 out=None, lse=None, ws=None, stream=None):
+    """The decode over each request's slice [token_begin[i], token_end[i]) of
+    its tokens: (bf16 out [rows, heads, 512], fp32 lse [rows, heads])."""
+    import torch
+
+    p = make_mla_problem(q, kv_cache, indices, block_tables, next_n, q_scale, kv_scale, sm_scale)
+    rows = p.bs * p.next_n
+    for t in (token_begin, token_end):
+        assert t.is_cuda and t.is_contiguous() and t.dtype == torch.int32 and t.numel() == p.bs
+    if out is None:
+        out = torch.empty((rows, p.heads, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((rows, p.heads), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = mla_workspace(rows, q.device, stream)
+    _check(load().pmqa_sparse_mla_decode_range(ctypes.byref(p), _ptr(token_begin), _ptr(token_end),
+                                               _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                               _stream(stream)), "pmqa_sparse_mla_decode_range")
+    return out, lse
+
+
+def pmqa_sparse_mla_merge(outs, lses, *, out=None, lse=None, stream=None):
+    """LSE-weighted merge of partial decodes outs [parts, rows, heads, 512]
+    (bf16) with lses [parts, rows, heads]; returns (out, lse)."""
+    import torch
+
+    parts, rows, heads, vdim = outs.shape
+    assert lses.shape == (parts, rows, heads) and vdim == 512
+    assert outs.is_contiguous() and lses.is_contiguous() and outs.dtype == torch.bfloat16
+    if out is None:
+        out = torch.empty((rows, heads, vdim), dtype=torch.bfloat16, device=outs.device)
+    if lse is None:
+        lse = torch.empty((rows, heads), dtype=torch.float32, device=outs.device)
+    _check(load().pmqa_sparse_mla_merge(_ptr(outs), _ptr(lses), parts, rows, heads, _ptr(out),
+                                        _ptr(lse), _stream(stream)), "pmqa_sparse_mla_merge")
+    return out, lse
 
 
 def pmqa_read_device_status(ws, stream=None) -> int:

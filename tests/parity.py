@@ -93,20 +93,24 @@ def check_topk_exact(idx: np.ndarray, vals32: np.ndarray, ctx, nn: int, k: int) 
         assert np.array_equal(got, want), f"row {r}: selected values differ from the top-{ke}"
 
 
-def check_mla(out, lse, ref, lref, tol):
+def check_mla(out, lse, ref, lref, tol, parts: int = 1):
     """Sparse MLA decode outputs against the oracle's. Tolerance per output
     entry, from the kernel's arithmetic: scores within e_s = 2^-9 * s_abs of
     exact (fp8 products summed on the tensor cores) move an output by at most
     e_s * d_abs; the softmax weights enter the second product as two fp8 terms
     (relative error 2^-8), at most 2^-7 * a_abs with margin; the bf16 output
     rounds by 2^-9 relative, 2^-8 |out| with margin. lse within e_s + 1e-4;
-    rows with no listed position exactly 0 and -inf. Returns (worst error as a
+    rows with no listed position exactly 0 and -inf. A merge of `parts` > 1
+    partial decodes (each rounded to bf16 before the merge) adds 2^-8 * a_abs.
+    Returns (worst error as a
     fraction of its bound, cos_diff = 1 - 2 <x, y> / (|x|^2 + |y|^2), the
     agreement measure the pages quote for MLA decode)."""
     out = np.asarray(out, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     e_s = 2.0 ** -9 * tol["s_abs"]
     bound = e_s[..., None] * tol["d_abs"] + 2.0 ** -7 * tol["a_abs"] + 2.0 ** -8 * np.abs(ref) + 1e-6
+    if parts > 1:
+        bound = bound + 2.0 ** -8 * tol["a_abs"]
     err = np.abs(out - ref)
     bad = err > bound
     assert not bad.any(), (

@@ -247,3 +247,26 @@ def test_mla_workspace_outputs_and_empty_batch(lib):
     # no rows: nothing is read or launched
     empty = _mla(bs=0, q=None, kv_cache=None, indices=None, block_tables=None)
     assert lib.pmqa_sparse_mla_decode(ctypes.byref(empty), None, None, WS, need, None) == 0
+
+
+def test_mla_range_and_merge_validation(lib):
+    need = pmqa.pmqa_sparse_mla_workspace_bytes(4)
+    p = _mla()
+    out = ctypes.c_void_p(0x60000)
+    B, E = ctypes.c_void_p(0x80000), ctypes.c_void_p(0x81000)
+    assert lib.pmqa_sparse_mla_decode_range(ctypes.byref(p), None, E, out, None, WS, need,
+                                            None) == -1
+    assert lib.pmqa_sparse_mla_decode_range(ctypes.byref(p), B, None, out, None, WS, need,
+                                            None) == -1
+    assert lib.pmqa_sparse_mla_decode_range(ctypes.byref(p), ctypes.c_void_p(0x80002), E, out,
+                                            None, WS, need, None) == -1
+    assert lib.pmqa_sparse_mla_decode_range(ctypes.byref(_mla(heads=8)), B, E, out, None, WS,
+                                            need, None) == pmqa.PMQA_ERR_UNSUPPORTED
+    O, L = ctypes.c_void_p(0x90000), ctypes.c_void_p(0xA0000)
+    assert lib.pmqa_sparse_mla_merge(O, L, 0, 4, 16, out, None, None) == -1
+    assert lib.pmqa_sparse_mla_merge(O, L, 2, -1, 16, out, None, None) == -1
+    assert lib.pmqa_sparse_mla_merge(O, L, 2, 4, 32, out, None, None) == pmqa.PMQA_ERR_UNSUPPORTED
+    assert lib.pmqa_sparse_mla_merge(None, L, 2, 4, 16, out, None, None) == -1
+    assert lib.pmqa_sparse_mla_merge(O, L, 2, 4, 16, None, None, None) == -1
+    assert lib.pmqa_sparse_mla_merge(O, ctypes.c_void_p(0xA0002), 2, 4, 16, out, None, None) == -1
+    assert lib.pmqa_sparse_mla_merge(None, None, 2, 0, 16, None, None, None) == 0

@@ -96,3 +96,51 @@ def test_gather_over_gloo_and_the_union_top_k():
         got, _ = _topk_window(np.where(np.isin(np.arange(r64.shape[1]), cand), r64[r], -np.inf),
                               0, n, min(k, n))
         assert np.array_equal(np.sort(got), np.sort(want))
+
+
+def _mla_rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    from synth.mla import MlaProblem, make_mla_problem
+
+    prob = make_mla_problem(2, 3, 16, 1, [1200, 700], topk=512, seed=5)
+    b, e = slice_bounds(prob.context_lens, world, rank)
+    filt = prob.indices.copy()
+    for r in range(prob.rows):
+        i = r // prob.next_n
+        filt[r][(filt[r] < b[i]) | (filt[r] >= e[i])] = -1
+    o, l, _ = oracle.sparse_mla(MlaProblem(**{**prob.__dict__, "indices": filt}))
+    go = [torch.empty(o.shape, dtype=torch.float64) for _ in range(world)]
+    gl = [torch.empty(l.shape, dtype=torch.float64) for _ in range(world)]
+    torch.distributed.all_gather(go, torch.from_numpy(o))
+    torch.distributed.all_gather(gl, torch.from_numpy(l))
+    out[rank] = (torch.stack(go).numpy(), torch.stack(gl).numpy())
+    torch.distributed.destroy_process_group()
+
+
+def test_lse_merge_of_slice_decodes_over_gloo():
+    """The decode split by context: each rank's oracle decode over the listed
+    positions of its slice, gathered over a two-rank gloo group, merged by the
+    slices' log-sum-exps (w_g = exp(lse_g - max), out = sum w_g out_g / sum w_g,
+    lse = max + ln sum w_g), equals the oracle's whole decode."""
+    from synth.mla import make_mla_problem
+
+    world = 2
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_mla_rank, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    outs, lses = res[0]
+    assert np.array_equal(outs, res[1][0]) and np.array_equal(lses, res[1][1])
+    M = lses.max(axis=0)
+    w = np.where(np.isneginf(lses), 0.0, np.exp(lses - np.where(np.isneginf(M), 0.0, M)))
+    L = w.sum(axis=0)
+    merged = (w[..., None] * outs).sum(axis=0) / np.where(L > 0, L, 1.0)[..., None]
+    lse = np.where(L > 0, M + np.log(np.where(L > 0, L, 1.0)), -np.inf)
+    prob = make_mla_problem(2, 3, 16, 1, [1200, 700], topk=512, seed=5)
+    ref, lref, _ = oracle.sparse_mla(prob)
+    np.testing.assert_allclose(merged, ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, lref, rtol=1e-12)

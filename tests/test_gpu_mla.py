@@ -170,3 +170,43 @@ def test_decode_over_the_indexers_top_k(cuda_lib):
     out, lse, status = run(cuda_lib, prob)
     assert status == 0
     check(out, lse, prob)
+
+
+@pytest.mark.parametrize("slices,P", [(2, 1), (4, 1), (3, 16)])
+def test_context_parallel_decode(cuda_lib, slices, P):
+    """The decode split by context: each slice attends to its listed positions
+    only, against a block table that maps only its pages (checked against the
+    oracle with the listing restricted to the slice), and the LSE merge of the
+    slices against the oracle's whole decode."""
+    from sparse_attention_indexer_pmqa_gb300.context_parallel import slice_bounds, slice_table
+
+    prob = make_mla_problem(3, 4, 16, P, [5000, 300, 9000], topk=2048, seed=12 + slices,
+                            holes=0.05)
+    dev = "cuda"
+    q = torch.from_numpy(prob.q.reshape(prob.rows, prob.heads, MLA_DIM)).to(dev)
+    kv = torch.from_numpy(prob.kv).to(dev)
+    idx = torch.from_numpy(prob.indices).to(dev)
+    outs, lses = [], []
+    for rank in range(slices):
+        b, e = slice_bounds(prob.context_lens, slices, rank)
+        bt = torch.from_numpy(slice_table(prob.block_tables, b, e, P)).to(dev)
+        ws = cuda_lib.mla_workspace(prob.rows)
+        out, lse = cuda_lib.pmqa_sparse_mla_decode_range(
+            q, kv, idx, bt, prob.next_n, prob.q_scale, prob.kv_scale, prob.sm_scale,
+            torch.from_numpy(b).to(dev), torch.from_numpy(e).to(dev), ws=ws)
+        torch.cuda.synchronize()
+        assert cuda_lib.pmqa_read_device_status(ws) == 0  # no page outside the slice was read
+        filt = prob.indices.copy()
+        for r in range(prob.rows):
+            i = r // prob.next_n
+            outside = (filt[r] < b[i]) | (filt[r] >= e[i])
+            filt[r][outside] = -1
+        part = MlaProblem(**{**prob.__dict__, "indices": filt})
+        check(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+              part)
+        outs.append(out)
+        lses.append(lse)
+    mo, ml = cuda_lib.pmqa_sparse_mla_merge(torch.stack(outs), torch.stack(lses))
+    torch.cuda.synchronize()
+    ref, lref, tol = oracle.sparse_mla(prob, want_tol=True)
+    check_mla(mo.float().cpu().numpy(), ml.cpu().numpy(), ref, lref, tol, parts=slices)
