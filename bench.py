@@ -60,6 +60,10 @@ def parse_args(argv=None):
     ap.add_argument("--mla", nargs="*", default=None,
                     help="also time the sparse MLA decode workloads (all of them, or the ones "
                          "named) under --headline-only")
+    ap.add_argument("--gather-ceiling", action="store_true",
+                    help="instead of the step: time the row-gather probe (three issue methods) "
+                         "on the rows the KV pass reads on C2 and C3 and the rows the sparse "
+                         "MLA decode reads on M1, beside those kernels")
     ap.add_argument("--prefill", action="store_true",
                     help="also time the prefill (non-paged) logits on PF1 (on with --all)")
     args = ap.parse_args(argv)
@@ -796,6 +800,130 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- gather ceiling
+
+GATHER_METHODS = {0: "ld16 (16-byte loads into registers)",
+                  1: "cp.async16 (16-byte cp.async into shared memory)",
+                  2: "bulk (one cp.async.bulk per row window)"}
+
+
+def gather_rows(name):
+    """The physical rows a kernel reads, in its order: every token of every
+    request for the KV pass (C*), every listed position of every query row for
+    the sparse MLA decode (M*). Returns (pool array, int32 rows, row pitch)."""
+    import numpy as np
+
+    if name.startswith("M"):
+        from synth import mla_config
+
+        p = mla_config(name)
+        req = np.arange(p.rows) // p.next_n
+        pos = p.indices.astype(np.int64)
+        ok = pos >= 0
+        page = p.block_tables[np.repeat(req, p.topk).reshape(p.rows, p.topk),
+                              np.where(ok, pos // p.block_size, 0)]
+        rows = (page.astype(np.int64) * p.block_size + pos % p.block_size)[ok]
+        return p.kv, rows.astype(np.int32), 576
+    from synth import config_problem
+
+    p = config_problem(name)
+    P = p.block_size
+    parts = []
+    for i, c in enumerate(p.context_lens):
+        t = np.arange(int(c), dtype=np.int64)
+        parts.append(p.block_tables[i, t // P].astype(np.int64) * P + t % P)
+    return p.kv, np.concatenate(parts).astype(np.int32), 132
+
+
+def run_gather_ceiling(args):
+    """How fast the GPU reads the same random rows the kernels read, by three
+    issue methods (pmqa_gather_probe), beside the kernels' own times on the
+    same workloads. One JSON line."""
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from sparse_attention_indexer_pmqa_gb300 import pmqa
+
+    peak, peak_kind = read_peak()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    reps = max(1, min(args.steps, 20))
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    sampler.start()
+    res = {}
+    for name in ("C2", "C3", "M1"):
+        pool_np, rows_np, pitch = gather_rows(name)
+        pool = torch.from_numpy(pool_np.reshape(-1)).to(device)
+        rows = torch.from_numpy(rows_np).to(device)
+        n = rows.numel()
+        win = 144 if pitch == 132 else 576
+        skipped = int(((rows_np.astype(np.int64) * pitch) // 16 * 16 + win > pool_np.size).sum())
+        entry = {"rows": n, "row_bytes": pitch, "window_bytes": win,
+                 "row_bytes_total": n * pitch, "rows_skipped_at_pool_end": skipped,
+                 "methods": {}}
+        xors = {}
+        for m, label in GATHER_METHODS.items():
+            out = torch.zeros(2, dtype=torch.int32, device=device)
+
+            def call():
+                pmqa.pmqa_gather_probe(pool, rows, pitch, m, out=out)
+
+            for _ in range(max(args.warmup, 1)):
+                flush()
+                call()
+            torch.cuda.synchronize()
+            out.zero_()
+            times = time_steps(call, reps, flush)
+            o = out.cpu().tolist()
+            # a window that would pass the pool's end (the pool's last row, read
+            # as a 144-byte window) is skipped and flagged, nothing else
+            if o[0] != (pmqa.PMQA_DEV_BAD_CONTEXT if skipped else 0):
+                raise RuntimeError(f"gather probe status {o[0]:#x} on {name}, method {m}")
+            xors[m] = o[1] if reps % 2 else None
+            ms = statistics.fmean(times)
+            entry["methods"][label] = {
+                "us": ms * 1e3, "us_median": statistics.median(times) * 1e3,
+                "row_gbs": n * pitch / (ms * 1e-3) / 1e9,
+                "window_gbs": n * win / (ms * 1e-3) / 1e9,
+                "row_frac": n * pitch / (ms * 1e-3) / 1e9 / peak}
+        if xors[1] is not None and xors[1] != xors[2]:
+            raise RuntimeError(f"cp.async and bulk copies read different bytes on {name}")
+        if name.startswith("M"):
+            r = bench_mla(name, args, device)
+            entry["kernel"] = {"what": "pmqa_sparse_mla_decode (one call)", "us": r["us"],
+                               "row_gbs": r["roofline"]["achieved"],
+                               "row_frac": r["roofline"]["frac"]}
+        else:
+            r = bench_workload(name, args, device, None, with_e2e=False, with_paths=False)
+            kv_bytes = 132 * r["prob"].total_ctx
+            entry["kernel"] = {"what": "KV pass (SCORE stage of pmqa_logits_topk)",
+                               "us": r["ms_score"] * 1e3,
+                               "row_gbs": kv_bytes / (r["ms_score"] * 1e-3) / 1e9,
+                               "row_frac": kv_bytes / (r["ms_score"] * 1e-3) / 1e9 / peak}
+        best = max(v["row_gbs"] for v in entry["methods"].values())
+        entry["kernel"]["of_best_probe"] = entry["kernel"]["row_gbs"] / best
+        res[name] = entry
+        del pool, rows
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    line = {"gather_ceiling": res, "peak": peak, "peak_source": f"{peak_kind} hbm_gbs",
+            "reps": reps, "l2": "flushed before every timed launch (256 MB device write)",
+            "note": "row_gbs counts the row bytes (132 or 576 per row); window_gbs the "
+                    "16-byte aligned windows read"}
+    if clocks:
+        line["clocks"] = clocks
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- reference arm
 
 
@@ -856,6 +984,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.gather_ceiling:
+        run_gather_ceiling(args)
     else:
         run_ours(args)
 

@@ -360,6 +360,28 @@ int pmqa_sparse_mla_merge(const void *outs, const float *lses, int32_t parts, in
                           int32_t heads, void *out, float *lse, pmqa_stream_t stream);
 
 /*
+ * Measurement aid beside the decode path (computes nothing of the method): reads
+ * the rows rows[0..n) of a pool of fixed-pitch rows, each as its 16-byte aligned
+ * window (144 bytes for row_pitch 132, the token row of the KV cache; 576 bytes
+ * for row_pitch 576, the latent row of the MLA cache), to time how fast the GPU
+ * gathers such rows. One launch, one CTA per SM.
+ *   pool      device, 16-byte aligned, pool_bytes long; a window that would pass
+ *             its end, and a negative row, is skipped (PMQA_DEV_BAD_CONTEXT in out[0])
+ *   rows      device int32 [n]
+ *   method    0: 16-byte loads into registers; 1: 16-byte cp.async into shared
+ *             memory; 2: one bulk copy (cp.async.bulk) per window into shared memory
+ *   out       device uint32 [2], zeroed by the caller: out[0] |= status bits
+ *             (PMQA_DEV_TIMEOUT for a wait that ran out), out[1] ^= the XOR of
+ *             every 32-bit word read (method 0) or of each window's first
+ *             word (methods 1, 2)
+ * Returns PMQA_ERR_UNSUPPORTED for another pitch, PMQA_ERR_INVALID_ARG for
+ * n < 0, a method outside 0..2, a null or misaligned pointer (n = 0 launches
+ * nothing and returns PMQA_OK).
+ */
+int pmqa_gather_probe(const void *pool, uint64_t pool_bytes, const int32_t *rows, int64_t n,
+                      int32_t row_pitch, int32_t method, uint32_t *out, pmqa_stream_t stream);
+
+/*
  * Synchronise the stream, return the device status bits recorded since the
  * last read (>= 0) and clear them, or a negative PMQA_ERR_* code.
  */

@@ -1,8 +1,8 @@
 """Build libpmqa.so in-tree with nvcc for sm_103a (GB300).
 
-Eleven translation units compile in parallel (the C ABI, the allocation-free
-entry point, the sparse MLA decode, and the decode and the prefill kernel once
-per supported head count) and link into one shared library
+Twelve translation units compile in parallel (the C ABI, the allocation-free
+entry point, the sparse MLA decode, the row-gather probe, and the decode and the
+prefill kernel once per supported head count) and link into one shared library
 with the CUDA runtime linked statically, so the library loads on a machine
 without a GPU too.
 """
@@ -34,7 +34,8 @@ def _sources():
     deps.append(os.path.join(INCLUDE, "pmqa.h"))
     units = [("pmqa_api", os.path.join(CSRC, "pmqa_api.cu"), []),
              ("pmqa_noalloc", os.path.join(CSRC, "pmqa_noalloc.cu"), []),
-             ("pmqa_mla", os.path.join(CSRC, "pmqa_mla.cu"), [])]
+             ("pmqa_mla", os.path.join(CSRC, "pmqa_mla.cu"), []),
+             ("pmqa_gather_probe", os.path.join(CSRC, "pmqa_gather_probe.cu"), [])]
     for h in HEADS:
         units.append((f"pmqa_main_h{h}", os.path.join(CSRC, "pmqa_main_inst.cu"),
                       [f"-DPMQA_HEADS={h}"]))

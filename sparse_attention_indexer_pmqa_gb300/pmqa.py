@@ -40,7 +40,7 @@ EXPORTED = (
     "pmqa_logits_topk_range",
     "pmqa_mqa_logits", "pmqa_topk_merge", "pmqa_sparse_mla_workspace_bytes",
     "pmqa_sparse_mla_decode", "pmqa_sparse_mla_decode_range", "pmqa_sparse_mla_merge",
-    "pmqa_read_device_status", "pmqa_status_string", "pmqa_version",
+    "pmqa_gather_probe", "pmqa_read_device_status", "pmqa_status_string", "pmqa_version",
 )
 
 
@@ -146,6 +146,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pmqa_sparse_mla_decode": ([PL, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_sparse_mla_decode_range": ([PL, V, V, V, V, V, SZ, V], ctypes.c_int),
         "pmqa_sparse_mla_merge": ([V, V, I32, I32, I32, V, V, V], ctypes.c_int),
+        "pmqa_gather_probe": ([V, ctypes.c_uint64, V, I64, I32, I32, V, V], ctypes.c_int),
         "pmqa_read_device_status": ([V, V], ctypes.c_int),
         "pmqa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "pmqa_version": ([], ctypes.c_int),
@@ -451,6 +452,22 @@ def pmqa_sparse_mla_merge(outs, lses, *, out=None, lse=None, stream=None):
     _check(load().pmqa_sparse_mla_merge(_ptr(outs), _ptr(lses), parts, rows, heads, _ptr(out),
                                         _ptr(lse), _stream(stream)), "pmqa_sparse_mla_merge")
     return out, lse
+
+
+def pmqa_gather_probe(pool, rows, row_pitch, method, *, out=None, stream=None):
+    """Read the pool's rows `rows` (int32) as 16-byte aligned windows by one
+    of three issue methods (a timing aid; include/pmqa.h). Returns `out`
+    (uint32 [2] viewed as int32: status bits, XOR of what was read), which
+    accumulates over calls when passed in."""
+    import torch
+
+    assert rows.dtype == torch.int32 and rows.is_contiguous() and pool.is_contiguous()
+    if out is None:
+        out = torch.zeros(2, dtype=torch.int32, device=pool.device)
+    _check(load().pmqa_gather_probe(_ptr(pool), pool.numel() * pool.element_size(), _ptr(rows),
+                                    rows.numel(), row_pitch, method, _ptr(out), _stream(stream)),
+           "pmqa_gather_probe")
+    return out
 
 
 def pmqa_read_device_status(ws, stream=None) -> int:

@@ -270,3 +270,19 @@ def test_mla_range_and_merge_validation(lib):
     assert lib.pmqa_sparse_mla_merge(O, L, 2, 4, 16, None, None, None) == -1
     assert lib.pmqa_sparse_mla_merge(O, ctypes.c_void_p(0xA0002), 2, 4, 16, out, None, None) == -1
     assert lib.pmqa_sparse_mla_merge(None, None, 2, 0, 16, None, None, None) == 0
+
+
+def test_gather_probe_validation(lib):
+    pool, rows, out = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000), ctypes.c_void_p(0x300000)
+    f = lib.pmqa_gather_probe
+    assert f(pool, 1 << 20, rows, -1, 132, 0, out, None) == -1
+    assert f(pool, 1 << 20, rows, 10, 132, 3, out, None) == -1
+    assert f(pool, 1 << 20, rows, 10, 132, -1, out, None) == -1
+    assert f(pool, 1 << 20, rows, 10, 128, 0, out, None) == pmqa.PMQA_ERR_UNSUPPORTED
+    assert f(None, 1 << 20, rows, 10, 576, 1, out, None) == -1
+    assert f(pool, 1 << 20, None, 10, 576, 1, out, None) == -1
+    assert f(pool, 1 << 20, rows, 10, 576, 2, None, None) == -1
+    assert f(ctypes.c_void_p(0x100008), 1 << 20, rows, 10, 132, 0, out, None) == -1
+    assert f(pool, 1 << 20, ctypes.c_void_p(0x200002), 10, 132, 0, out, None) == -1
+    assert f(pool, 1 << 20, rows, 10, 132, 0, ctypes.c_void_p(0x300002), None) == -1
+    assert f(None, 0, None, 0, 132, 2, None, None) == 0  # nothing to read: no launch
