@@ -11,7 +11,7 @@ namespace pmqa {
 
 static_assert(kMaxThreads <= 32 * 32, "CtaCtl holds per-warp sums for at most 32 warps");
 
-template <int H, bool SLICED>
+template <int H, bool SLICED, bool PAGE>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     pmqa_main_kernel(const __grid_constant__ MainArgs a)
 {
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     }
 
-    group_role<H, SLICED>(a, smem, ctl, warp >> 2, warp & 3);
+    group_role<H, SLICED, PAGE>(a, smem, ctl, warp >> 2, warp & 3);
 
     tc_fence_before_sync();
     __syncthreads();

@@ -490,6 +490,9 @@ struct Walk {
 // One warpgroup's gather of its own tiles: the block-table entries, the copies
 // of a tile's rows into the warpgroup's staging slot, and the repack of this
 // thread's row R into the 128B-swizzled K-major operand tile behind the slot.
+// PAGE: rows move as page runs by bulk copy (block size a multiple of 4), else
+// as 16-byte aligned windows by cp.async.
+template <bool PAGE>
 struct TileGather {
     const uint8_t *kv;
     const int32_t *bt;
@@ -497,7 +500,7 @@ struct TileGather {
     uint32_t *status;
     uint64_t pol;
     int P, W, p_shift;
-    bool p_pow2, page_mode, pool32;
+    bool p_pow2, pool32;
     uint32_t R, lane, last9;
     uint32_t stage, win, opx, wstage;
     uint64_t *run_bar;
@@ -519,12 +522,11 @@ struct TileGather {
         p_pow2 = (P & (P - 1)) == 0;
         p_shift = __ffs(P) - 1;
         status = a.status;
-        page_mode = a.page_mode != 0;
         lane = lane_;
         R = qd * 32u + lane;
         stage = stage_addr;
         // window mode: row R's 16-byte aligned window; page runs: the row itself
-        win = stage + (page_mode ? R * (uint32_t)kKvRowBytes : R * kWinBytes);
+        win = stage + (PAGE ? R * (uint32_t)kKvRowBytes : R * kWinBytes);
         // operand row R is 128-byte aligned: chunk ch sits at opx ^ (ch << 4)
         opx = (stage + kSlotBytes + R * 128u) ^ ((R & 7u) << 4);
         wstage = stage + qd * 32u * kWinBytes;  // this warp's 32 windows
@@ -567,7 +569,7 @@ struct TileGather {
                 atomicOr(status, 0x1u);
             }
         }
-        if (page_mode) {
+        if constexpr (PAGE) {
             // A run of consecutive valid rows moves as one bulk copy of whole
             // 4-row groups: its start is rounded down, and its length up, to
             // group boundaries. A group's 4 tokens are t = 4u .. 4u + 3 (the
@@ -643,7 +645,7 @@ struct TileGather {
     __device__ bool wait_rows(const int *abort_flag)
     {
         bool ok = true;
-        if (page_mode) {
+        if constexpr (PAGE) {
             ok = mbar_wait(run_bar, run_phase, abort_flag);
             run_phase ^= 1u;
         } else {
@@ -659,7 +661,7 @@ struct TileGather {
     __device__ float repack(uint32_t meta) const
     {
         float sc;
-        if (page_mode) {
+        if constexpr (PAGE) {
             // rows 132 bytes apart: word k of the 32 lanes' rows sits in bank
             // (R + k) mod 32, so 4-byte loads are conflict-free
 #pragma unroll
@@ -796,7 +798,7 @@ __device__ __forceinline__ TokenOut token_out(const MainArgs &a, const TilePos<S
 // Warpgroup g, warp quadrant qd (warp % 4): CTA tiles g, g + 4, g + 8, ...,
 // each carried through every step by this warpgroup alone. Shared memory is
 // addressed through 32-bit shared addresses throughout.
-template <int H, bool SLICED>
+template <int H, bool SLICED, bool PAGE>
 static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int g, int qd)
 {
     const Bars B(a, smem);
@@ -809,7 +811,7 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     const int N = a.N, nn = a.nn, QS = a.QS;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t stage = sbase + a.off_grp + (uint32_t)g * kGroupBytes;
-    TileGather G;
+    TileGather<PAGE> G;
     G.init(a, stage, (uint32_t)qd, (uint32_t)lane, &B.run[warp]);
     const uint32_t w_base = sbase + a.off_w;
     const uint32_t w_slot_bytes = (uint32_t)N * 4u;
