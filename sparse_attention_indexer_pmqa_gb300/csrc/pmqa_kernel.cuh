@@ -11,7 +11,9 @@ namespace pmqa {
 
 static_assert(kMaxThreads <= 32 * 32, "CtaCtl holds per-warp sums for at most 32 warps");
 
-template <int H, bool SLICED, bool PAGE>
+// NN = next_n; POOL32: every byte offset of the pool fits in 31 bits (window
+// mode only).
+template <int H, int NN, bool SLICED, bool PAGE, bool POOL32>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     pmqa_main_kernel(const __grid_constant__ MainArgs a)
 {
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     }
 
-    group_role<H, SLICED, PAGE>(a, smem, ctl, warp >> 2, warp & 3);
+    group_role<H, NN, SLICED, PAGE, POOL32>(a, smem, ctl, warp >> 2, warp & 3);
 
     tc_fence_before_sync();
     __syncthreads();

@@ -491,8 +491,9 @@ struct Walk {
 // of a tile's rows into the warpgroup's staging slot, and the repack of this
 // thread's row R into the 128B-swizzled K-major operand tile behind the slot.
 // PAGE: rows move as page runs by bulk copy (block size a multiple of 4), else
-// as 16-byte aligned windows by cp.async.
-template <bool PAGE>
+// as 16-byte aligned windows by cp.async, with 32-bit byte offsets when POOL32
+// (a pool under 2 GB).
+template <bool PAGE, bool POOL32>
 struct TileGather {
     const uint8_t *kv;
     const int32_t *bt;
@@ -500,7 +501,7 @@ struct TileGather {
     uint32_t *status;
     uint64_t pol;
     int P, W, p_shift;
-    bool p_pow2, pool32;
+    bool p_pow2;
     uint32_t R, lane, last9;
     uint32_t stage, win, opx, wstage;
     uint64_t *run_bar;
@@ -516,7 +517,6 @@ struct TileGather {
         bt = a.bt;
         num_blocks = a.num_blocks;
         pool_bytes = a.pool_bytes;
-        pool32 = pool_bytes < (1ll << 31) - 1024;  // every byte offset fits in 31 bits
         P = a.P;
         W = a.W;
         p_pow2 = (P & (P - 1)) == 0;
@@ -612,7 +612,7 @@ struct TileGather {
         const long long w0 = o & ~15ll;
         const uint32_t last = v ? (uint32_t)min(16ll, pool_bytes - (w0 + 128)) : 0u;
         const uint32_t ml = (v ? 0x100u : 0u) | last;
-        if (pool32) {
+        if constexpr (POOL32) {
             const int wrel = (int)w0 - (int)kWinBytes * (int)lane;
 #pragma unroll
             for (int qq = 0; qq < 9; ++qq) {
@@ -798,7 +798,7 @@ __device__ __forceinline__ TokenOut token_out(const MainArgs &a, const TilePos<S
 // Warpgroup g, warp quadrant qd (warp % 4): CTA tiles g, g + 4, g + 8, ...,
 // each carried through every step by this warpgroup alone. Shared memory is
 // addressed through 32-bit shared addresses throughout.
-template <int H, bool SLICED, bool PAGE>
+template <int H, int NN, bool SLICED, bool PAGE, bool POOL32>
 static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, int g, int qd)
 {
     const Bars B(a, smem);
@@ -808,10 +808,10 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     const uint32_t wg_bar = 1u + (uint32_t)g;
     const int count = (int)c.count;
     const uint32_t tmem_base = c.tmem_base;
-    const int N = a.N, nn = a.nn, QS = a.QS;
+    const int N = a.N, QS = a.QS;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t stage = sbase + a.off_grp + (uint32_t)g * kGroupBytes;
-    TileGather<PAGE> G;
+    TileGather<PAGE, POOL32> G;
     G.init(a, stage, (uint32_t)qd, (uint32_t)lane, &B.run[warp]);
     const uint32_t w_base = sbase + a.off_w;
     const uint32_t w_slot_bytes = (uint32_t)N * 4u;
@@ -823,7 +823,7 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     const uint64_t bdesc0 = sw128_kmajor_desc(sbase + a.off_q);
     const uint32_t q_units = (uint32_t)N * kHeadDim >> 4;
     constexpr int kRpp = kPassCols / H < kMaxRows ? kPassCols / H : kMaxRows;  // rows per pass
-    const int npass = (nn + kRpp - 1) / kRpp;
+    constexpr int npass = (NN + kRpp - 1) / kRpp;
     const uint64_t keep_pol = l2_evict_last_policy();
 
     ReqCtx<SLICED> rc;
@@ -870,8 +870,9 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
         const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
         const float mag = fabsf(sc);
         const bool all_pos = __all_sync(kFullMask, flip == 0u);
+#pragma unroll
         for (int p = 0; p < npass; ++p) {
-            const int j0 = p * kRpp, nr = min(kRpp, nn - j0);
+            const int j0 = p * kRpp, nr = min(kRpp, NN - j0);
             if (elected) {
                 const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
                                                         ((uint32_t)(j0 * H * kHeadDim) >> 4));

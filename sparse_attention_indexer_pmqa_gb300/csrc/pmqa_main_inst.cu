@@ -14,27 +14,43 @@
 
 namespace pmqa {
 
-template <bool SLICED, bool PAGE>
+template <int NN, bool SLICED, bool PAGE, bool POOL32>
 static cudaError_t launch(const MainArgs &a, int grid, int threads, cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(pmqa_main_kernel<PMQA_HEADS, SLICED, PAGE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto *kern = pmqa_main_kernel<PMQA_HEADS, NN, SLICED, PAGE, POOL32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)a.smem_bytes);
     if (e != cudaSuccess)
         return e;
-    pmqa_main_kernel<PMQA_HEADS, SLICED, PAGE><<<grid, threads, a.smem_bytes, stream>>>(a);
+    kern<<<grid, threads, a.smem_bytes, stream>>>(a);
     return cudaGetLastError();
+}
+
+// The gather's row-copy mode (page runs; windows with 32- or 64-bit offsets)
+// and the slice variant.
+template <int NN>
+static cudaError_t launch_nn(const MainArgs &a, int grid, int threads, cudaStream_t stream)
+{
+    const bool sliced = a.tok_begin != nullptr;
+    if (a.page_mode)
+        return sliced ? launch<NN, true, true, false>(a, grid, threads, stream)
+                      : launch<NN, false, true, false>(a, grid, threads, stream);
+    if (a.pool_bytes < (1ll << 31) - 1024)  // every byte offset fits in 31 bits
+        return sliced ? launch<NN, true, false, true>(a, grid, threads, stream)
+                      : launch<NN, false, false, true>(a, grid, threads, stream);
+    return sliced ? launch<NN, true, false, false>(a, grid, threads, stream)
+                  : launch<NN, false, false, false>(a, grid, threads, stream);
 }
 
 cudaError_t PMQA_CAT(launch_main_h, PMQA_HEADS)(const MainArgs &a, int grid, int threads,
                                                 cudaStream_t stream)
 {
-    // the gather's two row-copy modes and the slice variant compile apart
-    if (a.page_mode)
-        return a.tok_begin ? launch<true, true>(a, grid, threads, stream)
-                           : launch<false, true>(a, grid, threads, stream);
-    return a.tok_begin ? launch<true, false>(a, grid, threads, stream)
-                       : launch<false, false>(a, grid, threads, stream);
+    switch (a.nn) {
+    case 1: return launch_nn<1>(a, grid, threads, stream);
+    case 2: return launch_nn<2>(a, grid, threads, stream);
+    case 3: return launch_nn<3>(a, grid, threads, stream);
+    default: return launch_nn<4>(a, grid, threads, stream);
+    }
 }
 
 }  // namespace pmqa
