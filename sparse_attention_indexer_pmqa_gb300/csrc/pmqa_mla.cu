@@ -132,6 +132,7 @@ struct Args {
     float c_log2;         // sm_scale * q_scale * kv_scale * log2(e)
     float kv_scale;
     int next_n, topk, T, P, W;
+    int p_shift;          // log2(P) when P is a power of two, else -1
     long long num_blocks;
     long long N;          // R * T tiles
     int G;                // CTAs
@@ -154,6 +155,33 @@ __device__ __forceinline__ int cta_of(const Args &a, long long x)
 {
     return (int)(((x + 1) * (long long)a.G - 1) / a.N);
 }
+
+// Row r, tile j of the row and request i = r / next_n of the flattened tile x,
+// moved on one tile at a time without a division.
+struct TileCursor {
+    long long r;
+    int j;
+    long long i;
+    int jn;
+    __device__ void init(const Args &a, long long x)
+    {
+        r = x / a.T;
+        j = (int)(x - r * a.T);
+        i = r / a.next_n;
+        jn = (int)(r - i * a.next_n);
+    }
+    __device__ void next(const Args &a)
+    {
+        if (++j == a.T) {
+            j = 0;
+            ++r;
+            if (++jn == a.next_n) {
+                jn = 0;
+                ++i;
+            }
+        }
+    }
+};
 
 // Reduce 16 per-lane values over the warp; lane returns the result for head
 // (lane >> 1) & 15 (halves exchanged by lane bits 4, 3, 2, 1, then bit 0).
@@ -275,26 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
         // entry of tile it + 2 load while tile it is issued.
         const int pw = warp, tok = tid;
         const long long wp = (long long)a.W * a.P;
-        auto load_pos = [&](long long x) -> int {
+        auto load_pos = [&](long long x, const TileCursor &c) -> int {
             if (x >= x1)
                 return -1;
-            const long long r = x / a.T;
-            const int e = (int)(x - r * a.T) * kTile + tok;
-            return e < a.topk ? __ldg(a.idx + r * a.topk + e) : -1;
+            const int e = c.j * kTile + tok;
+            return e < a.topk ? __ldg(a.idx + c.r * a.topk + e) : -1;
         };
-        auto load_page = [&](long long x, int pos) -> int {
+        auto page_of = [&](int pos) -> int { return a.p_shift >= 0 ? pos >> a.p_shift : pos / a.P; };
+        auto load_page = [&](long long x, const TileCursor &c, int pos) -> int {
             if (x >= x1 || pos < 0 || (long long)pos >= wp)
                 return -1;
-            return __ldg(a.bt + (x / a.T) / a.next_n * a.W + pos / a.P);
+            return __ldg(a.bt + c.i * a.W + page_of(pos));
         };
         // pool row of a looked-up position, -1 for none (bad entries recorded)
-        auto row_of = [&](int pos, int page, long long x) -> long long {
+        auto row_of = [&](int pos, int page, const TileCursor &c) -> long long {
             if (pos < 0)
                 return -1;
             if (a.tok_begin) {
                 // a slice of the request's tokens: other positions are not this call's
-                const long long i = (x / a.T) / a.next_n;
-                if (pos < __ldg(a.tok_begin + i) || pos >= __ldg(a.tok_end + i))
+                if (pos < __ldg(a.tok_begin + c.i) || pos >= __ldg(a.tok_end + c.i))
                     return -1;
             }
             if ((long long)pos >= wp) {
@@ -305,23 +332,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 atomicOr(a.status, (uint32_t)PMQA_DEV_BAD_BLOCK_ID);
                 return -1;
             }
-            return (long long)page * a.P + pos % a.P;
+            return (long long)page * a.P + (pos - page_of(pos) * a.P);
         };
-        int pos0 = load_pos(x0), pos1 = load_pos(x0 + 1), pos2 = load_pos(x0 + 2);
-        int page0 = load_page(x0, pos0), page1 = load_page(x0 + 1, pos1);
+        // cursors at tiles x, x + 1, x + 2 and x + 3
+        TileCursor c0, c1, c2, c3;
+        c0.init(a, x0);
+        c1 = c0;
+        c1.next(a);
+        c2 = c1;
+        c2.next(a);
+        c3 = c2;
+        c3.next(a);
+        int pos0 = load_pos(x0, c0), pos1 = load_pos(x0 + 1, c1), pos2 = load_pos(x0 + 2, c2);
+        int page0 = load_page(x0, c0, pos0), page1 = load_page(x0 + 1, c1, pos1);
         int seg = -1, vs = 0;
         uint32_t vph = 0;
         for (long long x = x0; x < x1; ++x) {
             const int it = (int)(x - x0), rs = it & 1;
             const uint32_t rph = (uint32_t)(it >> 1) & 1u;
-            const long long r = x / a.T;
-            const int j = (int)(x - r * a.T);
-            const bool first = x == x0 || j == 0;
+            const long long r = c0.r;
+            const bool first = x == x0 || c0.j == 0;
             if (first)
                 ++seg;
-            const int pos3 = load_pos(x + 3);
-            const int page2 = load_page(x + 2, pos2);
-            const long long srow = row_of(pos0, page0, x);
+            const int pos3 = load_pos(x + 3, c3);
+            const int page2 = load_page(x + 2, c2, pos2);
+            const long long srow = row_of(pos0, page0, c0);
             pos0 = pos1;
             page0 = page1;
             pos1 = pos2;
@@ -379,6 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 vs = 0;
                 vph ^= 1u;
             }
+            c0 = c1;
+            c1 = c2;
+            c2 = c3;
+            c3.next(a);
         }
         cp_async_wait_all();
     } else if (warp >= 4 && warp < 8) {
@@ -392,15 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
         int seg = -1, vs = -1;
         uint32_t vph = 1;
         bool ok = true;
-        for (long long x = x0; x < x1; ++x) {
+        TileCursor cx;
+        cx.init(a, x0);
+        for (long long x = x0; x < x1; ++x, cx.next(a)) {
             const int it = (int)(x - x0), stage = it & 1;
             const uint32_t kph = (uint32_t)(it >> 1) & 1u;
             if (++vs == kVStages || it == 0) {
                 vs = 0;
                 vph ^= 1u;
             }
-            const long long r = x / a.T;
-            const int j = (int)(x - r * a.T);
+            const long long r = cx.r;
+            const int j = cx.j;
             const bool first = x == x0 || j == 0;
             const bool last = x == x1 - 1 || j == a.T - 1;
             if (first) {
@@ -597,6 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
         // early as possible.
         const int n = (int)(x1 - x0);
         int nq = 0, np = 0, seg = -1, idle = 0;
+        TileCursor cq, cp;  // tiles x0 + nq and x0 + np
+        cq.init(a, x0);
+        cp = cq;
         int qv = 0, pv = 0;              // value slots of tiles nq and np
         uint32_t qvph = 0;
         uint64_t idle_since = 0;
@@ -608,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 const int sb = np & 1;
                 if (mbar_test(&bar[kBarPFull + sb], (uint32_t)(np >> 1) & 1u)) {
                     const long long x = x0 + np;
-                    const bool pfirst = x == x0 || (x % a.T) == 0;
+                    const bool pfirst = x == x0 || cp.j == 0;
                     tc_fence_after_sync();
                     const uint32_t vb = sbase + kOffV + (uint32_t)pv * kVStage;
                     const uint32_t pb = sbase + kOffP + (uint32_t)sb * kPBytes;
@@ -626,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                     if (++pv == kVStages)
                         pv = 0;
                     ++np;
+                    cp.next(a);
                     prog = true;
                 }
             }
@@ -634,8 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                 const uint32_t ph = (uint32_t)(nq >> 1) & 1u;
                 if (mbar_test(&bar[kBarReady + qv], qvph) && mbar_test(&bar[kBarSFree + sb], ph ^ 1u)) {
                     const long long x = x0 + nq;
-                    const long long r = x / a.T;
-                    const int j = (int)(x - r * a.T);
+                    const int j = cq.j;
                     if (x == x0 || j == 0)
                         ++seg;
                     fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
@@ -664,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const Args a)
                         qvph ^= 1u;
                     }
                     ++nq;
+                    cq.next(a);
                     prog = true;
                 }
             }
@@ -854,6 +899,7 @@ static int sparse_mla_call(const pmqa_mla_problem *p, const int32_t *tok_begin,
     a.topk = p->topk;
     a.T = (int)T;
     a.P = p->block_size;
+    a.p_shift = (a.P & (a.P - 1)) == 0 ? __builtin_ctz((unsigned)a.P) : -1;
     a.W = p->max_blocks_per_seq;
     a.num_blocks = p->num_blocks;
     a.N = rows * T;
