@@ -247,10 +247,13 @@ static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int
     int islot = 0, prev_slot = 0;
     uint32_t iqphase = 0;
     bool prev_last = false, ok = true, have_q = false;
+    // item k's key stage s = k % S and that stage's fill parity, kept as
+    // counters (no division on the issuing thread's path)
+    int s = 0, s_prev = 0;
+    uint32_t s_phase = 0;
     for (int k = 0; k < count; ++k) {
-        const int s = k % S;
         const bool last = ip.m == ip.nt - 1 || k == count - 1;
-        ok = ok && mbar_wait(&B.kfull[s], (uint32_t)(k / S) & 1u, &c.abort);
+        ok = ok && mbar_wait(&B.kfull[s], s_phase, &c.abort);
         if (!have_q) {
             ok = ok && mbar_wait(&B.qfull[islot], iqphase, &c.abort);
             have_q = true;
@@ -281,7 +284,7 @@ static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int
             // results): its key stage takes item k - 1 + S, and if it ended a
             // super-group, that super-group's query slot takes the one QS ahead
             if (k - 1 + S < count) {
-                pf_load_k(a, kbase, B, (k - 1) % S, kp.tile());
+                pf_load_k(a, kbase, B, s_prev, kp.tile());
                 ++kloads;
                 kp.next(a);
             }
@@ -295,6 +298,11 @@ static __device__ void pf_control(const PfArgs &a, uint8_t *smem, CtaCtl &c, int
         }
         prev_last = last;
         prev_slot = islot;
+        s_prev = s;
+        if (++s == S) {
+            s = 0;
+            s_phase ^= 1u;
+        }
         if (last) {
             if (++islot == QS) {
                 islot = 0;
