@@ -807,32 +807,44 @@ GATHER_METHODS = {0: "ld16 (16-byte loads into registers)",
                   2: "bulk (one cp.async.bulk per row window)"}
 
 
-def gather_rows(name):
-    """The physical rows a kernel reads, in its order: every token of every
-    request for the KV pass (C*), every listed position of every query row for
-    the sparse MLA decode (M*). Returns (pool array, int32 rows, row pitch)."""
+def kv_rows(p):
+    """Pool rows the KV pass reads for an indexer problem, in its order: every
+    token t < ctx_i of request i through the block table (int32)."""
     import numpy as np
 
-    if name.startswith("M"):
-        from synth import mla_config
-
-        p = mla_config(name)
-        req = np.arange(p.rows) // p.next_n
-        pos = p.indices.astype(np.int64)
-        ok = pos >= 0
-        page = p.block_tables[np.repeat(req, p.topk).reshape(p.rows, p.topk),
-                              np.where(ok, pos // p.block_size, 0)]
-        rows = (page.astype(np.int64) * p.block_size + pos % p.block_size)[ok]
-        return p.kv, rows.astype(np.int32), 576
-    from synth import config_problem
-
-    p = config_problem(name)
     P = p.block_size
     parts = []
     for i, c in enumerate(p.context_lens):
         t = np.arange(int(c), dtype=np.int64)
         parts.append(p.block_tables[i, t // P].astype(np.int64) * P + t % P)
-    return p.kv, np.concatenate(parts).astype(np.int32), 132
+    return np.concatenate(parts).astype(np.int32)
+
+
+def mla_rows(p):
+    """Pool rows the sparse MLA decode reads for an MLA problem, in its order:
+    every listed position (holes skipped) of every query row (int32)."""
+    import numpy as np
+
+    req = np.arange(p.rows) // p.next_n
+    pos = p.indices.astype(np.int64)
+    ok = pos >= 0
+    page = p.block_tables[np.repeat(req, p.topk).reshape(p.rows, p.topk),
+                          np.where(ok, pos // p.block_size, 0)]
+    return (page.astype(np.int64) * p.block_size + pos % p.block_size)[ok].astype(np.int32)
+
+
+def gather_rows(name):
+    """(pool array, int32 rows, row pitch) of a workload: the KV pass's rows
+    for C*, the sparse MLA decode's for M*."""
+    if name.startswith("M"):
+        from synth import mla_config
+
+        p = mla_config(name)
+        return p.kv, mla_rows(p), 576
+    from synth import config_problem
+
+    p = config_problem(name)
+    return p.kv, kv_rows(p), 132
 
 
 def run_gather_ceiling(args):

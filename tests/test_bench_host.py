@@ -118,3 +118,21 @@ def test_cpu_description_and_cpu_ranges():
     assert d["cpu_model"] and d["logical_cpus"] >= 1 and d["affinity"]
     assert bench._ranges([0, 1, 2, 5, 7, 8]) == "0-2,5,7-8"
     assert bench._ranges([3]) == "3"
+
+
+def test_gather_probe_row_lists():
+    """The rows `bench.py --gather-ceiling` hands the probe are the rows the
+    kernels read: every token through the block table (pages of 4, a partial
+    last page), and every listed position of every query row (holes
+    skipped)."""
+    from synth.mla import make_mla_problem
+
+    prob = make_problem(2, 1, 16, 4, [10, 3], 16, seed=2, table="perm")
+    rows = bench.kv_rows(prob)
+    want = [prob.block_tables[i, t // 4] * 4 + t % 4 for i, c in enumerate([10, 3])
+            for t in range(c)]
+    assert rows.dtype == np.int32 and rows.tolist() == want
+    mp_ = make_mla_problem(2, 2, 16, 1, [300, 40], topk=64, seed=3, holes=0.2)
+    rows = bench.mla_rows(mp_)
+    want = [mp_.block_tables[r // 2, pos] for r in range(4) for pos in mp_.indices[r] if pos >= 0]
+    assert rows.tolist() == want
