@@ -112,6 +112,29 @@ def test_block_sizes_and_draft_rows(cuda_lib, case):
         check_logits(logits.cpu().numpy(), ref, tol)
 
 
+# A pool past 2 GB: byte offsets of rows no longer fit in 31 bits, which
+# selects the gather with 64-bit offsets (windows) and exercises the page runs'
+# 64-bit addressing. The small problem's blocks are moved past 2 GB + 1 MB of
+# zero blocks; the oracle runs on the small problem (the same logical cache).
+@pytest.mark.parametrize("P,nn", [(1, 2), (3, 1), (64, 4)])
+def test_pool_past_2_gb(cuda_lib, P, nn):
+    import dataclasses
+
+    prob = make_problem(2, nn, 64, P, [700, 300], 1024, seed=11 + P, table="perm",
+                        extra_blocks=3)
+    ref, r64, tol = oracle_all(prob)
+    shift = -(-(2**31 + 2**20) // (P * 132))
+    kv = np.zeros((shift + prob.num_blocks, P, 132), dtype=np.uint8)
+    kv[shift:] = prob.kv
+    bt = np.where(prob.block_tables >= 0, prob.block_tables + shift, -1).astype(np.int32)
+    big = dataclasses.replace(prob, kv=kv, block_tables=bt)
+    assert big.num_blocks * P * 132 > 2**31
+    d = dev(big)
+    check_logits(gpu_logits(cuda_lib, big, d=d), ref, tol)
+    idx, vals = gpu_fused(cuda_lib, big, 2048, d=d)
+    check_topk_rows(idx, r64, tol, prob.context_lens, nn, 2048, vals=vals)
+
+
 # The scale's sign: relu(s * x) = |s| * relu(-x) for s < 0, which the kernel
 # applies per token by flipping the sign of the row's signed sum. Mixed signs
 # put both kinds of token in every warp; an all-negative range makes every
