@@ -43,6 +43,8 @@ def check(out, lse, prob, rows=None):
     (2, 4, 1, [5000, 2049], 2048, dict(repeats=0.05)),        # repeated positions
     (3, 2, 64, [7000, 129, 4097], 1000, {}),                  # pages of 64, topk % 128 != 0
     (4, 1, 1, [0, 3, 1, 2500], 256, {}),                      # empty and tiny rows
+    (2, 2, 48, [5000, 777], 1024, {}),                        # pages of 48: position / P divides
+    (1, 3, 3, [2000], 512, dict(holes=0.05)),                 # pages of 3
 ])
 def test_parity_small(cuda_lib, bs, nn, P, ctx, topk, kw):
     prob = make_mla_problem(bs, nn, 16, P, ctx, topk=topk, seed=sum(ctx) + topk, **kw)
