@@ -35,7 +35,7 @@ constexpr int kVersion = 300;  // 0.3.0
 constexpr uint32_t kMaxDynSmem = 232448 - ((uint32_t)sizeof(CtaCtl) + 127u) / 128u * 128u;
 constexpr uint32_t kMinMainSmem = 120 * 1024;  // > half an SM: one CTA per SM
 constexpr size_t kWsAlign = 256;
-constexpr int kSelChunk = kSelThreads * kSelPer;  // positions per selection CTA (4096)
+constexpr int kSelChunk = kSelThreads * kSelPer;  // positions per selection CTA (8192)
 // Tuning constants of the main kernel (compile time; -D overrides in tuning builds).
 #ifndef PMQA_L2_POLICY
 #define PMQA_L2_POLICY 0

@@ -42,8 +42,8 @@ struct SelectArgs {
     int chunk;   // positions per CTA
 };
 
-constexpr int kSelThreads = 256;
-constexpr int kSelPer = 16;  // positions per thread: one CTA covers 256 * 16 = 4096
+constexpr int kSelThreads = 512;
+constexpr int kSelPer = 16;  // positions per thread: one CTA covers 512 * 16 = 8192
 
 // Positions [lo, hi) that row `row` selects from: the admitted positions
 // t < valid_len, inside its request's slice [tok_begin, tok_end) when one is
@@ -188,7 +188,7 @@ __device__ __forceinline__ float f32_from_order_key(uint32_t key)
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// One CTA = up to 4096 positions of one row. The CTA holds its positions'
+// One CTA = up to 8192 positions of one row. The CTA holds its positions'
 // logits in registers (all loads in flight at once), counts the sure winners
 // (key bin above b*) and the candidates (bin b*), takes its output ranges
 // with one atomic each and writes them. The last CTA of the row resolves the
@@ -777,7 +777,7 @@ struct MergeArgs {
 // One CTA per row: a histogram of the valid candidates' top 11 key bits, the
 // boundary bin, one pass that writes the winners and sets the boundary bin's
 // candidates aside, and those resolved with two more digits.
-__global__ void __launch_bounds__(kSelThreads) pmqa_merge_kernel(const __grid_constant__ MergeArgs a)
+__global__ void __launch_bounds__(kSelThreads, 1) pmqa_merge_kernel(const __grid_constant__ MergeArgs a)
 {
     __shared__ SelShared s;
     const int row = blockIdx.x, tid = threadIdx.x;
