@@ -115,6 +115,11 @@ bool main_layout(int heads, int nn, MainArgs &a)
         cols <<= 1;
     a.cols = cols;
     a.tmem_cols = kGroups * cols;
+    if (N > kPassCols && N <= 2 * kPassCols) {
+        // two 256-column halves, each shared by two warpgroups in turn
+        a.cols = 2 * kPassCols;
+        a.tmem_cols = 4 * kPassCols;
+    }
     for (int QS = 2; QS >= 1; --QS) {
         uint32_t off = 0;
         a.off_grp = off;

@@ -311,15 +311,18 @@ struct ReqWalk {
 //   mma[4]        a warpgroup's MMA pass finished (one tcgen05.commit)
 //   run[16]       a warp's page runs of its warpgroup's staging slot landed
 struct Bars {
-    uint64_t *qfull, *mma, *run;
+    uint64_t *qfull, *mma, *run, *tfree;
     __device__ Bars(const MainArgs &a, uint8_t *smem)
     {
         qfull = reinterpret_cast<uint64_t *>(smem + a.off_bar);
         mma = qfull + a.QS;
         run = mma + kGroups;
+        tfree = run + kNumWarps;
     }
 };
-constexpr int kNumBars = kGroups + kNumWarps;  // plus QS
+// tfree[h]: TMEM half h released by the warpgroup that used it last (when two
+// warpgroups share each 256-column half)
+constexpr int kNumBars = kGroups + kNumWarps + 2;  // plus QS
 
 __device__ __forceinline__ void raise_abort(const MainArgs &a, CtaCtl &c)
 {
@@ -816,13 +819,18 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     const uint32_t w_base = sbase + a.off_w;
     const uint32_t w_slot_bytes = (uint32_t)N * 4u;
     // TMEM: this warp's lane quadrant, the group's columns
-    const uint32_t dcol = tmem_base + (uint32_t)(g * a.cols);
+    // next_n * H in (128, 256]: one MMA pass of N = next_n * H per tile into a
+    // 256-column TMEM half that warpgroups g and g ^ 2 use in turn (tile order
+    // alternates between them); else passes of at most 128 columns in the
+    // warpgroup's own columns
+    constexpr bool kShare = NN * H > kPassCols && NN * H <= 2 * kPassCols;
+    const uint32_t dcol = tmem_base + (uint32_t)(kShare ? (g & 1) * 2 * kPassCols : g * a.cols);
     const uint32_t tacc = dcol + ((uint32_t)(qd * 32) << 16);
     // MMA operands; passes of at most 128 accumulator columns (whole draft rows)
     const uint64_t adesc = sw128_kmajor_desc(stage + kSlotBytes);
     const uint64_t bdesc0 = sw128_kmajor_desc(sbase + a.off_q);
     const uint32_t q_units = (uint32_t)N * kHeadDim >> 4;
-    constexpr int kRpp = kPassCols / H < kMaxRows ? kPassCols / H : kMaxRows;  // rows per pass
+    constexpr int kRpp = kShare ? NN : (kPassCols / H < kMaxRows ? kPassCols / H : kMaxRows);  // rows per pass
     constexpr int npass = (NN + kRpp - 1) / kRpp;
     const uint64_t keep_pol = l2_evict_last_policy();
 
@@ -843,6 +851,7 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     nx.step(rc, kGroups, count);
     int32_t b_nx = nx.kk < count ? G.table_entry(nx.cur) : -1;
     uint32_t mma_phase = 0;
+    uint32_t use = (uint32_t)(g >> 1);  // kShare: this tile's use of the half, counting both users
 
     while (w.kk < count) {
         // 1. the tile's rows have landed; 2. repack row R, scale -> register
@@ -873,20 +882,25 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
 #pragma unroll
         for (int p = 0; p < npass; ++p) {
             const int j0 = p * kRpp, nr = min(kRpp, NN - j0);
-            if (elected) {
-                const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
-                                                        ((uint32_t)(j0 * H * kHeadDim) >> 4));
-                const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
-#pragma unroll
-                for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
-                    umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
-                umma_commit(&B.mma[g]);
-            }
-            // the elected thread waits for the MMAs; the rest of the group
-            // sleeps on the named barrier meanwhile
             bool mma_ok = true;
-            if (elected)
-                mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
+            if (elected) {
+                // a shared half: the other warpgroup's previous tile has read it
+                if (kShare && use > 0)
+                    mma_ok = mbar_wait(&B.tfree[g & 1], (use - 1u) & 1u, &c.abort);
+                if (mma_ok) {
+                    tc_fence_after_sync();
+                    const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
+                                                            ((uint32_t)(j0 * H * kHeadDim) >> 4));
+                    const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
+#pragma unroll
+                    for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
+                        umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
+                    umma_commit(&B.mma[g]);
+                    // the elected thread waits for the MMAs; the rest of the
+                    // group sleeps on the named barrier meanwhile
+                    mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
+                }
+            }
             mma_phase ^= 1u;
             ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
             tc_fence_after_sync();
@@ -902,6 +916,16 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
                 named_bar_sync(wg_bar, 128);
                 tc_fence_after_sync();
             }
+        }
+        if constexpr (kShare) {
+            // every TMEM read of the tile is done: the half goes to the other
+            // warpgroup (an arrival even after a failed wait keeps the phases
+            // in step)
+            tc_fence_before_sync();
+            named_bar_sync(wg_bar, 128);
+            if (elected)
+                mbar_arrive(&B.tfree[g & 1]);
+            use += 2u;
         }
         qs.pass_ends(a, smem, B, rc, c, count, w.step(rc, kGroups, count));
     }
