@@ -137,7 +137,8 @@ def read_peak():
 KERNEL_SOURCES = {
     "indexer": ("pmqa_ptx.cuh", "pmqa_main.cuh", "pmqa_kernel.cuh", "pmqa_main_inst.cu",
                 "pmqa_select.cuh", "pmqa_api.cu"),
-    "prefill": ("pmqa_ptx.cuh", "pmqa_prefill.cuh", "pmqa_prefill_inst.cu", "pmqa_api.cu"),
+    "prefill": ("pmqa_ptx.cuh", "pmqa_main.cuh", "pmqa_prefill.cuh", "pmqa_prefill_inst.cu",
+                "pmqa_api.cu"),
     "mla": ("pmqa_ptx.cuh", "pmqa_mla_ptx.cuh", "pmqa_mla.cu"),
 }
 

@@ -409,11 +409,12 @@ __device__ __forceinline__ float acc_sum(float (&acc)[8], uint32_t flip)
 // [(j - j0) * H, (j - j0) * H + H) from taddr, weights w[j][h] at shared
 // address wsl + 4 * ((j - j0) * H + h). The NR * H / 16 chunks of 16 columns
 // alternate between two register buffers, the next chunk loading while the
-// current one is reduced. Calls out(j, score) per row once every TMEM read of
-// the pass has completed.
-template <int H, int NR, bool SIGNED, class Out>
+// current one is reduced. Once every TMEM read of the pass has completed it
+// calls done() (the columns may be reused from then on), then out(j, score)
+// per row.
+template <int H, int NR, bool SIGNED, class Out, class Done>
 __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t flip, float mag,
-                                         int j0, Out &&out)
+                                         int j0, Out &&out, Done &&done)
 {
     constexpr int NC = 16;
     constexpr int CPR = H / NC;  // chunks per draft row
@@ -439,6 +440,7 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t 
             reg_fence_cols<NC>(b[(ch + 1) & 1]);
         }
     }
+    done();
 #pragma unroll
     for (int u = 0; u < NR; ++u)
         out(j0 + u, res[u]);
@@ -447,17 +449,17 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t 
 
 // epi_rows for nr (1 .. RPP) rows, the scale's sign known warp-wide (all_pos)
 // or per thread.
-template <int H, int RPP, class Out>
+template <int H, int RPP, class Out, class Done>
 __device__ __forceinline__ void epi_dispatch(int nr, bool all_pos, uint32_t taddr, uint32_t wsl,
-                                             uint32_t flip, float mag, int j0, Out &out)
+                                             uint32_t flip, float mag, int j0, Out &out, Done &done)
 {
     if (nr == RPP) {
         if (all_pos)
-            epi_rows<H, RPP, false>(taddr, wsl, flip, mag, j0, out);
+            epi_rows<H, RPP, false>(taddr, wsl, flip, mag, j0, out, done);
         else
-            epi_rows<H, RPP, true>(taddr, wsl, flip, mag, j0, out);
+            epi_rows<H, RPP, true>(taddr, wsl, flip, mag, j0, out, done);
     } else if constexpr (RPP > 1) {
-        epi_dispatch<H, RPP - 1>(nr, all_pos, taddr, wsl, flip, mag, j0, out);
+        epi_dispatch<H, RPP - 1>(nr, all_pos, taddr, wsl, flip, mag, j0, out, done);
     }
 }
 
@@ -904,11 +906,23 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             mma_phase ^= 1u;
             ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
             tc_fence_after_sync();
+            // a shared half goes to the other warpgroup as soon as all four
+            // warps have read their lanes, before the tile's outputs (an
+            // arrival even after a failed wait keeps the phases in step)
+            auto release = [&]() {
+                if constexpr (kShare) {
+                    tc_fence_before_sync();
+                    named_bar_sync(wg_bar, 128);
+                    if (elected)
+                        mbar_arrive(&B.tfree[g & 1]);
+                }
+            };
             // one outcome per warp: the tile body uses warp-wide votes
             if (__all_sync(kFullMask, ok)) {
                 const uint32_t wj0 = wsl + (uint32_t)(j0 * H * 4);
-                epi_dispatch<H, kRpp>(nr, all_pos, tacc, wj0, flip, mag, j0, out);
+                epi_dispatch<H, kRpp>(nr, all_pos, tacc, wj0, flip, mag, j0, out, release);
             } else {
+                release();
                 raise_abort(a, c);
             }
             if (p + 1 < npass) {  // the next pass reuses the columns
@@ -917,16 +931,8 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
                 tc_fence_after_sync();
             }
         }
-        if constexpr (kShare) {
-            // every TMEM read of the tile is done: the half goes to the other
-            // warpgroup (an arrival even after a failed wait keeps the phases
-            // in step)
-            tc_fence_before_sync();
-            named_bar_sync(wg_bar, 128);
-            if (elected)
-                mbar_arrive(&B.tfree[g & 1]);
+        if constexpr (kShare)
             use += 2u;
-        }
         qs.pass_ends(a, smem, B, rc, c, count, w.step(rc, kGroups, count));
     }
     cp_async_wait_all();

@@ -376,8 +376,9 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
                 if (t < n)
                     orow[(long long)j * n] = (t >= rks[j] && t < rke[j]) ? v : NEG_INF;
             };
+            auto done = []() {};
             if (nr > 0)
-                epi_dispatch<H, G>(nr, all_pos, tacc, wsl, flip, mag, 0, out);
+                epi_dispatch<H, G>(nr, all_pos, tacc, wsl, flip, mag, 0, out, done);
         } else if (lane == 0 && !aborted(c)) {
             c.abort = 1;
             atomicOr(a.status, 0x4u);
