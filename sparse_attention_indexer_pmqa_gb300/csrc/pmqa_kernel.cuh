@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         for (int w = 0; w < kNumWarps; ++w)
             mbar_init(&B.run[w], 1);
         for (int h = 0; h < 2; ++h)
-            mbar_init(&B.tfree[h], 1);
+            mbar_init(&B.tfree[h], 4);  // one arrival per warp of the user
         mbar_init_fence();
     }
     __syncwarp();

@@ -320,7 +320,7 @@ struct Bars {
         tfree = run + kNumWarps;
     }
 };
-// tfree[h]: TMEM half h released by the warpgroup that used it last (when two
+// tfree[h]: TMEM half h released by the warpgroup that used it last, one arrival per warp (when two
 // warpgroups share each 256-column half)
 constexpr int kNumBars = kGroups + kNumWarps + 2;  // plus QS
 
@@ -409,9 +409,9 @@ __device__ __forceinline__ float acc_sum(float (&acc)[8], uint32_t flip)
 // [(j - j0) * H, (j - j0) * H + H) from taddr, weights w[j][h] at shared
 // address wsl + 4 * ((j - j0) * H + h). The NR * H / 16 chunks of 16 columns
 // alternate between two register buffers, the next chunk loading while the
-// current one is reduced. Once every TMEM read of the pass has completed it
-// calls done() (the columns may be reused from then on), then out(j, score)
-// per row.
+// current one is reduced. Once every TMEM read of the pass has completed (the
+// last chunk is in registers) it calls done(): the columns may be reused from
+// then on. Then out(j, score) per row.
 template <int H, int NR, bool SIGNED, class Out, class Done>
 __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t flip, float mag,
                                          int j0, Out &&out, Done &&done)
@@ -425,6 +425,8 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t 
     tmem_ld_cols<NC>(taddr, b[0]);
     tmem_ld_wait();
     reg_fence_cols<NC>(b[0]);
+    if (TOTAL == 1)
+        done();
 #pragma unroll
     for (int ch = 0; ch < TOTAL; ++ch) {
         if (ch + 1 < TOTAL)
@@ -438,9 +440,10 @@ __device__ __forceinline__ void epi_rows(uint32_t taddr, uint32_t wsl, uint32_t 
         if (ch + 1 < TOTAL) {
             tmem_ld_wait();
             reg_fence_cols<NC>(b[(ch + 1) & 1]);
+            if (ch + 2 == TOTAL)
+                done();  // the last chunk is in registers
         }
     }
-    done();
 #pragma unroll
     for (int u = 0; u < NR; ++u)
         out(j0 + u, res[u]);
@@ -906,14 +909,15 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
             mma_phase ^= 1u;
             ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
             tc_fence_after_sync();
-            // a shared half goes to the other warpgroup as soon as all four
-            // warps have read their lanes, before the tile's outputs (an
-            // arrival even after a failed wait keeps the phases in step)
+            // a shared half goes to the other warpgroup once each of the four
+            // warps has read its lanes (one arrival per warp, no warpgroup
+            // barrier), before the tile's outputs; an arrival even after a
+            // failed wait keeps the phases in step
             auto release = [&]() {
                 if constexpr (kShare) {
                     tc_fence_before_sync();
-                    named_bar_sync(wg_bar, 128);
-                    if (elected)
+                    __syncwarp();
+                    if (lane == 0)
                         mbar_arrive(&B.tfree[g & 1]);
                 }
             };
