@@ -158,7 +158,8 @@ struct PfPos {
 //   kfull[S]    a key tile landed in stage s
 //   qfull[QS]   query rows + weights of a super-group landed
 //   acc[2]      pair p's MMA finished (TMEM columns [256 p, 256 p + 256): warpgroups 2 p, 2 p + 1)
-//   bufree[2]   both warpgroups of pair p have read their columns (2 arrivals)
+//   bufree[2]   both warpgroups of pair p have read their columns (8 arrivals:
+//               one per warp, as soon as its last chunk is in registers)
 struct PfBars {
     uint64_t *kfull, *qfull, *acc, *bufree;
     __device__ PfBars(const PfArgs &a, uint8_t *smem)
@@ -369,6 +370,15 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
             acc_ok = mbar_wait(&B.acc[g >> 1], (uint32_t)kk & 1u, &c.abort);
         ok = named_bar_and(wg_bar, 128, acc_ok) && ok;
         tc_fence_after_sync();
+        // this warp has read its lanes: once every warp of the pair has, the
+        // control warp may reuse the columns (one arrival per warp per item,
+        // before the outputs; also when the warp had nothing to read)
+        auto done = [&]() {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&B.bufree[g >> 1]);
+        };
         if (__all_sync(kFullMask, ok)) {
             const bool all_pos = __all_sync(kFullMask, flip == 0u);
             float *const orow = logits + (long long)r0 * n + t;
@@ -376,19 +386,17 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
                 if (t < n)
                     orow[(long long)j * n] = (t >= rks[j] && t < rke[j]) ? v : NEG_INF;
             };
-            auto done = []() {};
             if (nr > 0)
                 epi_dispatch<H, G>(nr, all_pos, tacc, wsl, flip, mag, 0, out, done);
-        } else if (lane == 0 && !aborted(c)) {
-            c.abort = 1;
-            atomicOr(a.status, 0x4u);
+            else
+                done();
+        } else {
+            done();
+            if (lane == 0 && !aborted(c)) {
+                c.abort = 1;
+                atomicOr(a.status, 0x4u);
+            }
         }
-        // this warpgroup has read its columns: once both warpgroups of the
-        // pair have, the control warp may reuse them
-        tc_fence_before_sync();
-        named_bar_sync(wg_bar, 128);
-        if (elected)
-            mbar_arrive(&B.bufree[g >> 1]);
         if (cur.m == cur.nt - 1 || kk == count - 1) {
             if (++q_slot == QS) {
                 q_slot = 0;
@@ -419,7 +427,7 @@ __global__ void __launch_bounds__(kPfBoundThreads, 1) pmqa_prefill_kernel(const 
             mbar_init(&B.qfull[q], 1);
         for (int p = 0; p < 2; ++p) {
             mbar_init(&B.acc[p], 1);
-            mbar_init(&B.bufree[p], 2);
+            mbar_init(&B.bufree[p], 8);
         }
         mbar_init_fence();
     }
