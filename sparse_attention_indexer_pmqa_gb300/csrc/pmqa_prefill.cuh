@@ -325,8 +325,6 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
     const PfBars B(a, smem);
     const int lane = threadIdx.x & 31;
     const uint32_t R = (uint32_t)(qd * 32 + lane);
-    const bool elected = qd == 0 && lane == 0;
-    const uint32_t wg_bar = 1u + (uint32_t)g;
     const int count = (int)c.count;
     const int QS = a.QS, SGR = a.SGR, m = a.m, n = a.n;
     const uint32_t w_slot_bytes = (uint32_t)(SGR * H * 4);
@@ -365,10 +363,8 @@ static __device__ void pf_reduce_role(const PfArgs &a, uint8_t *smem, CtaCtl &c,
         const uint32_t wsl = launder_u32(wbase + (uint32_t)q_slot * w_slot_bytes);
         const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
         const float mag = fabsf(sc);
-        bool acc_ok = true;
-        if (elected)
-            acc_ok = mbar_wait(&B.acc[g >> 1], (uint32_t)kk & 1u, &c.abort);
-        ok = named_bar_and(wg_bar, 128, acc_ok) && ok;
+        // every thread waits for the pair's MMA itself
+        ok = mbar_wait(&B.acc[g >> 1], (uint32_t)kk & 1u, &c.abort) && ok;
         tc_fence_after_sync();
         // this warp has read its lanes: once every warp of the pair has, the
         // control warp may reuse the columns (one arrival per warp per item,
