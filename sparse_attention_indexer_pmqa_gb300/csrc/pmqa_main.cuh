@@ -857,6 +857,25 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
     int32_t b_nx = nx.kk < count ? G.table_entry(nx.cur) : -1;
     uint32_t mma_phase = 0;
     uint32_t use = (uint32_t)(g >> 1);  // kShare: this tile's use of the half, counting both users
+    // one pass per tile: the previous tile's scores and where they go
+    struct Pending {
+        TokenOut out;
+        float v[kRpp];
+        __device__ void keep(int j, float x)
+        {
+#pragma unroll
+            for (int u = 0; u < kRpp; ++u)
+                if (j == u)
+                    v[u] = x;
+        }
+        __device__ void flush() const
+        {
+#pragma unroll
+            for (int u = 0; u < NN && u < kRpp; ++u)
+                out(u, v[u]);
+        }
+    } pend;
+    int pend_n = 0;
 
     while (w.kk < count) {
         // 1. the tile's rows have landed; 2. repack row R, scale -> register
@@ -884,9 +903,24 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
         const uint32_t flip = sc < 0.0f ? 0x80000000u : 0u;
         const float mag = fabsf(sc);
         const bool all_pos = __all_sync(kFullMask, flip == 0u);
-#pragma unroll
-        for (int p = 0; p < npass; ++p) {
-            const int j0 = p * kRpp, nr = min(kRpp, NN - j0);
+        // a shared half goes to the other warpgroup once each of the four
+        // warps has read its lanes (one arrival per warp, no warpgroup
+        // barrier), before the tile's outputs; an arrival even after a
+        // failed wait keeps the phases in step
+        auto release = [&]() {
+            if constexpr (kShare) {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&B.tfree[g & 1]);
+            }
+        };
+        if constexpr (npass == 1) {
+            // one pass in the warpgroup's own columns: the tile's outputs are
+            // written during the next tile's MMA (the scores wait in
+            // registers). With a shared half they are written at once (the
+            // half's wait leaves nothing to hide them behind, and deferring
+            // them measured slower).
             bool mma_ok = true;
             if (elected) {
                 // a shared half: the other warpgroup's previous tile has read it
@@ -894,39 +928,62 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
                     mma_ok = mbar_wait(&B.tfree[g & 1], (use - 1u) & 1u, &c.abort);
                 if (mma_ok) {
                     tc_fence_after_sync();
-                    const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
-                                                            ((uint32_t)(j0 * H * kHeadDim) >> 4));
-                    const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
+                    const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units);
+                    const uint32_t idesc = idesc_e4m3_f32(128, NN * H);
 #pragma unroll
                     for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
                         umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
                     umma_commit(&B.mma[g]);
-                    // the elected thread waits for the MMAs; the rest of the
-                    // group sleeps on the named barrier meanwhile
-                    mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
                 }
+            }
+            if (pend_n) {
+                pend.flush();
+                pend_n = 0;
+            }
+            // the elected thread waits for the MMAs; the rest of the group
+            // sleeps on the named barrier meanwhile
+            if (elected && mma_ok)
+                mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
+            mma_phase ^= 1u;
+            ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
+            tc_fence_after_sync();
+            // one outcome per warp: the tile body uses warp-wide votes
+            if (__all_sync(kFullMask, ok)) {
+                if constexpr (kShare) {
+                    epi_dispatch<H, kRpp>(NN, all_pos, tacc, wsl, flip, mag, 0, out, release);
+                } else {
+                    pend.out = out;
+                    auto keep = [&](int j, float v) { pend.keep(j, v); };
+                    epi_dispatch<H, kRpp>(NN, all_pos, tacc, wsl, flip, mag, 0, keep, release);
+                    pend_n = NN;
+                }
+            } else {
+                release();
+                raise_abort(a, c);
+            }
+        } else {
+#pragma unroll
+        for (int p = 0; p < npass; ++p) {
+            const int j0 = p * kRpp, nr = min(kRpp, NN - j0);
+            bool mma_ok = true;
+            if (elected) {
+                tc_fence_after_sync();
+                const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
+                                                        ((uint32_t)(j0 * H * kHeadDim) >> 4));
+                const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
+#pragma unroll
+                for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
+                    umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
+                umma_commit(&B.mma[g]);
+                mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
             }
             mma_phase ^= 1u;
             ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
             tc_fence_after_sync();
-            // a shared half goes to the other warpgroup once each of the four
-            // warps has read its lanes (one arrival per warp, no warpgroup
-            // barrier), before the tile's outputs; an arrival even after a
-            // failed wait keeps the phases in step
-            auto release = [&]() {
-                if constexpr (kShare) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&B.tfree[g & 1]);
-                }
-            };
-            // one outcome per warp: the tile body uses warp-wide votes
             if (__all_sync(kFullMask, ok)) {
                 const uint32_t wj0 = wsl + (uint32_t)(j0 * H * 4);
                 epi_dispatch<H, kRpp>(nr, all_pos, tacc, wj0, flip, mag, j0, out, release);
             } else {
-                release();
                 raise_abort(a, c);
             }
             if (p + 1 < npass) {  // the next pass reuses the columns
@@ -935,10 +992,13 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
                 tc_fence_after_sync();
             }
         }
+        }
         if constexpr (kShare)
             use += 2u;
         qs.pass_ends(a, smem, B, rc, c, count, w.step(rc, kGroups, count));
     }
+    if (pend_n)
+        pend.flush();
     cp_async_wait_all();
     qs.drain(B, QS);
 }
