@@ -21,12 +21,17 @@
 //   3. issue the copies of the warpgroup's next tile (block-table entries for
 //      the one after it are already in registers);
 //   4. one thread issues tcgen05.mma: D[token][(j,h)] = K_tile[128 x 128] *
-//      Q[(j,h) x 128]^T, fp8 e4m3 in, fp32 accumulators in the warpgroup's
-//      TMEM columns, at most 128 columns (whole draft rows) per pass;
+//      Q[(j,h) x 128]^T, fp8 e4m3 in, fp32 accumulators in TMEM: the
+//      warpgroup's own 128 columns up to next_n * H = 128; for up to 256
+//      columns a 256-column half that warpgroups g and g ^ 2 use in turn
+//      (each warp hands it on by an mbarrier arrival once it has read its
+//      lane); beyond that, passes of 128 columns (whole draft rows);
 //   5. each thread reads its lane of the accumulators (tcgen05.ld), forms
 //      sum_h w[j][h] * relu(x) per draft row, scales, masks, and writes full
 //      logits rows and/or the compact logits plus the per-row key histogram
-//      (global atomics) that the selection reads.
+//      (global atomics) that the selection reads. In a warpgroup's own
+//      columns these outputs wait in registers and are written while the
+//      next tile's MMA runs.
 // At the end of each request the four warpgroups meet at a CTA barrier and
 // thread 0 loads the query and weights of the request QS ahead into the slot
 // just freed (TMA). Every wait is bounded.
@@ -962,36 +967,39 @@ static __device__ void group_role(const MainArgs &a, uint8_t *smem, CtaCtl &c, i
                 raise_abort(a, c);
             }
         } else {
+            // passes of at most 128 columns (next_n * H above 256): each pass
+            // reuses the columns once all four warps have read the last
+            // (a warpgroup barrier), outputs at once
 #pragma unroll
-        for (int p = 0; p < npass; ++p) {
-            const int j0 = p * kRpp, nr = min(kRpp, NN - j0);
-            bool mma_ok = true;
-            if (elected) {
-                tc_fence_after_sync();
-                const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
-                                                        ((uint32_t)(j0 * H * kHeadDim) >> 4));
-                const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
+            for (int p = 0; p < npass; ++p) {
+                const int j0 = p * kRpp, nr = min(kRpp, NN - j0);
+                bool mma_ok = true;
+                if (elected) {
+                    tc_fence_after_sync();
+                    const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)q_slot * q_units +
+                                                            ((uint32_t)(j0 * H * kHeadDim) >> 4));
+                    const uint32_t idesc = idesc_e4m3_f32(128, nr * H);
 #pragma unroll
-                for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
-                    umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
-                umma_commit(&B.mma[g]);
-                mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
-            }
-            mma_phase ^= 1u;
-            ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
-            tc_fence_after_sync();
-            if (__all_sync(kFullMask, ok)) {
-                const uint32_t wj0 = wsl + (uint32_t)(j0 * H * 4);
-                epi_dispatch<H, kRpp>(nr, all_pos, tacc, wj0, flip, mag, j0, out, release);
-            } else {
-                raise_abort(a, c);
-            }
-            if (p + 1 < npass) {  // the next pass reuses the columns
-                tc_fence_before_sync();
-                named_bar_sync(wg_bar, 128);
+                    for (int k4 = 0; k4 < kHeadDim / 32; ++k4)
+                        umma_e4m3(dcol, adesc + 2u * k4, bd + 2u * k4, idesc, k4 > 0 ? 1u : 0u);
+                    umma_commit(&B.mma[g]);
+                    mma_ok = mbar_wait(&B.mma[g], mma_phase, &c.abort);
+                }
+                mma_phase ^= 1u;
+                ok = named_bar_and(wg_bar, 128, mma_ok) && ok;
                 tc_fence_after_sync();
+                if (__all_sync(kFullMask, ok)) {
+                    const uint32_t wj0 = wsl + (uint32_t)(j0 * H * 4);
+                    epi_dispatch<H, kRpp>(nr, all_pos, tacc, wj0, flip, mag, j0, out, release);
+                } else {
+                    raise_abort(a, c);
+                }
+                if (p + 1 < npass) {  // the next pass reuses the columns
+                    tc_fence_before_sync();
+                    named_bar_sync(wg_bar, 128);
+                    tc_fence_after_sync();
+                }
             }
-        }
         }
         if constexpr (kShare)
             use += 2u;
